@@ -1,0 +1,416 @@
+/*
+ * CPU fp64 oracle for single-query paged decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and
+ * the CPU-baseline leg of the benchmark load this file.  The library's product
+ * path never links, loads or calls it, and it shares no code, header, table or
+ * helper with the CUDA kernels.
+ *
+ * What it computes (plain definitions, no blocking or fusion):
+ *
+ *   MLA-as-MQA decode.  The cache row of a token is one latent vector
+ *   [kv_c (kv_lora_rank) | k_pe (rope)] of head_size D.  It is the key of every
+ *   query head, and its first R = kv_lora_rank columns are the value.
+ *     Sources: "Triton と MLA" page (vllm-arch-zh, ja/attention/triton-mla),
+ *     sections 役割 / 設計動機 (single KV channel, head_size 320 or 576) and
+ *     データフロー (the cache passed as a single-head K cache, V = its first
+ *     kv_lora_rank columns, k_scale passed as both scales).
+ *
+ *   Paged address translation: logical block = pos / page, physical block from
+ *   the request's block table, slot = physical block * page + pos % page.
+ *     Source: attention-kernel tutorial page (lshu.cn/news/265860), §11
+ *     "Paged KV Cache 如何参与计算".
+ *
+ *   Decode has no mask: the single query sits after every cached key.
+ *     Source: tutorial page §9.
+ *
+ *   Online softmax (running max m, sum l, accumulator acc, rescale factor
+ *   alpha = exp(m_old - m_new)).  Source: tutorial page §7.
+ *
+ *   Split-KV segments merged by m = max m_s, l = sum_s exp(m_s - m) l_s,
+ *   O = sum_s exp(m_s - m) O_s / l.  Source: tutorial page §12.
+ *
+ *   Number of KV splits: ceil(max_seq_len / 512) capped at 2 * sm_count, and 1
+ *   in batch-invariant mode.  Source: "Triton と MLA" page, 主要ファイル
+ *   (_compute_num_kv_splits) and データフロー (VLLM_BATCH_INVARIANT branch).
+ *
+ *   GQA paged decode over a [num_blocks, 2, page, num_kv_heads, head_size]
+ *   cache.  Source: "AttentionBackend" page (vllm-arch-zh, fr/attention/backend),
+ *   section "Motivation de conception" (FlashAttention cache layout).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - lse is the natural log of sum_t exp(s_t) of the SCALED logits s_t.
+ *   - bf16 caches ignore k_scale (the page's "is_fp8 check is a no-op").
+ *   - fp8 caches are OCP e4m3fn; value = k_scale * e4m3(code) for K and V.
+ *   - a sequence of length 0 gives out = 0 and lse = -inf.
+ *   - GQA query head h reads KV head h / (Hq / Hkv).
+ *   - split s of a sequence with n tokens covers the page-aligned token range
+ *     [s*L, min((s+1)*L, n)), L = ceil(ceil(n/page)/S) * page.
+ *
+ * Every public function returns 0 on success and -1 if a block-table entry that
+ * a valid token needs is outside [0, num_blocks) (nothing is read then).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_KV_BF16 = 0, ORACLE_KV_FP8_E4M3 = 1 };
+
+/* ---- element decoders --------------------------------------------------- */
+
+/* bf16 is the upper 16 bits of an IEEE-754 binary32; the value is exact. */
+double oracle_bf16_value(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* OCP 8-bit floating point, E4M3 ("fn": no infinities): 1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits.  Exponent field 0 is subnormal
+ * (m * 2^-9); exponent 15 with mantissa 7 is NaN; the largest finite value is
+ * 1.75 * 2^8 = 448. */
+double oracle_e4m3_value(uint8_t code) {
+    int sign = (code >> 7) & 1;
+    int e = (code >> 3) & 15;
+    int m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+void oracle_bf16_values(const uint16_t* bits, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_value(bits[i]);
+}
+
+void oracle_e4m3_values(const uint8_t* codes, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_value(codes[i]);
+}
+
+/* ---- host-side helpers named on the pages ------------------------------- */
+
+int oracle_num_kv_splits(int max_seq_len, int sm_count, int batch_invariant) {
+    if (batch_invariant) return 1;
+    long s = max_seq_len <= 0 ? 1 : ((long)max_seq_len + 511) / 512;
+    long cap = 2L * (long)sm_count;
+    if (cap >= 1 && s > cap) s = cap;
+    if (s < 1) s = 1;
+    return (int)s;
+}
+
+/* Slot of logical position pos of request req (tutorial page, §11). */
+int64_t oracle_physical_slot(const int32_t* block_table, int max_blocks, int req,
+                             int64_t pos, int page_size) {
+    int64_t logical_block = pos / page_size;
+    int64_t physical_block = block_table[(int64_t)req * max_blocks + logical_block];
+    return physical_block * page_size + pos % page_size;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ---- token access --------------------------------------------------------- */
+
+/* Describes where token t of request b keeps its key and value vectors. */
+typedef struct {
+    const void* kv;
+    int kv_dtype;
+    const int32_t* block_table;
+    int max_blocks, page, num_blocks;
+    /* element offsets of (physical slot 0, plane) and per-slot stride */
+    int64_t slot_stride;   /* elements between consecutive slots of one plane */
+    int64_t block_stride;  /* elements between consecutive physical blocks */
+    int64_t k_offset;      /* element offset of the key inside a slot */
+    int64_t v_offset;      /* element offset of the value inside a slot */
+    int dk, dv;            /* key and value lengths */
+    double k_mult, v_mult; /* dequantisation multipliers (1 for bf16) */
+} token_view;
+
+static double elem(const token_view* tv, int64_t idx) {
+    if (tv->kv_dtype == ORACLE_KV_BF16)
+        return oracle_bf16_value(((const uint16_t*)tv->kv)[idx]);
+    return oracle_e4m3_value(((const uint8_t*)tv->kv)[idx]);
+}
+
+/* Base element index of token t of request b, or -1 for a bad block id. */
+static int64_t token_base(const token_view* tv, int b, int64_t t) {
+    int64_t logical_block = t / tv->page;
+    int32_t blk = tv->block_table[(int64_t)b * tv->max_blocks + logical_block];
+    if (blk < 0 || blk >= tv->num_blocks) return -1;
+    return (int64_t)blk * tv->block_stride + (t % tv->page) * tv->slot_stride;
+}
+
+static int check_table(const token_view* tv, int b, int n) {
+    if (((int64_t)n + tv->page - 1) / tv->page > tv->max_blocks) return -1;
+    for (int64_t t = 0; t < n; t += tv->page)
+        if (token_base(tv, b, t) < 0) return -1;
+    return 0;
+}
+
+/* Scaled logit s_t = scale * sum_d q[d] * K_t[d]. */
+static double logit(const token_view* tv, const double* qd, int64_t base, double scale) {
+    double acc = 0.0;
+    for (int d = 0; d < tv->dk; ++d)
+        acc += qd[d] * (tv->k_mult * elem(tv, base + tv->k_offset + d));
+    return scale * acc;
+}
+
+/* ---- the three formulations ---------------------------------------------- */
+
+/* Direct definition: lse = log sum_t exp(s_t) (evaluated as m + log sum
+ * exp(s_t - m)), out = sum_t exp(s_t - lse) V_t. */
+static int attend_direct(const token_view* tv, int b, int n, const double* qd, double scale,
+                         double* out, double* lse) {
+    int dv = tv->dv;
+    for (int r = 0; r < dv; ++r) out[r] = 0.0;
+    if (n <= 0) {
+        *lse = -INFINITY;
+        return 0;
+    }
+    if (check_table(tv, b, n)) return -1;
+    double* s = (double*)malloc(sizeof(double) * (size_t)n);
+    double m = -INFINITY;
+    for (int t = 0; t < n; ++t) {
+        s[t] = logit(tv, qd, token_base(tv, b, t), scale);
+        if (s[t] > m) m = s[t];
+    }
+    double sum = 0.0;
+    for (int t = 0; t < n; ++t) sum += exp(s[t] - m);
+    double L = m + log(sum);
+    for (int t = 0; t < n; ++t) {
+        double w = exp(s[t] - L);
+        int64_t base = token_base(tv, b, t);
+        for (int r = 0; r < dv; ++r) out[r] += w * (tv->v_mult * elem(tv, base + tv->v_offset + r));
+    }
+    *lse = L;
+    free(s);
+    return 0;
+}
+
+/* Online softmax over consecutive tiles of `tile` tokens (tutorial page §7):
+ * m_new = max(m_old, rowmax S_tile); alpha = exp(m_old - m_new);
+ * l_new = alpha l_old + sum exp(S_tile - m_new);
+ * acc_new = alpha acc_old + exp(S_tile - m_new) V_tile;  out = acc / l. */
+static int attend_streaming(const token_view* tv, int b, int n, const double* qd, double scale,
+                            int tile, double* out, double* lse) {
+    int dv = tv->dv;
+    double* acc = (double*)calloc((size_t)dv, sizeof(double));
+    double* s = (double*)malloc(sizeof(double) * (size_t)(tile > 0 ? tile : 1));
+    double m = -INFINITY, l = 0.0;
+    if (n > 0 && check_table(tv, b, n)) {
+        free(acc);
+        free(s);
+        return -1;
+    }
+    for (int t0 = 0; t0 < n; t0 += tile) {
+        int t1 = t0 + tile < n ? t0 + tile : n;
+        double tile_max = -INFINITY;
+        for (int t = t0; t < t1; ++t) {
+            s[t - t0] = logit(tv, qd, token_base(tv, b, t), scale);
+            if (s[t - t0] > tile_max) tile_max = s[t - t0];
+        }
+        double m_new = m > tile_max ? m : tile_max;
+        double alpha = exp(m - m_new);
+        double psum = 0.0;
+        for (int r = 0; r < dv; ++r) acc[r] *= alpha;
+        for (int t = t0; t < t1; ++t) {
+            double p = exp(s[t - t0] - m_new);
+            int64_t base = token_base(tv, b, t);
+            psum += p;
+            for (int r = 0; r < dv; ++r) acc[r] += p * (tv->v_mult * elem(tv, base + tv->v_offset + r));
+        }
+        l = alpha * l + psum;
+        m = m_new;
+    }
+    for (int r = 0; r < dv; ++r) out[r] = l > 0.0 ? acc[r] / l : 0.0;
+    *lse = l > 0.0 ? m + log(l) : -INFINITY;
+    free(acc);
+    free(s);
+    return 0;
+}
+
+/* Split-KV: each segment keeps (m_s, l_s, O_s unnormalised); the segments are
+ * then merged with the tutorial page's §12 formulas.  Segment s covers the
+ * page-aligned token range [s*L, min((s+1)*L, n)) with
+ * L = ceil(ceil(n / page) / S) * page; segments past the end are empty
+ * (m_s = -inf, l_s = 0, O_s = 0) and get weight 0. */
+static int attend_split(const token_view* tv, int b, int n, const double* qd, double scale,
+                        int num_splits, double* out, double* lse) {
+    int dv = tv->dv, S = num_splits < 1 ? 1 : num_splits;
+    if (n > 0 && check_table(tv, b, n)) return -1;
+    double* ms = (double*)malloc(sizeof(double) * (size_t)S);
+    double* ls = (double*)malloc(sizeof(double) * (size_t)S);
+    double* Os = (double*)calloc((size_t)S * (size_t)dv, sizeof(double));
+    int64_t pages = ((int64_t)n + tv->page - 1) / tv->page;
+    int64_t L = ((pages + S - 1) / S) * tv->page;
+    for (int sp = 0; sp < S; ++sp) {
+        int64_t t0 = (int64_t)sp * L, t1 = t0 + L < n ? t0 + L : n;
+        double m = -INFINITY;
+        for (int64_t t = t0; t < t1; ++t) {
+            double st = logit(tv, qd, token_base(tv, b, t), scale);
+            if (st > m) m = st;
+        }
+        double l = 0.0;
+        for (int64_t t = t0; t < t1; ++t) {
+            int64_t base = token_base(tv, b, t);
+            double p = exp(logit(tv, qd, base, scale) - m);
+            l += p;
+            for (int r = 0; r < dv; ++r)
+                Os[(size_t)sp * dv + r] += p * (tv->v_mult * elem(tv, base + tv->v_offset + r));
+        }
+        ms[sp] = m;
+        ls[sp] = l;
+    }
+    double M = -INFINITY;
+    for (int sp = 0; sp < S; ++sp)
+        if (ms[sp] > M) M = ms[sp];
+    double Lsum = 0.0;
+    for (int r = 0; r < dv; ++r) out[r] = 0.0;
+    if (M == -INFINITY) {
+        *lse = -INFINITY;
+    } else {
+        for (int sp = 0; sp < S; ++sp) {
+            if (ls[sp] == 0.0) continue; /* empty segment: weight 0 */
+            double w = exp(ms[sp] - M);
+            Lsum += w * ls[sp];
+            for (int r = 0; r < dv; ++r) out[r] += w * Os[(size_t)sp * dv + r];
+        }
+        for (int r = 0; r < dv; ++r) out[r] /= Lsum;
+        *lse = M + log(Lsum);
+    }
+    free(ms);
+    free(ls);
+    free(Os);
+    return 0;
+}
+
+/* ---- MLA and GQA drivers --------------------------------------------------- */
+
+enum { FORM_DIRECT = 0, FORM_STREAMING = 1, FORM_SPLIT = 2 };
+
+static int run_heads(const token_view* tv, const uint16_t* q, const int32_t* seq_lens,
+                     double scale, int B, int Hq, int group, int dq, double* out, double* lse,
+                     int form, int param) {
+    int failed = 0;
+    int64_t pairs = (int64_t)B * Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int64_t bh = 0; bh < pairs; ++bh) {
+        int b = (int)(bh / Hq), h = (int)(bh % Hq);
+        (void)group;
+        double* qd = (double*)malloc(sizeof(double) * (size_t)dq);
+        for (int d = 0; d < dq; ++d) qd[d] = oracle_bf16_value(q[bh * dq + d]);
+        int n = seq_lens[b];
+        /* GQA: query head h reads KV head h / group (the view's k/v offsets
+         * are those of KV head 0; add the head's offset). */
+        token_view v = *tv;
+        int g = h / group;
+        v.k_offset += (int64_t)g * tv->dk;
+        v.v_offset += (int64_t)g * tv->dv;
+        double* o = out + bh * tv->dv;
+        int rc;
+        if (form == FORM_STREAMING)
+            rc = attend_streaming(&v, b, n, qd, scale, param, o, lse + bh);
+        else if (form == FORM_SPLIT)
+            rc = attend_split(&v, b, n, qd, scale, param, o, lse + bh);
+        else
+            rc = attend_direct(&v, b, n, qd, scale, o, lse + bh);
+        failed |= (rc != 0);
+        free(qd);
+    }
+    return failed ? -1 : 0;
+}
+
+static token_view mla_view(const void* kv, int kv_dtype, const int32_t* block_table, double k_scale,
+                           int D, int R, int num_blocks, int P, int max_blocks) {
+    token_view tv;
+    tv.kv = kv;
+    tv.kv_dtype = kv_dtype;
+    tv.block_table = block_table;
+    tv.max_blocks = max_blocks;
+    tv.page = P;
+    tv.num_blocks = num_blocks;
+    tv.slot_stride = D;
+    tv.block_stride = (int64_t)P * D;
+    tv.k_offset = 0;
+    tv.v_offset = 0; /* V is the first R columns of the same row */
+    tv.dk = D;
+    tv.dv = R;
+    tv.k_mult = kv_dtype == ORACLE_KV_FP8_E4M3 ? k_scale : 1.0;
+    tv.v_mult = tv.k_mult; /* v_scale = k_scale for MLA */
+    return tv;
+}
+
+/* q: bf16 bits [B, H, D]; kv: [num_blocks, P, D] bf16 bits or e4m3 codes;
+ * out: [B, H, R]; lse: [B, H]. */
+int oracle_mla_decode(const uint16_t* q, const void* kv, int kv_dtype, const int32_t* block_table,
+                      const int32_t* seq_lens, double scale, double k_scale, double* out,
+                      double* lse, int B, int H, int D, int R, int num_blocks, int P,
+                      int max_blocks) {
+    token_view tv = mla_view(kv, kv_dtype, block_table, k_scale, D, R, num_blocks, P, max_blocks);
+    tv.dk = D; /* the whole latent row is the key */
+    return run_heads(&tv, q, seq_lens, scale, B, H, H /* one KV head */, D, out, lse,
+                     FORM_DIRECT, 0);
+}
+
+int oracle_mla_decode_streaming(const uint16_t* q, const void* kv, int kv_dtype,
+                                const int32_t* block_table, const int32_t* seq_lens, double scale,
+                                double k_scale, double* out, double* lse, int B, int H, int D,
+                                int R, int num_blocks, int P, int max_blocks, int tile) {
+    token_view tv = mla_view(kv, kv_dtype, block_table, k_scale, D, R, num_blocks, P, max_blocks);
+    return run_heads(&tv, q, seq_lens, scale, B, H, H, D, out, lse, FORM_STREAMING,
+                     tile < 1 ? 1 : tile);
+}
+
+int oracle_mla_decode_split(const uint16_t* q, const void* kv, int kv_dtype,
+                            const int32_t* block_table, const int32_t* seq_lens, double scale,
+                            double k_scale, double* out, double* lse, int B, int H, int D, int R,
+                            int num_blocks, int P, int max_blocks, int num_splits) {
+    token_view tv = mla_view(kv, kv_dtype, block_table, k_scale, D, R, num_blocks, P, max_blocks);
+    return run_heads(&tv, q, seq_lens, scale, B, H, H, D, out, lse, FORM_SPLIT, num_splits);
+}
+
+/* q: bf16 bits [B, Hq, D]; kv: [num_blocks, 2, P, Hkv, D] (plane 0 = K,
+ * plane 1 = V); out: [B, Hq, D]; lse: [B, Hq]. */
+int oracle_gqa_paged_decode(const uint16_t* q, const void* kv, int kv_dtype,
+                            const int32_t* block_table, const int32_t* seq_lens, double scale,
+                            double k_scale, double v_scale, double* out, double* lse, int B,
+                            int Hq, int Hkv, int D, int num_blocks, int P, int max_blocks) {
+    if (Hkv <= 0 || Hq % Hkv != 0) return -1;
+    token_view tv;
+    tv.kv = kv;
+    tv.kv_dtype = kv_dtype;
+    tv.block_table = block_table;
+    tv.max_blocks = max_blocks;
+    tv.page = P;
+    tv.num_blocks = num_blocks;
+    tv.slot_stride = (int64_t)Hkv * D;
+    tv.block_stride = 2LL * P * Hkv * D;
+    tv.k_offset = 0;
+    tv.v_offset = (int64_t)P * Hkv * D; /* plane 1 */
+    tv.dk = D;
+    tv.dv = D;
+    tv.k_mult = kv_dtype == ORACLE_KV_FP8_E4M3 ? k_scale : 1.0;
+    tv.v_mult = kv_dtype == ORACLE_KV_FP8_E4M3 ? v_scale : 1.0;
+    return run_heads(&tv, q, seq_lens, scale, B, Hq, Hq / Hkv, D, out, lse, FORM_DIRECT, 0);
+}
