@@ -1,0 +1,415 @@
+"""Benchmark: paged MLA/GQA decode on GB300 through the C ABI.
+
+One step = one decode call (split-KV stage 1 + LSE merge) over one batch of the
+chosen workload, inputs resident in HBM.  Default workload: the MLA
+V2-Lite-like batch (B=64, H=16, head 576 = 512 + 64, bf16, seq_lens uniform in
+[1024, 8192], page 64, random block permutation over a 1.5x pool).
+
+Prints ONE JSON line (rank 0).  `value` is KV GB/s (algorithmic KV bytes of the
+valid tokens / device time, summed over ranks); `ms_per_step` gives the
+per-call latency; `roofline` compares the decode call against the measured HBM
+or bf16 tensor peak; `e2e` is the same metric with the per-step host<->device
+copies (query, block table and lengths in; output and lse out) inside the
+timed region; `cpu_baseline` times the fp64 CPU oracle on the host cores.
+
+Timing: W untimed warm-up steps, then K steps.  Before every step a 256 MiB
+buffer (> the 129 MB L2) is overwritten so no KV line is L2-resident; each
+step is bracketed by CUDA events on the launching stream (the flush is outside
+the events).  Under torchrun every rank runs an independent replica (the path
+has no cross-GPU exchange), the timed region is bracketed by a barrier and
+synchronize on both sides, and rank 0 reports the max over ranks.
+
+`--impl reference` times the CPU oracle instead (no GPU work), on the same
+workload, with a bounded sample of requests per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode µs/call, KV GB/s and % of roofline at B×H×seq_len (1 GB300)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per decode call
+# from one ncu capture, keyed by workload; valid only while the kernel sources
+# hash to `src_sha`.
+NCU_TRAFFIC = {}
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "mqa_decode_attention_paged_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        with open(os.path.join(d, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_stats(case, splits):
+    """Algorithmic bytes and flops of one decode call."""
+    tokens = int(case.seq_lens.astype(np.int64).sum())
+    elt = 2 if case.kv_dtype == "bf16" else 1
+    B, H, D = case.q.shape
+    if case.kind == "mla":
+        R = case.kv_lora_rank
+        kv_bytes = tokens * D * elt
+        flops = 2.0 * H * tokens * (D + R)
+        out_w = R
+    else:
+        Hkv = case.num_kv_heads
+        kv_bytes = tokens * 2 * Hkv * D * elt
+        flops = 2.0 * H * tokens * 2 * D
+        out_w = D
+    io_bytes = B * H * D * 2 + B * H * out_w * 2 + B * H * 4
+    return dict(tokens=tokens, kv_bytes=kv_bytes, alg_bytes=kv_bytes + io_bytes, flops=flops,
+                q_bytes=B * H * D * 2, out_bytes=B * H * out_w * 2, lse_bytes=B * H * 4)
+
+
+def workload_config(case, name, splits):
+    spec = __import__("mqa_decode_attention_paged_gb300.synth", fromlist=["WORKLOADS"]).WORKLOADS[name]
+    cfg = {"workload": name, "kind": case.kind, "batch": case.batch, "num_heads": case.num_heads,
+           "head_size": case.head_size, "page_size": case.page, "kv_dtype": case.kv_dtype,
+           "seq_lens": spec["seq_lens"] if not isinstance(spec["seq_lens"], tuple) else list(spec["seq_lens"]),
+           "total_tokens": int(case.seq_lens.astype(np.int64).sum()),
+           "num_kv_splits": splits, "seed": spec["seed"],
+           "l2": "flushed before every timed step (256 MiB write, outside the timed events)"}
+    if case.kind == "mla":
+        cfg["kv_lora_rank"] = case.kv_lora_rank
+    else:
+        cfg["num_kv_heads"] = case.num_kv_heads
+    return cfg
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def time_oracle(case, budget_s=12.0, min_reps=1):
+    """Time the fp64 oracle on bounded request samples; returns (GB/s, cores, sample text)."""
+    import oracle
+    from mqa_decode_attention_paged_gb300 import synth
+    cores = oracle.max_threads()
+    rng = np.random.default_rng(0)
+    order = rng.permutation(case.batch)
+    stats_full = workload_stats(case, 1)
+    per_tok = stats_full["kv_bytes"] / max(stats_full["tokens"], 1)
+    done_tokens, elapsed, reps, rows_used = 0, 0.0, 0, 0
+    n = 1
+    while elapsed < budget_s and rows_used < case.batch:
+        rows = order[rows_used:rows_used + n]
+        sub = synth.replace(case, q=case.q[rows], block_table=case.block_table[rows],
+                            seq_lens=case.seq_lens[rows])
+        t0 = time.perf_counter()
+        if case.kind == "mla":
+            oracle.mla_decode(sub.q, sub.kv, sub.kv_dtype, sub.block_table, sub.seq_lens, sub.scale,
+                              k_scale=sub.k_scale, kv_lora_rank=sub.kv_lora_rank)
+        else:
+            oracle.gqa_paged_decode(sub.q, sub.kv, sub.kv_dtype, sub.block_table, sub.seq_lens,
+                                    sub.scale, k_scale=sub.k_scale, v_scale=sub.v_scale)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        done_tokens += int(sub.seq_lens.astype(np.int64).sum())
+        rows_used += len(rows)
+        reps += 1
+        n = min(case.batch - rows_used, max(1, len(rows) * 2))
+        if n <= 0:
+            break
+    gbs = done_tokens * per_tok / elapsed / 1e9
+    sample = (f"{rows_used} of {case.batch} requests (all heads, {done_tokens} tokens) in {elapsed:.1f} s "
+              f"of fp64 oracle work on {cores} host threads")
+    return gbs, cores, sample, elapsed, done_tokens
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from mqa_decode_attention_paged_gb300 import synth
+    case = synth.workload(args.workload)
+    splits = args.splits or 1
+    st = workload_stats(case, splits)
+    times = []
+    tokens = 0
+    total_gb = 0.0
+    # each step is a bounded sample so that the whole run stays within minutes
+    budget = max(0.05, min(args.ref_budget, 150.0 / (args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        gbs, cores, sample, elapsed, tok = time_oracle(case, budget_s=budget)
+        if i >= args.warmup:
+            times.append(elapsed)
+            tokens += tok
+            total_gb += gbs
+    value = total_gb / max(len(times), 1)
+    per_tok_ms = 1e3 * sum(times) / max(tokens, 1)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per_tok_ms * st["tokens"], 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(case, args.workload, splits),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample + " per step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from mqa_decode_attention_paged_gb300 import _binding as mqa
+    from mqa_decode_attention_paged_gb300 import synth
+
+    case = synth.workload(args.workload)
+    st = workload_stats(case, 1)
+    sms = mqa.device_sm_count()
+    splits = args.splits or mqa.num_kv_splits(int(case.seq_lens.max()), sms, False)
+
+    # inputs resident in HBM
+    q = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    if case.kv_dtype == "bf16":
+        kv = torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).to(dev)
+    else:
+        kv = torch.from_numpy(case.kv).view(torch.float8_e4m3fn).to(dev)
+    bt = torch.from_numpy(case.block_table).to(dev)
+    sl = torch.from_numpy(case.seq_lens).to(dev)
+    B, H, D = q.shape
+    R = case.kv_lora_rank if case.kind == "mla" else D
+    out = torch.empty((B, H, R), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+    if case.kind == "mla":
+        need = mqa.mla_decode_workspace_bytes(B, H, R, splits)
+    else:
+        need = mqa.gqa_paged_decode_workspace_bytes(B, H, D, splits)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_call = 1 if splits == 1 else 2
+
+    def call(qq=q, btt=bt, sll=sl, oo=out, ll=lse):
+        if case.kind == "mla":
+            mqa.mla_decode(qq, kv, btt, sll, case.scale, case.k_scale, out=oo, lse=ll,
+                           num_kv_splits=splits, workspace=ws, kv_lora_rank=R, stream=stream)
+        else:
+            mqa.gqa_paged_decode(qq, kv, btt, sll, case.scale, case.k_scale, case.v_scale, out=oo,
+                                 lse=ll, num_kv_splits=splits, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    with sampler:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_ms = sum(step_ms) / len(step_ms)
+
+    # ---- end to end: host buffers, copies inside the timed region
+    q_h = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    bt_h = torch.from_numpy(case.block_table).pin_memory()
+    sl_h = torch.from_numpy(case.seq_lens).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d, bt_d, sl_d = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(sl)
+    e2e_steps = max(3, min(args.steps, 200))
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        flush.fill_(i & 0xFF)
+        j = i - 2
+        if j >= 0:
+            es[j].record(stream)
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        call(q_d, bt_d, sl_d, out, lse)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        if j >= 0:
+            ee[j].record(stream)
+        stream.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e2e_steps
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    # ---- max over ranks
+    t = torch.tensor([mean_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    mean_ms, e2e_ms = float(t[0]), float(t[1])
+
+    peaks, peak_src = load_peaks()
+    kv_gbs = world * st["kv_bytes"] / (mean_ms * 1e-3) / 1e9
+    alg_gbs = st["alg_bytes"] / (mean_ms * 1e-3) / 1e9
+    tflops = st["flops"] / (mean_ms * 1e-3) / 1e12
+    t_hbm = st["alg_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_tc = st["flops"] / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    traffic = None
+    tr = NCU_TRAFFIC.get(args.workload)
+    if tr and tr.get("src_sha") == kernel_sources_sha() and tr.get("splits") == splits:
+        traffic = tr["bytes"]
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(alg_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(alg_gbs / peaks["hbm_gbs"], 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops"], 4)}
+    roof["traffic"] = traffic
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["kernel"] = "decode call: split-KV stage-1 kernel + LSE merge"
+    roof["alg_bytes_per_call"] = st["alg_bytes"]
+    roof["alg_flops_per_call"] = st["flops"]
+    roof["ideal_us"] = round(1e6 * max(t_hbm, t_tc), 2)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        gbs, cores, sample, _, _ = time_oracle(case, budget_s=args.ref_budget)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": METRIC, "value": round(kv_gbs, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
+        "us_per_call": round(mean_ms * 1e3, 2), "tflops": round(tflops, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if case.kv_dtype == "bf16" else "bf16 (fp8-e4m3 KV)",
+        "data": "synthetic (seeded N(0,1) q/KV, random block permutation)",
+        "config": workload_config(case, args.workload, splits),
+        "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": round(world * st["kv_bytes"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "per step: q, block_table, seq_lens host->device and out, lse device->host "
+                        "(pinned host buffers); the KV cache is decode state resident in HBM"},
+        "gpu_launches": args.steps * launches_per_call,
+        "clocks": sampler.summary(),
+        "kernel_src_sha": kernel_sources_sha(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mla_v2lite")
+    ap.add_argument("--splits", type=int, default=0, help="num_kv_splits (0 = heuristic)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+/*
+ * mqa_decode.h — C ABI of the GB300 (sm_103a) paged decode-attention library.
+ *
+ * One query token per request attends to that request's paged KV cache.  Two
+ * cache formats are served:
+ *
+ *   MLA (primary).  The cache row of a token is one latent vector
+ *   [kv_c (kv_lora_rank) | k_pe (64 rope dims)], head_size 576 or 320.  That
+ *   row is the key of EVERY query head, and its first kv_lora_rank columns are
+ *   the value ("Triton と MLA" page, vllm-arch-zh ja/attention/triton-mla:
+ *   sections 設計動機 and データフロー, where forward_mqa hands the cache to the
+ *   decode kernel as a single-head K cache and its first kv_lora_rank columns
+ *   as V).
+ *
+ *   GQA (secondary).  Standard paged attention over a
+ *   [num_blocks, 2, page, num_kv_heads, head_size] cache ("AttentionBackend"
+ *   page, vllm-arch-zh fr/attention/backend: section "Motivation de
+ *   conception", the FlashAttention layout).
+ *
+ * For request b and query head h the library returns
+ *   s_t      = scale * <q[b,h,:], K_t>                  for t < seq_lens[b]
+ *   lse[b,h] = ln sum_t exp(s_t)                        (natural log, fp32)
+ *   out[b,h] = sum_t exp(s_t - lse[b,h]) * V_t          (bf16)
+ * where token t lives in physical block block_table[b][t / page] at slot
+ * t % page (attention-kernel tutorial page, lshu.cn/news/265860, §11), there is
+ * no mask inside [0, seq_lens[b]) (same page, §9), and a sequence of length 0
+ * yields out = 0, lse = -inf.
+ *
+ * The work on one sequence may be cut into KV segments that run on separate
+ * thread blocks; their partial results are merged by LogSumExp
+ * (m = max_s m_s, l = sum_s e^{m_s-m} l_s, O = sum_s e^{m_s-m} O_s / l; same
+ * page, §12).  num_kv_splits bounds how many segment partials per request the
+ * caller's workspace holds, exactly as the workspace shape
+ * [B, H, num_kv_splits, kv_lora_rank + 1] fp32 of the Triton MLA backend does
+ * ("Triton と MLA" page, データフロー).  num_kv_splits == 1 processes every
+ * request in one thread block in a fixed order: the result is bitwise
+ * reproducible and independent of the other requests in the batch
+ * (batch-invariant mode, same section).
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers to caller-owned, contiguous,
+ *     row-major memory on the current CUDA device, 16-byte aligned.
+ *   - The library allocates nothing, never synchronises the stream and keeps
+ *     no per-call state: a call only enqueues kernels on `stream`
+ *     (a cudaStream_t; NULL = legacy default stream).
+ *   - Argument errors are returned before anything is enqueued.  A launch
+ *     failure returns MQA_ERR_CUDA.  Conditions found on the device (a block
+ *     id outside [0, num_blocks), seq_len < 0 or > max_blocks * page, a wait
+ *     that exceeded its time limit) are written into *device_status (an int in
+ *     device memory that the caller zeroes; the kernels only raise it to the
+ *     matching mqa_status code) and the offending page is treated as empty.
+ */
+#ifndef MQA_DECODE_H
+#define MQA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MQA_ABI_VERSION 1
+
+typedef enum mqa_status {
+    MQA_OK = 0,
+    MQA_ERR_INVALID_ARG = 1,         /* null/unaligned pointer, bad size or count */
+    MQA_ERR_UNSUPPORTED = 2,         /* shape or dtype the library does not serve */
+    MQA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below the *_workspace_bytes value */
+    MQA_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
+    MQA_ERR_DEVICE_CHECK = 5,        /* device-side: bad block id or sequence length */
+    MQA_ERR_DEVICE_TIMEOUT = 6       /* device-side: a bounded wait expired */
+} mqa_status;
+
+typedef enum mqa_kv_dtype {
+    MQA_KV_BF16 = 0,     /* bfloat16 cache; k_scale / v_scale are ignored */
+    MQA_KV_FP8_E4M3 = 1  /* OCP e4m3fn cache; element value = scale * e4m3(code) */
+} mqa_kv_dtype;
+
+/* ABI version of the loaded library (MQA_ABI_VERSION at build time). */
+int mqa_abi_version(void);
+
+/* Static, NUL-terminated description of a status code. */
+const char* mqa_status_string(int status);
+
+/* Number of streaming multiprocessors of the current device, or -1. */
+int mqa_device_sm_count(void);
+
+/* Split-count heuristic of the Triton MLA backend ("Triton と MLA" page,
+ * 主要ファイル: _compute_num_kv_splits, and データフロー: the
+ * VLLM_BATCH_INVARIANT branch): ceil(max_seq_len / 512), at least 1, at most
+ * 2 * sm_count; 1 when batch_invariant is non-zero.  Host-only, pure. */
+int mqa_num_kv_splits(int max_seq_len, int sm_count, int batch_invariant);
+
+/* Workspace bytes mla_decode needs: batch * num_heads * num_kv_splits *
+ * (kv_lora_rank + 1) * 4, i.e. the fp32 [B, H, S, R + 1] partial buffer of the
+ * Triton MLA backend ("Triton と MLA" page, データフロー).  0 when
+ * num_kv_splits == 1 (no partials are kept).  0 on invalid arguments. */
+size_t mla_decode_workspace_bytes(int batch, int num_heads, int kv_lora_rank, int num_kv_splits);
+
+/* Workspace bytes gqa_paged_decode needs: batch * num_q_heads * num_kv_splits *
+ * (head_size + 1) * 4; 0 when num_kv_splits == 1. */
+size_t gqa_paged_decode_workspace_bytes(int batch, int num_q_heads, int head_size,
+                                        int num_kv_splits);
+
+/* MLA decode (the MQA view of MLA: forward_mqa, "Triton と MLA" page,
+ * データフロー).
+ *
+ *   q            bf16 [batch, num_heads, head_size]: the absorbed query
+ *                (q_nope absorbed ‖ q_pe) already concatenated.
+ *   kv_cache     [num_blocks, page_size, head_size], bf16 or e4m3 codes
+ *                (kv_dtype).  Row layout [kv_c (kv_lora_rank) | k_pe].
+ *   block_table  int32 [batch, max_blocks]: physical block of each logical
+ *                block.  Only entries below ceil(seq_lens[b] / page_size) are
+ *                read.
+ *   seq_lens     int32 [batch]: KV length of each request.
+ *   scale        softmax scale applied to q.K.
+ *   k_scale      fp8 dequantisation scale (used for K and V); ignored for bf16.
+ *   out          bf16 [batch, num_heads, kv_lora_rank], fully written.
+ *   lse          fp32 [batch, num_heads] natural-log LSE of the scaled logits,
+ *                or NULL.  (fp32 rather than the query dtype: a bf16 lse cannot
+ *                carry the 1e-3 accuracy the merge across shards needs.)
+ *   head_size / kv_lora_rank must be 576/512 or 320/256 ("Triton と MLA" page,
+ *   境界と失敗: head sizes 320 and 576 only).  page_size must be a multiple of
+ *   16 ("AttentionBackend" page, "Limites et échecs": MultipleOf(16)).
+ *   num_heads in [1, 128]; batch >= 1; max_blocks >= 1; num_blocks >= 1.
+ *   num_kv_splits >= 1: the per-request partial budget (see the file header);
+ *   workspace / workspace_bytes: caller scratch of at least
+ *   mla_decode_workspace_bytes(...) bytes (may be NULL when that is 0).
+ *   device_status: device int or NULL (see the file header).
+ */
+mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                      int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
+                      int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
+                      void* workspace, size_t workspace_bytes, int* device_status, void* stream);
+
+/* GQA paged decode (TritonAttentionImpl.forward's paged_attention path,
+ * "Triton と MLA" page, 主要ファイル; cache layout from the "AttentionBackend"
+ * page, "Motivation de conception").
+ *
+ *   q            bf16 [batch, num_q_heads, head_size]
+ *   kv_cache     [num_blocks, 2, page_size, num_kv_heads, head_size]; plane 0
+ *                holds K, plane 1 holds V.  bf16 only in this version.
+ *   out          bf16 [batch, num_q_heads, head_size]; lse fp32 [batch,
+ *                num_q_heads] or NULL.
+ *   Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   head_size in {64, 128}; num_kv_heads in [1, 8]; num_q_heads a multiple of
+ *   num_kv_heads with at most 16 query heads per KV head; page_size a multiple
+ *   of 16.  Other arguments as for mla_decode.
+ */
+mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, float scale, float k_scale, float v_scale,
+                            void* out, float* lse, int batch, int num_q_heads, int num_kv_heads,
+                            int head_size, int num_blocks, int page_size, int max_blocks,
+                            mqa_kv_dtype kv_dtype, int num_kv_splits, void* workspace,
+                            size_t workspace_bytes, int* device_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQA_DECODE_H */

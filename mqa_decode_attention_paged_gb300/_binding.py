@@ -1,0 +1,166 @@
+"""ctypes binding of ``libmqa_decode.so`` (the C ABI declared in include/mqa_decode.h).
+
+Argument marshalling only: every step of the decode runs in the library's
+CUDA kernels.  torch supplies device memory and the current stream.  When the
+shared library is missing this module raises at import time instead of falling
+back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_WORKSPACE_TOO_SMALL = 3
+ERR_CUDA = 4
+ERR_DEVICE_CHECK = 5
+ERR_DEVICE_TIMEOUT = 6
+
+KV_BF16 = 0
+KV_FP8_E4M3 = 1
+
+LIB_PATH = _build.LIB_PATH
+
+
+class MqaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it first with `python -m mqa_decode_attention_paged_gb300.build` "
+            "(requires nvcc); there is no fallback implementation")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.mqa_abi_version.restype = I
+    lib.mqa_abi_version.argtypes = []
+    lib.mqa_status_string.restype = ctypes.c_char_p
+    lib.mqa_status_string.argtypes = [I]
+    lib.mqa_device_sm_count.restype = I
+    lib.mqa_device_sm_count.argtypes = []
+    lib.mqa_num_kv_splits.restype = I
+    lib.mqa_num_kv_splits.argtypes = [I, I, I]
+    lib.mla_decode_workspace_bytes.restype = SZ
+    lib.mla_decode_workspace_bytes.argtypes = [I, I, I, I]
+    lib.gqa_paged_decode_workspace_bytes.restype = SZ
+    lib.gqa_paged_decode_workspace_bytes.argtypes = [I, I, I, I]
+    lib.mla_decode.restype = I
+    lib.mla_decode.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
+    lib.gqa_paged_decode.restype = I
+    lib.gqa_paged_decode.argtypes = [P, P, P, P, F, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
+    return lib
+
+
+lib = _load()
+
+
+def abi_version() -> int:
+    return int(lib.mqa_abi_version())
+
+
+def status_string(code: int) -> str:
+    return lib.mqa_status_string(int(code)).decode()
+
+
+def device_sm_count() -> int:
+    return int(lib.mqa_device_sm_count())
+
+
+def num_kv_splits(max_seq_len: int, sm_count: int, batch_invariant: bool = False) -> int:
+    return int(lib.mqa_num_kv_splits(int(max_seq_len), int(sm_count), int(bool(batch_invariant))))
+
+
+def mla_decode_workspace_bytes(batch: int, num_heads: int, kv_lora_rank: int, num_kv_splits: int) -> int:
+    return int(lib.mla_decode_workspace_bytes(batch, num_heads, kv_lora_rank, num_kv_splits))
+
+
+def gqa_paged_decode_workspace_bytes(batch: int, num_q_heads: int, head_size: int, num_kv_splits: int) -> int:
+    return int(lib.gqa_paged_decode_workspace_bytes(batch, num_q_heads, head_size, num_kv_splits))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _kv_code(kv_cache, kv_dtype):
+    import torch
+    if kv_dtype is not None:
+        return {"bf16": KV_BF16, "fp8_e4m3": KV_FP8_E4M3}[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+    if kv_cache.dtype == torch.bfloat16:
+        return KV_BF16
+    if kv_cache.dtype == torch.float8_e4m3fn:
+        return KV_FP8_E4M3
+    raise TypeError("kv_cache must be bf16 or float8_e4m3fn (or pass kv_dtype with uint8 storage)")
+
+
+def mla_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *, out=None, lse=None,
+               num_kv_splits=1, workspace=None, kv_lora_rank=None, kv_dtype=None,
+               device_status=None, stream=None, return_lse=True):
+    """MLA decode through the C ABI.  q [B,H,D] bf16, kv_cache [num_blocks, page, D],
+    block_table [B, max_blocks] int32, seq_lens [B] int32 (all on one CUDA device).
+    Allocates out / lse / workspace with torch when they are not given."""
+    import torch
+    B, H, D = q.shape
+    nb, page, D2 = kv_cache.shape
+    if D2 != D:
+        raise ValueError("q and kv_cache head sizes differ")
+    R = (D - 64) if kv_lora_rank is None else int(kv_lora_rank)
+    code = _kv_code(kv_cache, kv_dtype)
+    if out is None:
+        out = torch.empty((B, H, R), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    need = mla_decode_workspace_bytes(B, H, R, num_kv_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.mla_decode(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), float(scale),
+                        float(k_scale), _ptr(out), _ptr(lse), B, H, D, R, nb, page,
+                        block_table.shape[1], code, int(num_kv_splits), _ptr(workspace), ws_bytes,
+                        _ptr(device_status), _stream(stream))
+    if rc != OK:
+        raise MqaError(rc, "mla_decode")
+    return out, lse
+
+
+def gqa_paged_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, v_scale=1.0, *,
+                     out=None, lse=None, num_kv_splits=1, workspace=None, kv_dtype=None,
+                     device_status=None, stream=None, return_lse=True):
+    """GQA paged decode through the C ABI.  q [B,Hq,D] bf16, kv_cache
+    [num_blocks, 2, page, Hkv, D] bf16."""
+    import torch
+    B, Hq, D = q.shape
+    nb, two, page, Hkv, D2 = kv_cache.shape
+    if two != 2 or D2 != D:
+        raise ValueError("kv_cache must be [num_blocks, 2, page, num_kv_heads, head_size]")
+    code = _kv_code(kv_cache, kv_dtype)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = gqa_paged_decode_workspace_bytes(B, Hq, D, num_kv_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.gqa_paged_decode(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+                              float(scale), float(k_scale), float(v_scale), _ptr(out), _ptr(lse),
+                              B, Hq, Hkv, D, nb, page, block_table.shape[1], code,
+                              int(num_kv_splits), _ptr(workspace), ws_bytes, _ptr(device_status),
+                              _stream(stream))
+    if rc != OK:
+        raise MqaError(rc, "gqa_paged_decode")
+    return out, lse

@@ -1,0 +1,222 @@
+// C ABI entry points: argument validation, work decomposition and launches.
+// See include/mqa_decode.h for the contract of every function.
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+#include "plan.cuh"
+
+#include "args.cuh"
+
+namespace {
+
+constexpr int kMaxBatch = 8192;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int sm_count_current() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return n;
+}
+
+size_t partial_bytes(int batch, int heads, int width, int splits) {
+    if (batch <= 0 || heads <= 0 || width <= 0 || splits <= 0) return 0;
+    if (splits == 1) return 0;
+    return static_cast<size_t>(batch) * heads * splits * (static_cast<size_t>(width) + 1) * 4;
+}
+
+// Work units for balanced mode: about `resident` thread blocks per head
+// group, never more than the workspace's partial budget allows.
+int balanced_units(int batch, int splits, int resident_per_group) {
+    long long cap = static_cast<long long>(batch) * (splits - 1) + 1;
+    long long u = resident_per_group < 1 ? 1 : resident_per_group;
+    return static_cast<int>(u < cap ? u : cap);
+}
+
+}  // namespace
+
+extern "C" {
+
+int mqa_abi_version(void) { return MQA_ABI_VERSION; }
+
+const char* mqa_status_string(int status) {
+    switch (status) {
+        case MQA_OK: return "ok";
+        case MQA_ERR_INVALID_ARG: return "invalid argument";
+        case MQA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case MQA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MQA_ERR_CUDA: return "CUDA error";
+        case MQA_ERR_DEVICE_CHECK: return "device check failed (block id or sequence length)";
+        case MQA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int mqa_device_sm_count(void) { return sm_count_current(); }
+
+int mqa_num_kv_splits(int max_seq_len, int sm_count, int batch_invariant) {
+    if (batch_invariant) return 1;
+    long long s = max_seq_len <= 0 ? 1 : (static_cast<long long>(max_seq_len) + 511) / 512;
+    const long long cap = 2LL * sm_count;
+    if (cap >= 1 && s > cap) s = cap;
+    if (s < 1) s = 1;
+    return static_cast<int>(s);
+}
+
+size_t mla_decode_workspace_bytes(int batch, int num_heads, int kv_lora_rank, int num_kv_splits) {
+    return partial_bytes(batch, num_heads, kv_lora_rank, num_kv_splits);
+}
+
+size_t gqa_paged_decode_workspace_bytes(int batch, int num_q_heads, int head_size, int num_kv_splits) {
+    return partial_bytes(batch, num_q_heads, head_size, num_kv_splits);
+}
+
+mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                      int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
+                      int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
+                      void* workspace, size_t workspace_bytes, int* device_status, void* stream) {
+    if (!q || !kv_cache || !block_table || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (device_status && !aligned(device_status, 4)))
+        return MQA_ERR_INVALID_ARG;
+    if (batch < 1 || num_heads < 1 || num_blocks < 1 || max_blocks < 1 || page_size < 1 || num_kv_splits < 1)
+        return MQA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !std::isfinite(k_scale)) return MQA_ERR_INVALID_ARG;
+    if (!((head_size == 576 && kv_lora_rank == 512) || (head_size == 320 && kv_lora_rank == 256)))
+        return MQA_ERR_UNSUPPORTED;
+    if (page_size % 16 != 0) return MQA_ERR_UNSUPPORTED;
+    if (kv_dtype != MQA_KV_BF16 && kv_dtype != MQA_KV_FP8_E4M3) return MQA_ERR_UNSUPPORTED;
+    if (num_heads > 128 || batch > kMaxBatch) return MQA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(max_blocks) * page_size > INT32_MAX ||
+        static_cast<long long>(num_blocks) * page_size > INT32_MAX)
+        return MQA_ERR_UNSUPPORTED;
+
+    const size_t need = mla_decode_workspace_bytes(batch, num_heads, kv_lora_rank, num_kv_splits);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return MQA_ERR_WORKSPACE_TOO_SMALL;
+    if (need > 0 && !aligned(workspace, 16)) return MQA_ERR_INVALID_ARG;
+
+    const int sms = sm_count_current();
+    if (sms < 1) return MQA_ERR_CUDA;
+    const bool fp8 = kv_dtype == MQA_KV_FP8_E4M3;
+    const int groups = (num_heads + 15) / 16;
+
+    mqa::MlaArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.kv = static_cast<const uint8_t*>(kv_cache);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    const size_t slots = static_cast<size_t>(batch) * num_kv_splits;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = need > 0 ? a.ws_o + slots * num_heads * kv_lora_rank : nullptr;
+    a.status = device_status;
+    const float ks = fp8 ? k_scale : 1.0f;
+    a.sl2 = scale * ks * mqa::kLog2e;
+    a.out_scale = ks;
+    a.H = num_heads;
+    a.num_blocks = num_blocks;
+    a.plan.batch = batch;
+    a.plan.page = page_size;
+    a.plan.max_blocks = max_blocks;
+    a.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
+    a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms / groups);
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (mqa::mla_mma_stage1(a, head_size, fp8, a.plan.units * groups, st) != cudaSuccess)
+        return MQA_ERR_CUDA;
+    if (!a.plan.per_seq) {
+        mqa::MergeArgs m{};
+        m.ws_o = a.ws_o;
+        m.ws_lse = a.ws_lse;
+        m.seq_lens = seq_lens;
+        m.out = a.out;
+        m.lse = lse;
+        m.status = device_status;
+        m.out_scale = 1.0f;  // stage-1 partials already carry k_scale
+        m.H = num_heads;
+        m.R = kv_lora_rank;
+        m.plan = a.plan;
+        if (mqa::lse_merge(m, st) != cudaSuccess) return MQA_ERR_CUDA;
+    }
+    return MQA_OK;
+}
+
+mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, float scale, float k_scale, float v_scale,
+                            void* out, float* lse, int batch, int num_q_heads, int num_kv_heads,
+                            int head_size, int num_blocks, int page_size, int max_blocks,
+                            mqa_kv_dtype kv_dtype, int num_kv_splits, void* workspace,
+                            size_t workspace_bytes, int* device_status, void* stream) {
+    (void)k_scale;
+    (void)v_scale;
+    if (!q || !kv_cache || !block_table || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (device_status && !aligned(device_status, 4)))
+        return MQA_ERR_INVALID_ARG;
+    if (batch < 1 || num_q_heads < 1 || num_kv_heads < 1 || num_blocks < 1 || max_blocks < 1 ||
+        page_size < 1 || num_kv_splits < 1)
+        return MQA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return MQA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return MQA_ERR_INVALID_ARG;
+    if (head_size != 64 && head_size != 128) return MQA_ERR_UNSUPPORTED;
+    if (num_kv_heads > 8 || num_q_heads / num_kv_heads > 16) return MQA_ERR_UNSUPPORTED;
+    if (page_size % 16 != 0) return MQA_ERR_UNSUPPORTED;
+    if (kv_dtype != MQA_KV_BF16) return MQA_ERR_UNSUPPORTED;
+    if (batch > kMaxBatch) return MQA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(max_blocks) * page_size > INT32_MAX ||
+        static_cast<long long>(num_blocks) * page_size > INT32_MAX)
+        return MQA_ERR_UNSUPPORTED;
+
+    const size_t need = gqa_paged_decode_workspace_bytes(batch, num_q_heads, head_size, num_kv_splits);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return MQA_ERR_WORKSPACE_TOO_SMALL;
+    if (need > 0 && !aligned(workspace, 16)) return MQA_ERR_INVALID_ARG;
+
+    const int sms = sm_count_current();
+    if (sms < 1) return MQA_ERR_CUDA;
+
+    mqa::GqaArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.kv = static_cast<const uint8_t*>(kv_cache);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    const size_t slots = static_cast<size_t>(batch) * num_kv_splits;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = need > 0 ? a.ws_o + slots * num_q_heads * head_size : nullptr;
+    a.status = device_status;
+    a.sl2 = scale * mqa::kLog2e;
+    a.Hq = num_q_heads;
+    a.Hkv = num_kv_heads;
+    a.num_blocks = num_blocks;
+    a.plan.batch = batch;
+    a.plan.page = page_size;
+    a.plan.max_blocks = max_blocks;
+    a.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
+    a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms);
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (mqa::gqa_mma_stage1(a, head_size, a.plan.units, st) != cudaSuccess) return MQA_ERR_CUDA;
+    if (!a.plan.per_seq) {
+        mqa::MergeArgs m{};
+        m.ws_o = a.ws_o;
+        m.ws_lse = a.ws_lse;
+        m.seq_lens = seq_lens;
+        m.out = a.out;
+        m.lse = lse;
+        m.status = device_status;
+        m.out_scale = 1.0f;
+        m.H = num_q_heads;
+        m.R = head_size;
+        m.plan = a.plan;
+        if (mqa::lse_merge(m, st) != cudaSuccess) return MQA_ERR_CUDA;
+    }
+    return MQA_OK;
+}
+
+}  // extern "C"

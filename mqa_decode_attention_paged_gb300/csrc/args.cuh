@@ -1,0 +1,59 @@
+// Kernel argument blocks, passed by value to the stage-1 and stage-2
+// kernels and filled in by the C ABI layer (api.cu).
+#pragma once
+
+#include "common.cuh"
+#include "plan.cuh"
+
+namespace mqa {
+
+struct MlaArgs {
+    const __nv_bfloat16* q;
+    const uint8_t* kv;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    __nv_bfloat16* out;
+    float* lse;
+    float* ws_o;    // [slots, H, R]
+    float* ws_lse;  // [slots, H]
+    int* status;
+    float sl2;        // scale * k_scale(fp8) * log2(e)
+    float out_scale;  // k_scale for fp8, 1 for bf16
+    int H, num_blocks;
+    Plan plan;
+};
+
+struct GqaArgs {
+    const __nv_bfloat16* q;
+    const uint8_t* kv;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    __nv_bfloat16* out;
+    float* lse;
+    float* ws_o;
+    float* ws_lse;
+    int* status;
+    float sl2;
+    int Hq, Hkv, num_blocks;
+    Plan plan;
+};
+
+struct MergeArgs {
+    const float* ws_o;    // [slots, H, R]
+    const float* ws_lse;  // [slots, H]
+    const int32_t* seq_lens;
+    __nv_bfloat16* out;   // [B, H, R]
+    float* lse;           // [B, H] or null
+    int* status;
+    float out_scale;
+    int H, R;
+    Plan plan;
+};
+
+cudaError_t mla_mma_stage1(const MlaArgs& a, int D, bool fp8, int grid, cudaStream_t stream);
+size_t mla_mma_smem_bytes(int D, bool fp8, int batch);
+cudaError_t gqa_mma_stage1(const GqaArgs& a, int D, int grid, cudaStream_t stream);
+size_t gqa_mma_smem_bytes(int D, int hkv, int batch);
+cudaError_t lse_merge(const MergeArgs& a, cudaStream_t stream);
+
+}  // namespace mqa

@@ -1,0 +1,156 @@
+// Work decomposition shared by the stage-1 kernels and the stage-2 merge.
+//
+// The KV pages of all requests are laid end to end: request b owns the
+// global page range [cum[b], cum[b+1]), cum[b+1] - cum[b] = ceil(len_b / page).
+//
+//  * per-request mode (num_kv_splits == 1): work unit g is request g.  One
+//    thread block walks the whole request in order and writes the final
+//    output; the result does not depend on the other requests
+//    (batch-invariant, bitwise reproducible).
+//  * balanced mode (num_kv_splits >= 2): the T pages are cut into `units`
+//    contiguous ranges of (almost) equal length, unit g owning pages
+//    [floor(g*T/units), floor((g+1)*T/units)).  A unit that covers a whole
+//    request writes its final output directly; otherwise each (unit, request)
+//    overlap produces one partial (O normalised, lse) in workspace slot
+//    g + b, and the stage-2 merge combines the partials of each request by
+//    LogSumExp (attention-kernel tutorial page, lshu.cn/news/265860, §12).
+//    Along the staircase of overlaps g + b strictly increases, so slots are
+//    unique and lie below units + B - 1 <= B * num_kv_splits when
+//    units <= B * (num_kv_splits - 1) + 1 (the host enforces this).
+#pragma once
+
+#include "common.cuh"
+
+namespace mqa {
+
+struct Plan {
+    int batch;
+    int page;
+    int max_blocks;
+    int units;
+    int per_seq;
+};
+
+// Clamp a request length to [0, max_blocks * page]; report out-of-range values.
+__device__ __forceinline__ int clamp_len(int n, int max_blocks, int page, int* status) {
+    const long long cap = static_cast<long long>(max_blocks) * page;
+    if (n < 0) {
+        report(status, MQA_ERR_DEVICE_CHECK);
+        return 0;
+    }
+    if (n > cap) {
+        report(status, MQA_ERR_DEVICE_CHECK);
+        return static_cast<int>(cap);
+    }
+    return n;
+}
+
+// Fill cum[0..B] (shared memory) with the exclusive page prefix; every thread
+// of the block must call this.  Returns T = cum[B].
+__device__ __forceinline__ int build_cum(const Plan& p, const int32_t* __restrict__ seq_lens,
+                                         int* cum, int* status) {
+    for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
+        const int n = clamp_len(seq_lens[i], p.max_blocks, p.page, status);
+        cum[i + 1] = (n + p.page - 1) / p.page;
+    }
+    if (threadIdx.x == 0) cum[0] = 0;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int running = 0;
+        for (int base = 0; base < p.batch; base += 32) {
+            const int i = base + lane;
+            int v = i < p.batch ? cum[i + 1] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (i < p.batch) cum[i + 1] = running + v;
+            running += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    __syncthreads();
+    return cum[p.batch];
+}
+
+// Largest b in [0, B) with cum[b] <= pg: the request that owns global page pg
+// (empty requests share their cum value with the next one and are skipped).
+__device__ __forceinline__ int seq_of_page(const int* cum, int B, int pg) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum[mid] <= pg)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+// Balanced mode: the unit whose page range holds global page pg (T > 0).
+__device__ __forceinline__ int unit_of_page(int units, int T, int pg) {
+    return static_cast<int>(((static_cast<long long>(pg) + 1) * units - 1) / T);
+}
+
+__device__ __forceinline__ void unit_range(const Plan& p, const int* cum, int T, int g, int& p0,
+                                           int& p1) {
+    if (p.per_seq) {
+        p0 = cum[g];
+        p1 = cum[g + 1];
+    } else {
+        p0 = static_cast<int>(static_cast<long long>(g) * T / p.units);
+        p1 = static_cast<int>(static_cast<long long>(g + 1) * T / p.units);
+    }
+}
+
+// One (unit, request) overlap: local pages [j0, j1) of request b.
+struct Piece {
+    int b, j0, j1;
+    int whole;  // the unit covers the request entirely: write the final output
+    int slot;   // workspace partial slot (balanced mode)
+};
+
+// Iterates over the pieces of unit g in page order.  Per-request mode yields
+// exactly one piece (possibly with no pages) so that empty requests still get
+// their output written.
+struct PieceIter {
+    int g, B, p, p1, b, first_done;
+    int per_seq;
+
+    __device__ __forceinline__ void init(const Plan& plan, const int* cum, int T, int unit) {
+        g = unit;
+        B = plan.batch;
+        per_seq = plan.per_seq;
+        int p0;
+        unit_range(plan, cum, T, unit, p0, p1);
+        p = p0;
+        b = per_seq ? unit : (p0 < p1 ? seq_of_page(cum, B, p0) : 0);
+        first_done = 0;
+    }
+
+    __device__ __forceinline__ bool next(const int* cum, Piece& pc) {
+        if (per_seq) {
+            if (first_done) return false;
+            first_done = 1;
+            pc.b = b;
+            pc.j0 = 0;
+            pc.j1 = cum[b + 1] - cum[b];
+            pc.whole = 1;
+            pc.slot = 0;
+            return true;
+        }
+        if (p >= p1) return false;
+        while (cum[b + 1] <= p) ++b;  // skip empty requests
+        const int end = min(p1, cum[b + 1]);
+        pc.b = b;
+        pc.j0 = p - cum[b];
+        pc.j1 = end - cum[b];
+        pc.whole = (pc.j0 == 0 && end == cum[b + 1]) ? 1 : 0;
+        pc.slot = g + b;
+        p = end;
+        return true;
+    }
+};
+
+}  // namespace mqa

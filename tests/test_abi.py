@@ -1,0 +1,122 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function the
+header declares, its pure host helpers agree with the pages' rules, and host
+validation rejects bad arguments before anything touches the device.
+
+Every call below that passes fake device pointers is built to FAIL validation,
+so nothing is ever enqueued with them, on any machine.
+"""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from mqa_decode_attention_paged_gb300 import _binding as mqa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # aligned, never dereferenced (validation fails first)
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in {"defined"}))
+
+
+def test_header_symbols_are_exported():
+    names = _declared_functions()
+    assert {"mla_decode", "gqa_paged_decode", "mqa_num_kv_splits", "mla_decode_workspace_bytes",
+            "gqa_paged_decode_workspace_bytes", "mqa_status_string", "mqa_abi_version",
+            "mqa_device_sm_count"} <= set(names)
+    lib = ctypes.CDLL(mqa.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_abi_version_and_status_strings():
+    assert mqa.abi_version() == 1
+    for code in range(7):
+        assert mqa.status_string(code) and mqa.status_string(code) != "unknown status"
+    assert mqa.status_string(99) == "unknown status"
+
+
+def test_num_kv_splits_matches_golden():
+    with open(os.path.join(ROOT, "tests", "golden", "num_kv_splits.json")) as f:
+        g = json.load(f)
+    for c in g["cases"]:
+        assert mqa.num_kv_splits(c["max_seq_len"], c["sm_count"], c["batch_invariant"]) == c["splits"], c
+
+
+def test_workspace_bytes():
+    # [B, H, S, R + 1] fp32, nothing for a single split.
+    assert mqa.mla_decode_workspace_bytes(64, 16, 512, 16) == 64 * 16 * 16 * 513 * 4
+    assert mqa.mla_decode_workspace_bytes(4, 128, 512, 1) == 0
+    assert mqa.gqa_paged_decode_workspace_bytes(256, 32, 128, 32) == 256 * 32 * 32 * 129 * 4
+    assert mqa.mla_decode_workspace_bytes(0, 16, 512, 2) == 0
+
+
+def _mla(**kw):
+    a = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, scale=0.07, k_scale=1.0, out=FAKE, lse=None,
+             B=2, H=16, D=576, R=512, nb=10, P=16, maxb=8, kvd=0, S=1, ws=None, wsb=0,
+             status=None, stream=None)
+    a.update(kw)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)  # noqa: E731
+    return mqa.lib.mla_decode(P(a["q"]), P(a["kv"]), P(a["bt"]), P(a["sl"]), a["scale"], a["k_scale"],
+                              P(a["out"]), P(a["lse"]), a["B"], a["H"], a["D"], a["R"], a["nb"],
+                              a["P"], a["maxb"], a["kvd"], a["S"], P(a["ws"]), a["wsb"],
+                              P(a["status"]), P(a["stream"]))
+
+
+def _gqa(**kw):
+    a = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, scale=0.09, out=FAKE, lse=None, B=2, Hq=32, Hkv=8,
+             D=128, nb=10, P=16, maxb=8, kvd=0, S=1, ws=None, wsb=0)
+    a.update(kw)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)  # noqa: E731
+    return mqa.lib.gqa_paged_decode(P(a["q"]), P(a["kv"]), P(a["bt"]), P(a["sl"]), a["scale"], 1.0,
+                                    1.0, P(a["out"]), P(a["lse"]), a["B"], a["Hq"], a["Hkv"], a["D"],
+                                    a["nb"], a["P"], a["maxb"], a["kvd"], a["S"], P(a["ws"]), a["wsb"],
+                                    None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), mqa.ERR_INVALID_ARG),
+    (dict(kv=None), mqa.ERR_INVALID_ARG),
+    (dict(bt=None), mqa.ERR_INVALID_ARG),
+    (dict(sl=None), mqa.ERR_INVALID_ARG),
+    (dict(out=None), mqa.ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), mqa.ERR_INVALID_ARG),          # not 16-byte aligned
+    (dict(kv=FAKE + 4), mqa.ERR_INVALID_ARG),
+    (dict(B=0), mqa.ERR_INVALID_ARG),
+    (dict(H=0), mqa.ERR_INVALID_ARG),
+    (dict(S=0), mqa.ERR_INVALID_ARG),
+    (dict(scale=float("nan")), mqa.ERR_INVALID_ARG),
+    (dict(D=512, R=448), mqa.ERR_UNSUPPORTED),         # head sizes 320 / 576 only
+    (dict(D=576, R=256), mqa.ERR_UNSUPPORTED),
+    (dict(P=24), mqa.ERR_UNSUPPORTED),                 # page must be a multiple of 16
+    (dict(P=8), mqa.ERR_UNSUPPORTED),
+    (dict(kvd=7), mqa.ERR_UNSUPPORTED),
+    (dict(H=129), mqa.ERR_UNSUPPORTED),
+    (dict(S=4, ws=None, wsb=0), mqa.ERR_WORKSPACE_TOO_SMALL),
+    (dict(S=4, ws=FAKE, wsb=2 * 16 * 4 * 513 * 4 - 1), mqa.ERR_WORKSPACE_TOO_SMALL),
+])
+def test_mla_validation(kw, code):
+    assert _mla(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), mqa.ERR_INVALID_ARG),
+    (dict(Hq=30, Hkv=8), mqa.ERR_INVALID_ARG),         # Hq must be a multiple of Hkv
+    (dict(D=96), mqa.ERR_UNSUPPORTED),
+    (dict(Hkv=16, Hq=32), mqa.ERR_UNSUPPORTED),
+    (dict(Hkv=1, Hq=32), mqa.ERR_UNSUPPORTED),         # at most 16 query heads per KV head
+    (dict(kvd=1), mqa.ERR_UNSUPPORTED),                # GQA serves bf16 caches only
+    (dict(P=40), mqa.ERR_UNSUPPORTED),
+    (dict(S=2), mqa.ERR_WORKSPACE_TOO_SMALL),
+])
+def test_gqa_validation(kw, code):
+    assert _gqa(**kw) == code
