@@ -135,6 +135,43 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
                       int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
                       void* workspace, size_t workspace_bytes, int* device_status, void* stream);
 
+/* Size of the library-owned scratch array used by mla_decode_noalloc. */
+#define MQA_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* mla_decode without a caller workspace (the pages have no counterpart to this
+ * entry point; it exists for callers of this library that cannot allocate
+ * device memory).
+ *
+ * Who needs it: a plugin running inside a host program whose memory pool owns
+ * all device memory, a plain C caller without a caching allocator whose hot
+ * loop cannot pay for the device-wide synchronisation cudaMalloc/cudaFree may
+ * cause, or code with a fixed memory plan.  Such callers still pass q, the
+ * cache, the block table, the lengths, out and lse exactly as for mla_decode;
+ * only the split partials move into a fixed device array of
+ * MQA_NOALLOC_SCRATCH_BYTES (64 MiB) that this library declares at file scope.
+ * Every GPU that loads the library holds that array until the process exits.
+ *
+ *   - Calls needing more than the array returns MQA_ERR_WORKSPACE_TOO_SMALL
+ *     before anything is enqueued: the requirement is
+ *     mla_decode_workspace_bytes(batch, num_heads, kv_lora_rank, num_kv_splits)
+ *     <= MQA_NOALLOC_SCRATCH_BYTES (lower num_kv_splits to fit; e.g. B=64,
+ *     H=16, R=512 fits up to 31 splits, B=4, H=128 up to 63).
+ *   - The first call on a device looks up the array's device address (once,
+ *     with that device current); make that first call before any stream
+ *     capture.  The function allocates nothing and never calls cudaMalloc or
+ *     cudaFree.
+ *   - All calls share the one array, which keeps the previous call's contents
+ *     (nothing in it needs to start at zero).  Calls whose kernels may overlap
+ *     on the GPU (other streams, other host threads) race on it and must be
+ *     serialised by the caller.
+ *   Other arguments, results and errors are those of mla_decode. */
+mqa_status mla_decode_noalloc(const void* q, const void* kv_cache, const int32_t* block_table,
+                              const int32_t* seq_lens, float scale, float k_scale, void* out,
+                              float* lse, int batch, int num_heads, int head_size,
+                              int kv_lora_rank, int num_blocks, int page_size, int max_blocks,
+                              mqa_kv_dtype kv_dtype, int num_kv_splits, int* device_status,
+                              void* stream);
+
 /* GQA paged decode (TritonAttentionImpl.forward's paged_attention path,
  * "Triton と MLA" page, 主要ファイル; cache layout from the "AttentionBackend"
  * page, "Motivation de conception").

@@ -53,6 +53,8 @@ def _load() -> ctypes.CDLL:
     lib.gqa_paged_decode_workspace_bytes.argtypes = [I, I, I, I]
     lib.mla_decode.restype = I
     lib.mla_decode.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
+    lib.mla_decode_noalloc.restype = I
+    lib.mla_decode_noalloc.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, P]
     lib.gqa_paged_decode.restype = I
     lib.gqa_paged_decode.argtypes = [P, P, P, P, F, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
     return lib
@@ -163,4 +165,26 @@ def gqa_paged_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, v_s
                               _stream(stream))
     if rc != OK:
         raise MqaError(rc, "gqa_paged_decode")
+    return out, lse
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def mla_decode_noalloc(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *, out, lse=None,
+                       num_kv_splits=1, kv_lora_rank=None, kv_dtype=None, device_status=None,
+                       stream=None):
+    """MLA decode without a caller workspace, for callers that cannot allocate
+    device memory: the split partials go to the library's own fixed 64 MiB
+    device array, so `out` (and `lse`, if wanted) must already exist.  Calls
+    share that array: do not let two of them overlap on the GPU."""
+    B, H, D = q.shape
+    nb, page, _ = kv_cache.shape
+    R = (D - 64) if kv_lora_rank is None else int(kv_lora_rank)
+    rc = lib.mla_decode_noalloc(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+                                float(scale), float(k_scale), _ptr(out), _ptr(lse), B, H, D, R, nb,
+                                page, block_table.shape[1], _kv_code(kv_cache, kv_dtype),
+                                int(num_kv_splits), _ptr(device_status), _stream(stream))
+    if rc != OK:
+        raise MqaError(rc, "mla_decode_noalloc")
     return out, lse
