@@ -47,8 +47,11 @@ def up_to_date() -> bool:
 
 
 def nvcc_flags(extra=()):
+    # MQA_NVCC_FLAGS: extra nvcc flags, e.g. "-DMQA_MLA_TILE=32" to pick the
+    # MLA pipeline tile at build time.
+    env = os.environ.get("MQA_NVCC_FLAGS", "").split()
     return [ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-            "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), *extra]
+            "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), *env, *extra]
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:

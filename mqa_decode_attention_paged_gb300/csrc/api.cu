@@ -1,7 +1,11 @@
 // C ABI entry points: argument validation, work decomposition and launches.
 // See include/mqa_decode.h for the contract of every function.
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <cstdint>
+#include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "plan.cuh"
@@ -10,7 +14,7 @@
 
 namespace {
 
-constexpr int kMaxBatch = 8192;
+constexpr int kMaxBatch = mqa::kMaxBatchSmem;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -33,7 +37,69 @@ size_t partial_bytes(int batch, int heads, int width, int splits) {
 int balanced_units(int batch, int splits, int resident_per_group) {
     long long cap = static_cast<long long>(batch) * (splits - 1) + 1;
     long long u = resident_per_group < 1 ? 1 : resident_per_group;
+    if (u > mqa::kMaxMergeUnits) u = mqa::kMaxMergeUnits;
     return static_cast<int>(u < cap ? u : cap);
+}
+
+// ---- tensor maps (TMA descriptors) for bf16 MLA caches ----------------------
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void* base;
+    long long rows;
+    int cols, box_rows;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && rows == o.rows && cols == o.cols && box_rows == o.box_rows;
+    }
+};
+
+// Encodes (or returns a cached copy of) the 2D view {cols, rows} of a
+// row-major bf16 cache with {64, box_rows} boxes and the 128-byte swizzle.
+bool mla_tensor_map(CUtensorMap* out, const void* base, int cols, long long rows, int box_rows) {
+    constexpr int kSlots = 16;
+    static std::mutex mu;
+    static MapKey keys[kSlots];
+    static CUtensorMap maps[kSlots];
+    static int used = 0, next = 0;
+    const MapKey key{base, rows, cols, box_rows};
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (keys[i] == key) {
+            *out = maps[i];
+            return true;
+        }
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof m);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t elem[2] = {1, 1};
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    const int slot = used < kSlots ? used++ : (next++ % kSlots);
+    keys[slot] = key;
+    maps[slot] = m;
+    *out = m;
+    return true;
 }
 
 }  // namespace
@@ -125,6 +191,17 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
     a.plan.max_blocks = max_blocks;
     a.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
     a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms / groups);
+
+    if (!fp8) {
+        // tensor boxes never straddle a page: 64 rows when pages are multiples
+        // of 64 tokens, else 32 or 16
+        const int tile = mqa::mla_mma_tile();
+        int br = (page_size % 64 == 0) ? 64 : (page_size % 32 == 0 ? 32 : 16);
+        if (br > tile) br = tile;
+        a.box_rows = br;
+        if (!mla_tensor_map(&a.tmap, kv_cache, head_size, static_cast<long long>(num_blocks) * page_size, br))
+            return MQA_ERR_CUDA;
+    }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (mqa::mla_mma_stage1(a, head_size, fp8, a.plan.units * groups, st) != cudaSuccess)

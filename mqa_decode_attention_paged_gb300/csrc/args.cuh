@@ -2,12 +2,25 @@
 // kernels and filled in by the C ABI layer (api.cu).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 #include "plan.cuh"
 
 namespace mqa {
 
+// Upper bound on balanced-mode work units (the merge stages one weight per
+// unit in shared memory).
+constexpr int kMaxMergeUnits = 1024;
+
+// Largest batch whose page prefix the stage-1 kernels keep in shared memory.
+constexpr int kMaxBatchSmem = 4096;
+
 struct MlaArgs {
+    // 2D tiled view of a bf16 cache: dims {D, num_blocks * page}, boxes of
+    // {64 columns, box_rows rows}, 128-byte swizzle (unused for e4m3 caches).
+    CUtensorMap tmap;
+    int box_rows;
     const __nv_bfloat16* q;
     const uint8_t* kv;
     const int32_t* block_table;
@@ -52,6 +65,7 @@ struct MergeArgs {
 
 cudaError_t mla_mma_stage1(const MlaArgs& a, int D, bool fp8, int grid, cudaStream_t stream);
 size_t mla_mma_smem_bytes(int D, bool fp8, int batch);
+int mla_mma_tile();
 cudaError_t gqa_mma_stage1(const GqaArgs& a, int D, int grid, cudaStream_t stream);
 size_t gqa_mma_smem_bytes(int D, int hkv, int batch);
 cudaError_t lse_merge(const MergeArgs& a, cudaStream_t stream);

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/mqa_decode.h"
 
 namespace mqa {
@@ -93,8 +95,61 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Tiled 2D tensor copy global -> shared (box given by the tensor map) that
+// completes its bytes on `bar`.  x (innermost, elements) must be a multiple of
+// 16 bytes' worth of elements; the map lives in kernel parameter space.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// Byte offset of bf16 element (row, col) in a tile held as 64-column panels
+// of `rows` 128-byte rows with the 128-byte swizzle (16-byte chunk index XOR
+// row % 8), the layout a SWIZZLE_128B tensor copy writes into 1024-byte
+// aligned shared memory.
+__device__ __forceinline__ uint32_t swz128(int row, int col, int rows) {
+    const int panel = col >> 6, chunk = (col & 63) >> 3;
+    return static_cast<uint32_t>(panel * rows * 128 + row * 128 + ((chunk ^ (row & 7)) << 4) + (col & 7) * 2);
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- programmatic dependent launch --------------------------------------------
+// pdl_wait(): block until the preceding grid in the stream has completed and
+// its writes are visible (no-op when the launch did not allow overlap).
+// pdl_launch_dependents(): allow the next grid in the stream to start its
+// prologue early; it still waits for this grid's completion before it reads
+// what this grid writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Host: launch `kernel` allowing programmatic overlap with the previous grid.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_with_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                   cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---- named barriers ---------------------------------------------------------

@@ -68,66 +68,68 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
     for (int i = threadIdx.x * 16; i < nstage * sbytes; i += blockDim.x * 16)
         *reinterpret_cast<uint4*>(stages + i) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
+    pdl_wait();
+    pdl_launch_dependents();
     const int T = build_cum(a.plan, a.seq_lens, cum, a.status);
     const int P = a.plan.page;
 
     if (warp == Hkv) {
         // ------------------------------------------------------------ producer
         const uint64_t pol = l2_policy_evict_first();
-        PieceIter it;
-        it.init(a.plan, cum, T, unit);
-        Piece pc;
+        TileCursor cur;
+        cur.init(a.plan, cum, T, unit, C::kTile);
         int stage = 0;
         uint32_t phase = 0;
-        bool ok = true;
         int issued[8];
         for (int s = 0; s < 8; ++s) issued[s] = -1;
         // lane -> (plane, token): lanes 0-15 copy K rows, 16-31 V rows.
         const int plane = lane >> 4, r = lane & 15;
-        while (ok && it.next(cum, pc)) {
-            const int len = clamp_len(a.seq_lens[pc.b], a.plan.max_blocks, P, nullptr);
-            const int tok0 = pc.j0 * P;
-            const int tok_end = min(pc.j1 * P, len);
-            const int32_t* bt = a.block_table + static_cast<long long>(pc.b) * a.plan.max_blocks;
-            for (int t0 = tok0; t0 < tok_end; t0 += C::kTile) {
-                if (!mbar_wait(&empty[stage], phase ^ 1)) {
-                    report(a.status, MQA_ERR_DEVICE_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-                uint8_t* dst = stages + stage * sbytes + (plane * C::kTile + r) * stride;
-                const int tok = t0 + r;
-                bool valid = tok < tok_end;
-                const uint8_t* src = nullptr;
-                if (valid) {
-                    const int blk = bt[tok / P];
-                    if (blk < 0 || blk >= a.num_blocks) {
-                        report(a.status, MQA_ERR_DEVICE_CHECK);
-                        valid = false;
-                    } else {
-                        src = a.kv + ((static_cast<long long>(blk) * 2 + plane) * P + tok % P) *
-                                         static_cast<long long>(rbytes);
-                    }
-                }
-                if (!valid) {
-                    uint4* row = reinterpret_cast<uint4*>(dst);
-                    for (int c = 0; c < rbytes / 16; ++c) row[c] = make_uint4(0, 0, 0, 0);
-                    fence_proxy_async_smem();
-                }
-                const uint32_t m = __ballot_sync(0xffffffffu, valid);
-                __syncwarp();
-                if (lane == 0) {
-                    mask_s[stage] = (m & (m >> 16)) & 0xffffu;  // token valid iff both rows are
-                    mbar_arrive_expect_tx(&full[stage], __popc(m) * rbytes);
-                }
-                __syncwarp();
-                if (valid) bulk_g2s(dst, src, rbytes, &full[stage], pol);
-                issued[stage] = static_cast<int>(phase);
-                if (++stage == nstage) {
-                    stage = 0;
-                    phase ^= 1;
-                }
+        // block id of this lane's row, fetched one tile ahead of its use
+        bool have = cur.next(a.plan, cum, a.seq_lens, a.block_table);
+        int t0 = cur.t0;
+        bool val = have && t0 + r < cur.tok_end;
+        int blk = val ? cur.bt[(t0 + r) / P] : 0;
+        while (have) {
+            const bool have_next = cur.next(a.plan, cum, a.seq_lens, a.block_table);
+            const bool nval = have_next && cur.t0 + r < cur.tok_end;
+            const int nblk = nval ? cur.bt[(cur.t0 + r) / P] : 0;
+            if (!mbar_wait(&empty[stage], phase ^ 1)) {
+                report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+                break;
             }
+            uint8_t* dst = stages + stage * sbytes + (plane * C::kTile + r) * stride;
+            bool valid = val;
+            if (valid && (blk < 0 || blk >= a.num_blocks)) {
+                report(a.status, MQA_ERR_DEVICE_CHECK);
+                valid = false;
+            }
+            if (!valid) {
+                uint4* row = reinterpret_cast<uint4*>(dst);
+                for (int c = 0; c < rbytes / 16; ++c) row[c] = make_uint4(0, 0, 0, 0);
+                fence_proxy_async_smem();
+            }
+            const uint32_t m = __ballot_sync(0xffffffffu, valid);
+            __syncwarp();
+            if (lane == 0) {
+                mask_s[stage] = (m & (m >> 16)) & 0xffffu;  // token valid iff both rows are
+                mbar_arrive_expect_tx(&full[stage], __popc(m) * rbytes);
+            }
+            __syncwarp();
+            if (valid) {
+                const int tok = t0 + r;
+                const uint8_t* src = a.kv + ((static_cast<long long>(blk) * 2 + plane) * P + tok % P) *
+                                                static_cast<long long>(rbytes);
+                bulk_g2s(dst, src, rbytes, &full[stage], pol);
+            }
+            issued[stage] = static_cast<int>(phase);
+            if (++stage == nstage) {
+                stage = 0;
+                phase ^= 1;
+            }
+            have = have_next;
+            t0 = cur.t0;
+            val = nval;
+            blk = nblk;
         }
         for (int s = 0; s < nstage; ++s)
             if (issued[s] >= 0 && !mbar_wait(&full[s], static_cast<uint32_t>(issued[s])))
@@ -306,7 +308,8 @@ static cudaError_t launch_gqa(const GqaArgs& a, int grid, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<grid, 32 * (a.Hkv + 1), smem, stream>>>(a);
+    e = launch_with_pdl(kern, dim3(grid), dim3(32 * (a.Hkv + 1)), smem, stream, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

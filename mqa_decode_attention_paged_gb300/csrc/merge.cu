@@ -8,6 +8,10 @@
 // (attention-kernel tutorial page, lshu.cn/news/265860).  Segments with
 // lse_s = -inf get weight 0.  The merge order is fixed (ascending segment), so
 // the result is reproducible run to run.
+//
+// One thread block per (request, head).  It is launched as a programmatic
+// dependent of stage 1: the page prefix (from seq_lens only) is computed
+// before waiting for stage 1 to finish, the partials after.
 #include "common.cuh"
 #include "plan.cuh"
 #include "args.cuh"
@@ -15,13 +19,14 @@
 namespace mqa {
 
 constexpr int kMergeThreads = 128;
-constexpr int kMergeHeads = 4;
 
 __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergeArgs a) {
     const int b = blockIdx.x;
-    const int hb = blockIdx.y * kMergeHeads;
+    const int h = blockIdx.y;
     const int P = a.plan.page;
-    __shared__ int red[2][kMergeThreads / 32];
+    __shared__ int red_i[2][kMergeThreads / 32];
+    __shared__ float red_f[kMergeThreads / 32];
+    __shared__ float s_w[kMaxMergeUnits];
 
     // Page offset of request b and total page count, recomputed exactly as the
     // stage-1 kernel's prefix (same clamping).
@@ -38,75 +43,98 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergeArg
         total += __shfl_xor_sync(0xffffffffu, total, o);
     }
     if ((threadIdx.x & 31) == 0) {
-        red[0][threadIdx.x >> 5] = before;
-        red[1][threadIdx.x >> 5] = total;
+        red_i[0][threadIdx.x >> 5] = before;
+        red_i[1][threadIdx.x >> 5] = total;
     }
     __syncthreads();
     before = 0;
     total = 0;
 #pragma unroll
     for (int w = 0; w < kMergeThreads / 32; ++w) {
-        before += red[0][w];
-        total += red[1][w];
+        before += red_i[0][w];
+        total += red_i[1][w];
     }
     const int n_b = (clamp_len(a.seq_lens[b], a.plan.max_blocks, P, nullptr) + P - 1) / P;
-    const int nh = min(kMergeHeads, a.H - hb);
     const int R = a.R;
+    const long long orow = (static_cast<long long>(b) * a.H + h) * R;
 
+    int gf = 0, gl = 0;
+    if (n_b > 0) {
+        gf = unit_of_page(a.plan.units, total, before);
+        gl = unit_of_page(a.plan.units, total, before + n_b - 1);
+        if (gf == gl) return;  // one unit covered the request and wrote it directly
+    }
+    pdl_wait();  // stage-1 partials (and the outputs' previous readers) are done
     if (n_b == 0) {  // empty request: out = 0, lse = -inf
-        for (int i = threadIdx.x; i < nh * R; i += kMergeThreads)
-            a.out[(static_cast<long long>(b) * a.H + hb) * R + i] = __float2bfloat16(0.f);
-        if (a.lse && threadIdx.x < nh) a.lse[static_cast<long long>(b) * a.H + hb + threadIdx.x] = -INFINITY;
+        for (int i = threadIdx.x; i < R / 2; i += kMergeThreads)
+            reinterpret_cast<uint32_t*>(a.out + orow)[i] = 0u;
+        if (a.lse && threadIdx.x == 0) a.lse[static_cast<long long>(b) * a.H + h] = -INFINITY;
         return;
     }
-    const int gf = unit_of_page(a.plan.units, total, before);
-    const int gl = unit_of_page(a.plan.units, total, before + n_b - 1);
-    if (gf == gl) return;  // one unit covered the request and wrote it directly
 
     // Units between gf and gl overlap request b unless their page range is
     // empty (more units than pages); empty units wrote no partial.
-    auto has_pages = [&](int g) {
-        return static_cast<long long>(g) * total / a.plan.units <
-               static_cast<long long>(g + 1) * total / a.plan.units;
-    };
-    for (int hh = 0; hh < nh; ++hh) {
-        const int h = hb + hh;
-        float m = -INFINITY;
-        for (int g = gf; g <= gl; ++g)
-            if (has_pages(g)) m = fmaxf(m, a.ws_lse[static_cast<long long>(g + b) * a.H + h]);
-        float wsum = 0.f;
-        for (int g = gf; g <= gl; ++g) {
-            if (!has_pages(g)) continue;
-            const float l = a.ws_lse[static_cast<long long>(g + b) * a.H + h];
-            wsum += l == -INFINITY ? 0.f : __expf(l - m);
-        }
-        const float inv = wsum > 0.f ? a.out_scale / wsum : 0.f;
-        for (int c4 = threadIdx.x; c4 < R / 4; c4 += kMergeThreads) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int g = gf; g <= gl; ++g) {
-                if (!has_pages(g)) continue;
-                const float l = a.ws_lse[static_cast<long long>(g + b) * a.H + h];
-                const float w = l == -INFINITY ? 0.f : __expf(l - m);
-                const float4 v = *reinterpret_cast<const float4*>(
-                    a.ws_o + (static_cast<long long>(g + b) * a.H + h) * R + 4 * c4);
-                acc.x += w * v.x;
-                acc.y += w * v.y;
-                acc.z += w * v.z;
-                acc.w += w * v.w;
-            }
-            uint2 packed;
-            packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-            packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-            *reinterpret_cast<uint2*>(a.out + (static_cast<long long>(b) * a.H + h) * R + 4 * c4) = packed;
-        }
-        if (threadIdx.x == 0 && a.lse)
-            a.lse[static_cast<long long>(b) * a.H + h] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
+    const int np = gl - gf + 1;
+    float m = -INFINITY;
+    for (int i = threadIdx.x; i < np; i += kMergeThreads) {
+        const int g = gf + i;
+        const bool has = static_cast<long long>(g) * total / a.plan.units <
+                         static_cast<long long>(g + 1) * total / a.plan.units;
+        const float l = has ? a.ws_lse[static_cast<long long>(g + b) * a.H + h] : -INFINITY;
+        s_w[i] = l;
+        m = fmaxf(m, l);
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red_f[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = red_f[0];
+#pragma unroll
+    for (int w = 1; w < kMergeThreads / 32; ++w) m = fmaxf(m, red_f[w]);
+    __syncthreads();
+    float wsum = 0.f;
+    for (int i = threadIdx.x; i < np; i += kMergeThreads) {
+        const float l = s_w[i];
+        const float w = (l == -INFINITY || m == -INFINITY) ? 0.f : __expf(l - m);
+        s_w[i] = w;
+        wsum += w;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    if ((threadIdx.x & 31) == 0) red_f[threadIdx.x >> 5] = wsum;
+    __syncthreads();
+    wsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) wsum += red_f[w];
+    const float inv = wsum > 0.f ? a.out_scale / wsum : 0.f;
+
+    for (int c4 = threadIdx.x; c4 < R / 4; c4 += kMergeThreads) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* base = a.ws_o + (static_cast<long long>(gf + b) * a.H + h) * R + 4 * c4;
+        const long long step = static_cast<long long>(a.H) * R;
+#pragma unroll 4
+        for (int i = 0; i < np; ++i) {
+            const float w = s_w[i];
+            if (w == 0.f) continue;
+            const float4 v = *reinterpret_cast<const float4*>(base + i * step);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(a.out + orow + 4 * c4) = packed;
+    }
+    if (threadIdx.x == 0 && a.lse)
+        a.lse[static_cast<long long>(b) * a.H + h] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
 }
 
 cudaError_t lse_merge(const MergeArgs& a, cudaStream_t stream) {
-    dim3 grid(a.plan.batch, (a.H + kMergeHeads - 1) / kMergeHeads);
-    lse_merge_kernel<<<grid, kMergeThreads, 0, stream>>>(a);
+    cudaError_t e = launch_with_pdl(lse_merge_kernel, dim3(a.plan.batch, a.H), dim3(kMergeThreads), 0,
+                                    stream, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

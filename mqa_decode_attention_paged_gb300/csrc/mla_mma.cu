@@ -2,16 +2,17 @@
 // per thread block).
 //
 // One thread block = 8 consumer warps + 1 producer warp, persistent over a
-// work unit (see plan.cuh).  The producer walks the block table and stages
-// 64-token tiles of latent rows [kv_c | k_pe] into shared memory with
+// work unit (see plan.cuh).  The producer walks the block table (prefetching
+// the next tile's block ids while it waits for a free stage) and stages
+// kTile-token tiles of latent rows [kv_c | k_pe] into shared memory with
 // per-row bulk copies (TMA engine), zero-filling rows past the sequence end.
 // The same staged tile serves as K (all D columns) and V (first R columns),
 // the MQA view of MLA ("Triton と MLA" page, vllm-arch-zh
 // ja/attention/triton-mla, section データフロー).
 //
 // Per tile the consumers compute
-//   S = Q K^T  (16 heads x 64 tokens; 8 warps = 2 token halves x 4 quarters
-//               of the head dimension, partial sums reduced through smem),
+//   S = Q K^T  (16 heads x kTile tokens; 8 warps = 2 token halves x 4
+//               quarters of the head dimension, partial sums reduced in smem),
 //   online softmax per head (tutorial page lshu.cn/news/265860, §7: running
 //   max m, running sum l, rescale alpha = 2^(m_old - m_new) in base 2 with
 //   log2(e) folded into the scale),
@@ -25,48 +26,68 @@
 
 namespace mqa {
 
-template <int D, int R, bool FP8>
+// Shared-memory budget: everything but the staging ring is fixed, the ring
+// gets as many stages as fit (at most 8).
+
+template <int D, int R, bool FP8, int TILE>
 struct MlaMmaCfg {
     static constexpr int kHeads = 16;
-    static constexpr int kTile = 64;
+    static constexpr int kTile = TILE;                         // tokens per stage
+    static constexpr int kHalf = kTile / 2;                    // tokens per QK warp
+    static constexpr int kRowsPerLane = kTile / 32;            // fp8 producer rows per lane
+    static constexpr int kTokPerThread = kTile / 16;           // softmax tokens per thread
     static constexpr int kConsumerWarps = 8;
     static constexpr int kConsumers = 32 * kConsumerWarps;
     static constexpr int kThreads = kConsumers + 32;
-    static constexpr int kRowBytes = D * (FP8 ? 1 : 2);      // one cache row in global memory
-    static constexpr int kStageStride = kRowBytes + 16;      // padded row stride of a stage
-    static constexpr int kOpStride = D * 2 + 16;              // bf16 operand row stride (bytes)
-    static constexpr int kStages = (D == 576) ? 2 : (FP8 ? 4 : 3);
+    static constexpr int kPanels = D / 64;                     // 64-column bf16 panels
+    static constexpr int kOpBytes = kPanels * kTile * 128;     // swizzled bf16 operand tile
+    static constexpr int kFp8Stride = D + 16;                  // padded e4m3 staging row
+    static constexpr int kStageBytes = FP8 ? kTile * kFp8Stride : kOpBytes;
     static constexpr int kKSteps = D / 16;
-    static constexpr int kKq = kKSteps / 4;                   // k-steps per head-dim quarter
-    static constexpr int kColsPerWarp = R / kConsumerWarps;   // output columns per warp
-    static constexpr int kNbPV = kColsPerWarp / 8;            // n-blocks per warp in P.V
-    static constexpr int kRedStride = kTile + 8;              // floats
-    static constexpr int kPStride = kTile + 8;                // bf16 elements
+    static constexpr int kKq = kKSteps / 4;                    // k-steps per head-dim quarter
+    static constexpr int kColsPerWarp = R / kConsumerWarps;    // output columns per warp
+    static constexpr int kNbPV = kColsPerWarp / 8;             // n-blocks per warp in P.V
+    static constexpr int kRedStride = kTile + 8;               // floats
+    static constexpr int kPStride = kTile + 8;                 // bf16 elements
 
-    static constexpr int kStageBytes = kTile * kStageStride;
+    static constexpr int kRedBytes = 4 * kHeads * kRedStride * 4;
+    static constexpr int kPBytes = kHeads * kPStride * 2;
+    static constexpr int kMiscBytes = kHeads * 4 + kHeads * 8 + 8 * 8 + 16 * 8 + 16;
+    static constexpr int kFixed = 1024 + (FP8 ? kOpBytes : 0) + kRedBytes + kPBytes + kMiscBytes +
+                                  4 * (kMaxBatchSmem + 1) + 1024;
+    static constexpr int kStagesFit = (227 * 1024 - kFixed) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+
+    static constexpr int align1k(int x) { return (x + 1023) & ~1023; }
     static constexpr int kOffStages = 0;
-    static constexpr int kOffOp = kOffStages + kStages * kStageBytes;
-    static constexpr int kOpBytes = FP8 ? kTile * kOpStride : 0;
-    static constexpr int kOffRed = kOffOp + kOpBytes;
-    static constexpr int kOffP = kOffRed + 4 * kHeads * kRedStride * 4;
-    static constexpr int kOffAlpha = kOffP + kHeads * kPStride * 2;
+    static constexpr int kOffOp = align1k(kStages * kStageBytes);
+    static constexpr int kOffRed = kOffOp + (FP8 ? kOpBytes : 0);
+    static constexpr int kOffP = kOffRed + kRedBytes;
+    static constexpr int kOffAlpha = kOffP + kPBytes;
     static constexpr int kOffMl = kOffAlpha + kHeads * 4;
     static constexpr int kOffMask = kOffMl + kHeads * 8;
-    static constexpr int kOffBars = kOffMask + kStages * 8;
-    static constexpr int kOffFlags = kOffBars + 2 * kStages * 8;
+    static constexpr int kOffBars = kOffMask + 8 * 8;
+    static constexpr int kOffFlags = kOffBars + 16 * 8;
     static constexpr int kOffCum = kOffFlags + 16;
-    static size_t smem_bytes(int batch) { return kOffCum + 4 * (batch + 1); }
+    // +1024: the dynamic window is re-aligned to 1024 bytes in the kernel
+    static size_t smem_bytes(int batch) { return 1024 + kOffCum + 4 * (batch + 1); }
 
+    static_assert(kTile == 32 || kTile == 64, "tile of 32 or 64 tokens");
+    static_assert(kStages >= 2, "at least two pipeline stages");
     static_assert(D % 64 == 0 && kKSteps % 4 == 0, "head size must split into 4 quarters");
     static_assert(kColsPerWarp % 16 == 0, "P.V columns per warp must be a multiple of 16");
-    static_assert(kRowBytes % 16 == 0, "bulk copies need 16-byte rows");
+    static_assert(D % 16 == 0, "bulk copies need 16-byte rows");
+    static_assert(1024 + kOffCum + 4 * (kMaxBatchSmem + 1) <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, int R, bool FP8>
-__global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
-    mla_decode_mma_kernel(const MlaArgs a) {
-    using C = MlaMmaCfg<D, R, FP8>;
-    extern __shared__ __align__(128) uint8_t smem[];
+template <int D, int R, bool FP8, int TILE>
+__global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
+    mla_decode_mma_kernel(const __grid_constant__ MlaArgs a) {
+    using C = MlaMmaCfg<D, R, FP8, TILE>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned window: the 128-byte swizzle pattern is a function of
+    // address bits 7..9.
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* stages = smem + C::kOffStages;
     float* red = reinterpret_cast<float*>(smem + C::kOffRed);
     __nv_bfloat16* Ps = reinterpret_cast<__nv_bfloat16*>(smem + C::kOffP);
@@ -90,12 +111,16 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
         }
         *abort_s = 0;
         fence_mbar_init();
+        if constexpr (!FP8) prefetch_tmap(&a.tmap);
     }
-    // Zero every staging row once so that rows never written by a copy hold
-    // finite values.
-    for (int i = threadIdx.x * 16; i < C::kStages * C::kStageBytes; i += C::kThreads * 16)
-        *reinterpret_cast<uint4*>(stages + i) = make_uint4(0, 0, 0, 0);
+    // Zero the staging ring (and the widened operand tile) once so that rows
+    // never written by a copy hold finite values.
+    for (int i = threadIdx.x * 16; i < C::kOffRed; i += C::kThreads * 16)
+        *reinterpret_cast<uint4*>(smem + i) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
+    // Inputs may come from the previous grid in the stream.
+    pdl_wait();
+    pdl_launch_dependents();
     const int T = build_cum(a.plan, a.seq_lens, cum, a.status);  // contains __syncthreads
 
     const int P = a.plan.page;
@@ -103,67 +128,112 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
     if (warp == C::kConsumerWarps) {
         // ------------------------------------------------------------ producer
         const uint64_t pol = l2_policy_evict_first();
-        PieceIter it;
-        it.init(a.plan, cum, T, unit);
-        Piece pc;
+        TileCursor cur;
+        cur.init(a.plan, cum, T, unit, C::kTile);
         int stage = 0;
         uint32_t phase = 0;
-        bool ok = true;
         int issued[C::kStages];
         for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
-        while (ok && it.next(cum, pc)) {
-            const int len = clamp_len(a.seq_lens[pc.b], a.plan.max_blocks, P, nullptr);
-            const int tok0 = pc.j0 * P;
-            const int tok_end = min(pc.j1 * P, len);
-            const int32_t* bt = a.block_table + static_cast<long long>(pc.b) * a.plan.max_blocks;
-            for (int t0 = tok0; t0 < tok_end; t0 += C::kTile) {
-                if (!mbar_wait(&empty[stage], phase ^ 1)) {
-                    report(a.status, MQA_ERR_DEVICE_TIMEOUT);
-                    ok = false;
-                    break;
-                }
-                uint8_t* dst = stages + stage * C::kStageBytes;
-                const uint8_t* src[2];
-                bool valid[2];
+        const int BR = FP8 ? 1 : a.box_rows;          // rows per tensor box (bf16)
+        const int nbox = FP8 ? C::kRowsPerLane : C::kTile / BR;
+
+        // Block ids of the next tile, fetched one tile ahead of their use.
+        // bf16: lane k < nbox holds box k; e4m3: slot k holds row lane + 32k.
+        auto fetch = [&](const TileCursor& tc, int (&blk)[C::kRowsPerLane], bool (&val)[C::kRowsPerLane]) {
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int r = lane + 32 * k;
-                    const int tok = t0 + r;
-                    valid[k] = tok < tok_end;
-                    src[k] = nullptr;
-                    if (valid[k]) {
-                        const int blk = bt[tok / P];
-                        if (blk < 0 || blk >= a.num_blocks) {
-                            report(a.status, MQA_ERR_DEVICE_CHECK);
-                            valid[k] = false;
-                        } else {
-                            src[k] = a.kv + (static_cast<long long>(blk) * P + tok % P) * C::kRowBytes;
-                        }
-                    }
-                    if (!valid[k]) {
-                        uint4* row = reinterpret_cast<uint4*>(dst + r * C::kStageStride);
-                        for (int c = 0; c < C::kRowBytes / 16; ++c) row[c] = make_uint4(0, 0, 0, 0);
+            for (int k = 0; k < C::kRowsPerLane; ++k) {
+                const int tok = FP8 ? tc.t0 + lane + 32 * k : tc.t0 + lane * BR;
+                val[k] = (FP8 || (k == 0 && lane < nbox)) && tok < tc.tok_end;
+                blk[k] = val[k] ? tc.bt[tok / P] : 0;
+            }
+        };
+        bool have = cur.next(a.plan, cum, a.seq_lens, a.block_table);
+        int blk[C::kRowsPerLane];
+        bool val[C::kRowsPerLane];
+        int t0 = cur.t0, tend = cur.tok_end;
+        if (have) fetch(cur, blk, val);
+        while (have) {
+            const bool have_next = cur.next(a.plan, cum, a.seq_lens, a.block_table);
+            int nblk[C::kRowsPerLane];
+            bool nval[C::kRowsPerLane];
+            if (have_next) fetch(cur, nblk, nval);
+
+            if (!mbar_wait(&empty[stage], phase ^ 1)) {
+                report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+                break;
+            }
+            uint8_t* dst = stages + stage * C::kStageBytes;
+#pragma unroll
+            for (int k = 0; k < C::kRowsPerLane; ++k) {
+                if (val[k] && (blk[k] < 0 || blk[k] >= a.num_blocks)) {
+                    report(a.status, MQA_ERR_DEVICE_CHECK);
+                    val[k] = false;
+                }
+            }
+            const int n_tok = tend - t0;
+            const uint64_t live = n_tok >= 64 ? ~0ull : ((1ull << n_tok) - 1);
+            if constexpr (FP8) {
+                // one bulk copy per e4m3 row, invalid rows zero-filled here
+                uint64_t vmask = 0;
+#pragma unroll
+                for (int k = 0; k < C::kRowsPerLane; ++k) {
+                    if (!val[k]) {
+                        uint4* row = reinterpret_cast<uint4*>(dst + (lane + 32 * k) * C::kFp8Stride);
+                        for (int c = 0; c < D / 16; ++c) row[c] = make_uint4(0, 0, 0, 0);
                         fence_proxy_async_smem();
                     }
+                    vmask |= static_cast<uint64_t>(__ballot_sync(0xffffffffu, val[k])) << (32 * k);
                 }
-                const uint32_t m0 = __ballot_sync(0xffffffffu, valid[0]);
-                const uint32_t m1 = __ballot_sync(0xffffffffu, valid[1]);
                 __syncwarp();
                 if (lane == 0) {
-                    mask_s[stage] = static_cast<uint64_t>(m0) | (static_cast<uint64_t>(m1) << 32);
-                    mbar_arrive_expect_tx(&full[stage], (__popc(m0) + __popc(m1)) * C::kRowBytes);
+                    mask_s[stage] = vmask;
+                    mbar_arrive_expect_tx(&full[stage], __popcll(vmask) * D);
                 }
                 __syncwarp();
 #pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    if (valid[k])
-                        bulk_g2s(dst + (lane + 32 * k) * C::kStageStride, src[k], C::kRowBytes,
-                                 &full[stage], pol);
-                issued[stage] = static_cast<int>(phase);
-                if (++stage == C::kStages) {
-                    stage = 0;
-                    phase ^= 1;
+                for (int k = 0; k < C::kRowsPerLane; ++k) {
+                    if (val[k]) {
+                        const int tok = t0 + lane + 32 * k;
+                        const uint8_t* src = a.kv + (static_cast<long long>(blk[k]) * P + tok % P) * D;
+                        bulk_g2s(dst + (lane + 32 * k) * C::kFp8Stride, src, D, &full[stage], pol);
+                    }
                 }
+            } else {
+                // one tensor copy per (box, 64-column panel); rows of a box
+                // past the sequence end are zeroed by the consumers
+                const uint32_t bm = __ballot_sync(0xffffffffu, val[0]) & ((1u << nbox) - 1);
+                uint64_t boxbits = 0;
+                for (int bx = 0; bx < nbox; ++bx)
+                    if ((bm >> bx) & 1u) boxbits |= (BR == 64 ? ~0ull : ((1ull << BR) - 1)) << (bx * BR);
+                int bblk[4];
+#pragma unroll
+                for (int bx = 0; bx < 4; ++bx) bblk[bx] = __shfl_sync(0xffffffffu, blk[0], bx);
+                if (lane == 0) {
+                    mask_s[stage] = boxbits & live;
+                    mbar_arrive_expect_tx(&full[stage], __popc(bm) * BR * 128 * C::kPanels);
+                }
+                __syncwarp();
+                for (int i = lane; i < nbox * C::kPanels; i += 32) {
+                    const int bx = i / C::kPanels, pn = i % C::kPanels;
+                    if ((bm >> bx) & 1u) {
+                        const int row = bblk[bx] * P + (t0 + bx * BR) % P;
+                        tma_load_2d(dst + pn * C::kTile * 128 + bx * BR * 128, &a.tmap, pn * 64, row,
+                                    &full[stage], pol);
+                    }
+                }
+            }
+            issued[stage] = static_cast<int>(phase);
+            if (++stage == C::kStages) {
+                stage = 0;
+                phase ^= 1;
+            }
+            have = have_next;
+            t0 = cur.t0;
+            tend = cur.tok_end;
+#pragma unroll
+            for (int k = 0; k < C::kRowsPerLane; ++k) {
+                blk[k] = nblk[k];
+                val[k] = nval[k];
             }
         }
         // Never leave copies in flight behind: wait (bounded) for the last
@@ -177,8 +247,10 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
     // -------------------------------------------------------------- consumers
     const int g = lane >> 2, c = lane & 3;
     const int th = warp >> 2, dq = warp & 3;  // QK role: token half, head-dim quarter
-    const int t = threadIdx.x;                // softmax role: head sh, tokens 4*sk..4*sk+3
+    const int t = threadIdx.x;                // softmax role: head sh, tokens sk*kTPT ..
     const int sh = t >> 4, sk = t & 15;
+    constexpr int kTPT = C::kTokPerThread;
+    constexpr uint64_t kFullMask = C::kTile == 64 ? ~0ull : ((1ull << C::kTile) - 1);
 
     PieceIter it;
     it.init(a.plan, cum, T, unit);
@@ -217,18 +289,19 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
                 *abort_s = 1;
                 report(a.status, MQA_ERR_DEVICE_TIMEOUT);
             }
-            const uint8_t* stage_buf = stages + stage * C::kStageBytes;
-            const uint8_t* op = stage_buf;
-            int op_stride = C::kStageStride;
+            uint8_t* stage_buf = stages + stage * C::kStageBytes;
+            uint8_t* op = stage_buf;
+            const uint64_t vmask = mask_s[stage];
+            bool zeroed = false;
             if constexpr (FP8) {
-                // Widen the e4m3 tile to bf16 (exact) in the operand buffer.
-                uint8_t* opw = smem + C::kOffOp;
+                // Widen the e4m3 tile to bf16 (exact) into the swizzled operand tile.
+                op = smem + C::kOffOp;
                 named_bar_sync(3, C::kConsumers);  // previous tile's P.V is done
                 if (ok) {
                     constexpr int kChunks = C::kTile * (D / 16);
                     for (int i = t; i < kChunks; i += C::kConsumers) {
                         const int r = i / (D / 16), cc = i % (D / 16);
-                        const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + r * C::kStageStride + cc * 16);
+                        const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + r * C::kFp8Stride + cc * 16);
                         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                         uint32_t outw[8];
 #pragma unroll
@@ -242,41 +315,54 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
                                 outw[2 * j + hh] = pack_bf16x2(f.x, f.y);
                             }
                         }
-                        uint4* d = reinterpret_cast<uint4*>(opw + r * C::kOpStride + cc * 32);
-                        d[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-                        d[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+                        *reinterpret_cast<uint4*>(op + swz128(r, 16 * cc, C::kTile)) =
+                            make_uint4(outw[0], outw[1], outw[2], outw[3]);
+                        *reinterpret_cast<uint4*>(op + swz128(r, 16 * cc + 8, C::kTile)) =
+                            make_uint4(outw[4], outw[5], outw[6], outw[7]);
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stage]);
                 named_bar_sync(3, C::kConsumers);
-                op = opw;
-                op_stride = C::kOpStride;
+            } else if (vmask != kFullMask) {
+                // Rows past the sequence end may hold anything (the tail of a
+                // page, or an earlier tile): zero them in the V columns this
+                // warp reads, so P = 0 never meets a NaN.  K columns of those
+                // rows only reach logits that the mask replaces with -inf.
+                constexpr int kChunksPerWarp = C::kColsPerWarp / 8;
+                for (int i = lane; i < C::kTile * kChunksPerWarp; i += 32) {
+                    const int r = i / kChunksPerWarp;
+                    if (!((vmask >> r) & 1ull)) {
+                        const int col = warp * C::kColsPerWarp + (i % kChunksPerWarp) * 8;
+                        *reinterpret_cast<uint4*>(op + swz128(r, col, C::kTile)) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                zeroed = true;
+                __syncwarp();
             }
-            const uint64_t vmask = mask_s[stage];
 
             // ---- S partial = Q[:, quarter] K[tokens of half th, quarter]^T
-            float sacc[4][4];
+            float sacc[C::kHalf / 8][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+            for (int i = 0; i < C::kHalf / 8; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
             if (ok) {
 #pragma unroll
                 for (int ks = 0; ks < C::kKq; ++ks) {
                     const int k0 = (dq * C::kKq + ks) * 16;
 #pragma unroll
-                    for (int nb2 = 0; nb2 < 2; ++nb2) {
-                        const int row = th * 32 + nb2 * 16 + (lane & 7) + ((lane >> 4) << 3);
+                    for (int nb2 = 0; nb2 < C::kHalf / 16; ++nb2) {
+                        const int row = th * C::kHalf + nb2 * 16 + (lane & 7) + ((lane >> 4) << 3);
                         const int col = k0 + ((lane >> 3) & 1) * 8;
                         uint32_t b0, b1, b2, b3;
-                        ldsm_x4(b0, b1, b2, b3, op + row * op_stride + col * 2);
+                        ldsm_x4(b0, b1, b2, b3, op + swz128(row, col, C::kTile));
                         mma_bf16_16816(sacc[2 * nb2], qa[ks], b0, b1);
                         mma_bf16_16816(sacc[2 * nb2 + 1], qa[ks], b2, b3);
                     }
                 }
             }
 #pragma unroll
-            for (int nb = 0; nb < 4; ++nb) {
-                const int col = th * 32 + nb * 8 + 2 * c;
+            for (int nb = 0; nb < C::kHalf / 8; ++nb) {
+                const int col = th * C::kHalf + nb * 8 + 2 * c;
                 *reinterpret_cast<float2*>(&red[(dq * 16 + g) * C::kRedStride + col]) =
                     make_float2(sacc[nb][0], sacc[nb][1]);
                 *reinterpret_cast<float2*>(&red[(dq * 16 + g + 8) * C::kRedStride + col]) =
@@ -284,23 +370,30 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
             }
             named_bar_sync(1, C::kConsumers);
 
-            // ---- online softmax for head sh over tokens 4*sk .. 4*sk+3
+            // ---- online softmax for head sh over tokens sk*kTPT .. +kTPT-1
             {
-                float x[4];
+                float x[kTPT];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) x[i] = 0.f;
+                for (int i = 0; i < kTPT; ++i) x[i] = 0.f;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 v = *reinterpret_cast<const float4*>(&red[(q4 * 16 + sh) * C::kRedStride + 4 * sk]);
-                    x[0] += v.x;
-                    x[1] += v.y;
-                    x[2] += v.z;
-                    x[3] += v.w;
+                    const float* src = &red[(q4 * 16 + sh) * C::kRedStride + kTPT * sk];
+                    if constexpr (kTPT == 4) {
+                        const float4 v = *reinterpret_cast<const float4*>(src);
+                        x[0] += v.x;
+                        x[1] += v.y;
+                        x[2] += v.z;
+                        x[3] += v.w;
+                    } else {
+                        const float2 v = *reinterpret_cast<const float2*>(src);
+                        x[0] += v.x;
+                        x[1] += v.y;
+                    }
                 }
                 float mx = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const bool valid = (vmask >> (4 * sk + i)) & 1ull;
+                for (int i = 0; i < kTPT; ++i) {
+                    const bool valid = (vmask >> (kTPT * sk + i)) & 1ull;
                     x[i] = valid ? x[i] * a.sl2 : -INFINITY;
                     mx = fmaxf(mx, x[i]);
                 }
@@ -310,9 +403,9 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
                 const float m_use = m_new == -INFINITY ? 0.f : m_new;
                 const float alpha = ex2(m_run - m_use);
                 float psum = 0.f;
-                uint32_t pk[2];
+                uint32_t pk[kTPT / 2];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
+                for (int i = 0; i < kTPT / 2; ++i) {
                     // l sums the fp32 probabilities; P.V uses them rounded to bf16
                     const float p0 = ex2(x[2 * i] - m_use), p1 = ex2(x[2 * i + 1] - m_use);
                     psum += p0 + p1;
@@ -322,7 +415,10 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
                 for (int o2 = 8; o2 >= 1; o2 >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o2);
                 l_run = l_run * alpha + psum;
                 m_run = m_new;
-                *reinterpret_cast<uint2*>(&Ps[sh * C::kPStride + 4 * sk]) = make_uint2(pk[0], pk[1]);
+                if constexpr (kTPT == 4)
+                    *reinterpret_cast<uint2*>(&Ps[sh * C::kPStride + kTPT * sk]) = make_uint2(pk[0], pk[1]);
+                else
+                    *reinterpret_cast<uint32_t*>(&Ps[sh * C::kPStride + kTPT * sk]) = pk[0];
                 if (sk == 0) alpha_s[sh] = alpha;
             }
             named_bar_sync(2, C::kConsumers);
@@ -348,7 +444,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
                             const int tok = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
                             const int col = warp * C::kColsPerWarp + nb2 * 16 + (lane >> 4) * 8;
                             uint32_t b0, b1, b2, b3;
-                            ldsm_x4_t(b0, b1, b2, b3, op + tok * op_stride + col * 2);
+                            ldsm_x4_t(b0, b1, b2, b3, op + swz128(tok, col, C::kTile));
                             mma_bf16_16816(o[2 * nb2], pa, b0, b1);
                             mma_bf16_16816(o[2 * nb2 + 1], pa, b2, b3);
                         }
@@ -356,6 +452,8 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
                 }
             }
             if constexpr (!FP8) {
+                // the stage goes back to the tensor copies (async proxy)
+                if (zeroed) fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stage]);
             }
@@ -411,15 +509,27 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8>::kThreads, 1)
     }
 }
 
+// Tile size (tokens per pipeline stage; 32 or 64).  The number of stages is
+// the largest that fits the staging budget.
+#ifndef MQA_MLA_TILE
+#define MQA_MLA_TILE 64
+#endif
+template <int D, bool FP8>
+struct MlaTile {
+    static constexpr int value = MQA_MLA_TILE;
+};
+
 template <int D, int R, bool FP8>
 static cudaError_t launch_mla_mma(const MlaArgs& a, int grid, cudaStream_t stream) {
-    using C = MlaMmaCfg<D, R, FP8>;
+    constexpr int kTile = MlaTile<D, FP8>::value;
+    using C = MlaMmaCfg<D, R, FP8, kTile>;
     const size_t smem = C::smem_bytes(a.plan.batch);
-    auto kern = mla_decode_mma_kernel<D, R, FP8>;
+    auto kern = mla_decode_mma_kernel<D, R, FP8, kTile>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::kThreads, smem, stream>>>(a);
+    e = launch_with_pdl(kern, dim3(grid), dim3(C::kThreads), smem, stream, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -430,11 +540,13 @@ cudaError_t mla_mma_stage1(const MlaArgs& a, int D, bool fp8, int grid, cudaStre
                : launch_mla_mma<320, 256, false>(a, grid, stream);
 }
 
+int mla_mma_tile() { return MQA_MLA_TILE; }
+
 size_t mla_mma_smem_bytes(int D, bool fp8, int batch) {
-    if (D == 576) return fp8 ? MlaMmaCfg<576, 512, true>::smem_bytes(batch)
-                             : MlaMmaCfg<576, 512, false>::smem_bytes(batch);
-    return fp8 ? MlaMmaCfg<320, 256, true>::smem_bytes(batch)
-               : MlaMmaCfg<320, 256, false>::smem_bytes(batch);
+    if (D == 576) return fp8 ? MlaMmaCfg<576, 512, true, MQA_MLA_TILE>::smem_bytes(batch)
+                             : MlaMmaCfg<576, 512, false, MQA_MLA_TILE>::smem_bytes(batch);
+    return fp8 ? MlaMmaCfg<320, 256, true, MQA_MLA_TILE>::smem_bytes(batch)
+               : MlaMmaCfg<320, 256, false, MQA_MLA_TILE>::smem_bytes(batch);
 }
 
 }  // namespace mqa

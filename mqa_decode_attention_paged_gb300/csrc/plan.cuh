@@ -153,4 +153,38 @@ struct PieceIter {
     }
 };
 
+// Producer-side flat walk over the tiles of a unit: `tile` tokens at a time,
+// skipping pieces that hold no token.  After next() returns true, tokens
+// [t0, min(t0 + tile, tok_end)) of request pc.b are the current tile and `bt`
+// points at that request's block-table row.
+struct TileCursor {
+    PieceIter it;
+    Piece pc;
+    int t0, tok_end, tile;
+    const int32_t* bt;
+
+    __device__ __forceinline__ void init(const Plan& plan, const int* cum, int T, int unit,
+                                         int tile_tokens) {
+        it.init(plan, cum, T, unit);
+        t0 = 0;
+        tok_end = 0;
+        tile = tile_tokens;
+        bt = nullptr;
+    }
+
+    __device__ __forceinline__ bool next(const Plan& plan, const int* cum,
+                                         const int32_t* __restrict__ seq_lens,
+                                         const int32_t* __restrict__ block_table) {
+        t0 += tile;
+        while (t0 >= tok_end) {
+            if (!it.next(cum, pc)) return false;
+            const int len = clamp_len(seq_lens[pc.b], plan.max_blocks, plan.page, nullptr);
+            t0 = pc.j0 * plan.page;
+            tok_end = min(pc.j1 * plan.page, len);
+            bt = block_table + static_cast<long long>(pc.b) * plan.max_blocks;
+        }
+        return true;
+    }
+};
+
 }  // namespace mqa

@@ -101,6 +101,7 @@ def _gqa(**kw):
     (dict(P=8), mqa.ERR_UNSUPPORTED),
     (dict(kvd=7), mqa.ERR_UNSUPPORTED),
     (dict(H=129), mqa.ERR_UNSUPPORTED),
+    (dict(B=4097), mqa.ERR_UNSUPPORTED),
     (dict(S=4, ws=None, wsb=0), mqa.ERR_WORKSPACE_TOO_SMALL),
     (dict(S=4, ws=FAKE, wsb=2 * 16 * 4 * 513 * 4 - 1), mqa.ERR_WORKSPACE_TOO_SMALL),
 ])
