@@ -13,9 +13,10 @@ copies (query, block table and lengths in; output and lse out) inside the
 timed region; `cpu_baseline` times the fp64 CPU oracle on the host cores.
 
 Timing: W untimed warm-up steps, then K steps.  Before every step a 256 MiB
-buffer (> the 129 MB L2) is overwritten so no KV line is L2-resident; each
-step is bracketed by CUDA events on the launching stream (the flush is outside
-the events).  Under torchrun every rank runs an independent replica (the path
+buffer (> the 129 MB L2) is overwritten and then read back, so no KV line is
+L2-resident and the flush's own dirty lines are written back before the timed
+region instead of during it; each step is bracketed by CUDA events on the
+launching stream (the flush is outside the events).  Under torchrun every rank runs an independent replica (the path
 has no cross-GPU exchange), the timed region is bracketed by a barrier and
 synchronize on both sides, and rank 0 reports the max over ranks.
 
@@ -94,7 +95,8 @@ def workload_config(case, name, splits):
            "seq_lens": spec["seq_lens"] if not isinstance(spec["seq_lens"], tuple) else list(spec["seq_lens"]),
            "total_tokens": int(case.seq_lens.astype(np.int64).sum()),
            "num_kv_splits": splits, "seed": spec["seed"],
-           "l2": "flushed before every timed step (256 MiB write, outside the timed events)"}
+           "l2": "flushed before every timed step: 256 MiB written then read back (cold, clean L2), "
+                 "outside the timed events"}
     if case.kind == "mla":
         cfg["kv_lora_rank"] = case.kv_lora_rank
     else:
@@ -269,6 +271,12 @@ def run_ours(args):
         need = mqa.gqa_paged_decode_workspace_bytes(B, H, D, splits)
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush32 = flush.view(torch.int32)
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+        flush32.max()  # read back: the dirty lines leave L2 before the timed call
+
     stream = torch.cuda.current_stream()
     launches_per_call = 1 if splits == 1 else 2
 
@@ -280,8 +288,8 @@ def run_ours(args):
             mqa.gqa_paged_decode(qq, kv, btt, sll, case.scale, case.k_scale, case.v_scale, out=oo,
                                  lse=ll, num_kv_splits=splits, workspace=ws, stream=stream)
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
+    for i in range(args.warmup):
+        flush_l2(i)
         call()
     torch.cuda.synchronize()
 
@@ -293,7 +301,7 @@ def run_ours(args):
     sampler = ClockSampler(dev.index if world == 1 else local)
     with sampler:
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush_l2(i)
             starts[i].record(stream)
             call()
             ends[i].record(stream)
@@ -315,7 +323,7 @@ def run_ours(args):
     es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     for i in range(e2e_steps + 2):
-        flush.fill_(i & 0xFF)
+        flush_l2(i)
         j = i - 2
         if j >= 0:
             es[j].record(stream)

@@ -86,6 +86,12 @@ const char* mqa_status_string(int status);
 /* Number of streaming multiprocessors of the current device, or -1. */
 int mqa_device_sm_count(void);
 
+/* The cudaError_t code (and its text) of the last CUDA runtime call that made
+ * an entry point of this library return MQA_ERR_CUDA on the calling thread;
+ * 0 / "no error" if none did.  Diagnostic only. */
+int mqa_last_cuda_error(void);
+const char* mqa_last_cuda_error_string(void);
+
 /* Split-count heuristic of the Triton MLA backend ("Triton と MLA" page,
  * 主要ファイル: _compute_num_kv_splits, and データフロー: the
  * VLLM_BATCH_INVARIANT branch): ceil(max_seq_len / 512), at least 1, at most

@@ -29,7 +29,10 @@ LIB_PATH = _build.LIB_PATH
 class MqaError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = int(code)
-        super().__init__(f"{where}: {status_string(code)} (status {code})")
+        msg = f"{where}: {status_string(code)} (status {code})"
+        if self.code == ERR_CUDA:
+            msg += f": {lib.mqa_last_cuda_error_string().decode()}"
+        super().__init__(msg)
 
 
 def _load() -> ctypes.CDLL:
@@ -45,6 +48,10 @@ def _load() -> ctypes.CDLL:
     lib.mqa_status_string.argtypes = [I]
     lib.mqa_device_sm_count.restype = I
     lib.mqa_device_sm_count.argtypes = []
+    lib.mqa_last_cuda_error.restype = I
+    lib.mqa_last_cuda_error.argtypes = []
+    lib.mqa_last_cuda_error_string.restype = ctypes.c_char_p
+    lib.mqa_last_cuda_error_string.argtypes = []
     lib.mqa_num_kv_splits.restype = I
     lib.mqa_num_kv_splits.argtypes = [I, I, I]
     lib.mla_decode_workspace_bytes.restype = SZ

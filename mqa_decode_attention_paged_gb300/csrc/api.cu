@@ -14,6 +14,14 @@
 
 namespace {
 
+// Last CUDA error seen by this thread inside the library (for diagnostics).
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+mqa_status cuda_fail(cudaError_t e) {
+    g_last_cuda_error = e;
+    return MQA_ERR_CUDA;
+}
+
 constexpr int kMaxBatch = mqa::kMaxBatchSmem;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -62,21 +70,24 @@ EncodeTiledFn encode_tiled_fn() {
 struct MapKey {
     const void* base;
     long long rows;
-    int cols, box_rows;
+    int cols, box_rows, fp8;
     bool operator==(const MapKey& o) const {
-        return base == o.base && rows == o.rows && cols == o.cols && box_rows == o.box_rows;
+        return base == o.base && rows == o.rows && cols == o.cols && box_rows == o.box_rows && fp8 == o.fp8;
     }
 };
 
-// Encodes (or returns a cached copy of) the 2D view {cols, rows} of a
-// row-major bf16 cache with {64, box_rows} boxes and the 128-byte swizzle.
-bool mla_tensor_map(CUtensorMap* out, const void* base, int cols, long long rows, int box_rows) {
+// Encodes (or returns a cached copy of) a 3D view of a row-major MLA cache
+// [rows, cols] whose box is `box_rows` whole rows: bf16 rows are viewed as
+// {64 elements, cols/64 panels, rows} with the 128-byte swizzle, e4m3 rows as
+// {inner, cols/inner, rows} (inner <= 256 bytes) without swizzle.  One copy of
+// the box fetches box_rows complete cache rows.
+bool mla_tensor_map(CUtensorMap* out, const void* base, int cols, long long rows, int box_rows, bool fp8) {
     constexpr int kSlots = 16;
     static std::mutex mu;
     static MapKey keys[kSlots];
     static CUtensorMap maps[kSlots];
     static int used = 0, next = 0;
-    const MapKey key{base, rows, cols, box_rows};
+    const MapKey key{base, rows, cols, box_rows, fp8 ? 1 : 0};
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
         if (keys[i] == key) {
@@ -87,12 +98,17 @@ bool mla_tensor_map(CUtensorMap* out, const void* base, int cols, long long rows
     if (!fn) return false;
     CUtensorMap m;
     std::memset(&m, 0, sizeof m);
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t elem[2] = {1, 1};
-    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const int inner = fp8 ? (cols % 192 == 0 ? 192 : 160) : 64;  // elements
+    const int elt = fp8 ? 1 : 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(cols / inner),
+                                static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * elt, static_cast<cuuint64_t>(cols) * elt};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(cols / inner),
+                               static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    if (fn(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+           const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     const int slot = used < kSlots ? used++ : (next++ % kSlots);
@@ -122,6 +138,10 @@ const char* mqa_status_string(int status) {
 }
 
 int mqa_device_sm_count(void) { return sm_count_current(); }
+
+int mqa_last_cuda_error(void) { return static_cast<int>(g_last_cuda_error); }
+
+const char* mqa_last_cuda_error_string(void) { return cudaGetErrorString(g_last_cuda_error); }
 
 int mqa_num_kv_splits(int max_seq_len, int sm_count, int batch_invariant) {
     if (batch_invariant) return 1;
@@ -192,20 +212,21 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
     a.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
     a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms / groups);
 
-    if (!fp8) {
+    {
         // tensor boxes never straddle a page: 64 rows when pages are multiples
         // of 64 tokens, else 32 or 16
         const int tile = mqa::mla_mma_tile();
         int br = (page_size % 64 == 0) ? 64 : (page_size % 32 == 0 ? 32 : 16);
         if (br > tile) br = tile;
         a.box_rows = br;
-        if (!mla_tensor_map(&a.tmap, kv_cache, head_size, static_cast<long long>(num_blocks) * page_size, br))
-            return MQA_ERR_CUDA;
+        if (!mla_tensor_map(&a.tmap, kv_cache, head_size, static_cast<long long>(num_blocks) * page_size, br,
+                            fp8))
+            return cuda_fail(cudaErrorInvalidValue);
     }
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (mqa::mla_mma_stage1(a, head_size, fp8, a.plan.units * groups, st) != cudaSuccess)
-        return MQA_ERR_CUDA;
+    if (cudaError_t e = mqa::mla_mma_stage1(a, head_size, fp8, a.plan.units * groups, st); e != cudaSuccess)
+        return cuda_fail(e);
     if (!a.plan.per_seq) {
         mqa::MergeArgs m{};
         m.ws_o = a.ws_o;
@@ -218,7 +239,7 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
         m.H = num_heads;
         m.R = kv_lora_rank;
         m.plan = a.plan;
-        if (mqa::lse_merge(m, st) != cudaSuccess) return MQA_ERR_CUDA;
+        if (cudaError_t e = mqa::lse_merge(m, st); e != cudaSuccess) return cuda_fail(e);
     }
     return MQA_OK;
 }
@@ -278,7 +299,7 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
     a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (mqa::gqa_mma_stage1(a, head_size, a.plan.units, st) != cudaSuccess) return MQA_ERR_CUDA;
+    if (cudaError_t e = mqa::gqa_mma_stage1(a, head_size, a.plan.units, st); e != cudaSuccess) return cuda_fail(e);
     if (!a.plan.per_seq) {
         mqa::MergeArgs m{};
         m.ws_o = a.ws_o;
@@ -291,7 +312,7 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
         m.H = num_q_heads;
         m.R = head_size;
         m.plan = a.plan;
-        if (mqa::lse_merge(m, st) != cudaSuccess) return MQA_ERR_CUDA;
+        if (cudaError_t e = mqa::lse_merge(m, st); e != cudaSuccess) return cuda_fail(e);
     }
     return MQA_OK;
 }

@@ -14,11 +14,11 @@ namespace mqa {
 constexpr int kMaxMergeUnits = 1024;
 
 // Largest batch whose page prefix the stage-1 kernels keep in shared memory.
-constexpr int kMaxBatchSmem = 4096;
+constexpr int kMaxBatchSmem = 2048;
 
 struct MlaArgs {
-    // 2D tiled view of a bf16 cache: dims {D, num_blocks * page}, boxes of
-    // {64 columns, box_rows rows}, 128-byte swizzle (unused for e4m3 caches).
+    // 3D tiled view of the cache whose box is box_rows whole cache rows
+    // (bf16: 64-element panels with the 128-byte swizzle; e4m3: unswizzled).
     CUtensorMap tmap;
     int box_rows;
     const __nv_bfloat16* q;

@@ -95,29 +95,31 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
-// Tiled 2D tensor copy global -> shared (box given by the tensor map) that
-// completes its bytes on `bar`.  x (innermost, elements) must be a multiple of
-// 16 bytes' worth of elements; the map lives in kernel parameter space.
-__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,
-                                            uint64_t policy) {
+// Tiled 3D tensor copy global -> shared (box given by the tensor map, which
+// lives in kernel parameter space) that completes its bytes on `bar`.  The
+// innermost coordinate x must be a multiple of 16 bytes' worth of elements.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z,
+                                            uint64_t* bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// Byte offset of bf16 element (row, col) in a tile of whole cache rows (row
+// stride = panels * 128 bytes) written by a 128-byte-swizzled tensor copy of
+// box {64, panels, rows}: 128-byte line L = row * panels + col / 64 holds its
+// 16-byte chunks permuted by XOR with L % 8.  With an odd panel count eight
+// consecutive rows of one panel fall on eight different chunk slots, so
+// ldmatrix over them is bank-conflict free.
+__device__ __forceinline__ uint32_t swz_rows(int row, int col, int panels) {
+    const int line = row * panels + (col >> 6);
+    return static_cast<uint32_t>(line * 128 + ((((col & 63) >> 3) ^ (line & 7)) << 4) + (col & 7) * 2);
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
-}
-
-// Byte offset of bf16 element (row, col) in a tile held as 64-column panels
-// of `rows` 128-byte rows with the 128-byte swizzle (16-byte chunk index XOR
-// row % 8), the layout a SWIZZLE_128B tensor copy writes into 1024-byte
-// aligned shared memory.
-__device__ __forceinline__ uint32_t swz128(int row, int col, int rows) {
-    const int panel = col >> 6, chunk = (col & 63) >> 3;
-    return static_cast<uint32_t>(panel * rows * 128 + row * 128 + ((chunk ^ (row & 7)) << 4) + (col & 7) * 2);
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -151,6 +153,18 @@ static cudaError_t launch_with_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 blo
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
+// ---- 16-byte asynchronous global -> shared copies (cp.async) -------------------
+
+// Copies `src_bytes` (16 or 0) bytes and zero-fills the rest of the 16-byte
+// destination chunk.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ---- named barriers ---------------------------------------------------------
 

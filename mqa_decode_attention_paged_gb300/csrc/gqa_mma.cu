@@ -35,7 +35,7 @@ struct GqaCfg {
     __host__ __device__ static size_t off_bars(int hkv) { return off_masks(hkv) + 8 * stages(hkv); }
     __host__ __device__ static size_t off_flags(int hkv) { return off_bars(hkv) + 16 * stages(hkv); }
     __host__ __device__ static size_t off_cum(int hkv) { return off_flags(hkv) + 16; }
-    static size_t smem_bytes(int hkv, int batch) { return off_cum(hkv) + 4 * (batch + 1); }
+    static size_t smem_bytes(int hkv, int batch) { return off_cum(hkv) + 4 * (2 * batch + 1); }
 };
 
 template <int D>
@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::off_bars(Hkv));
     uint64_t* empty = full + nstage;
     int* cum = reinterpret_cast<int*>(smem + C::off_cum(Hkv));
+    int* lens = cum + a.plan.batch + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int unit = blockIdx.x;
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
     fence_proxy_async_smem();
     pdl_wait();
     pdl_launch_dependents();
-    const int T = build_cum(a.plan, a.seq_lens, cum, a.status);
+    const int T = build_cum(a.plan, a.seq_lens, cum, lens, a.status);
     const int P = a.plan.page;
 
     if (warp == Hkv) {
@@ -85,12 +86,12 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
         // lane -> (plane, token): lanes 0-15 copy K rows, 16-31 V rows.
         const int plane = lane >> 4, r = lane & 15;
         // block id of this lane's row, fetched one tile ahead of its use
-        bool have = cur.next(a.plan, cum, a.seq_lens, a.block_table);
+        bool have = cur.next(a.plan, cum, lens, a.block_table);
         int t0 = cur.t0;
         bool val = have && t0 + r < cur.tok_end;
         int blk = val ? cur.bt[(t0 + r) / P] : 0;
         while (have) {
-            const bool have_next = cur.next(a.plan, cum, a.seq_lens, a.block_table);
+            const bool have_next = cur.next(a.plan, cum, lens, a.block_table);
             const bool nval = have_next && cur.t0 + r < cur.tok_end;
             const int nblk = nval ? cur.bt[(cur.t0 + r) / P] : 0;
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
     bool aborted = false;
 
     while (!aborted && it.next(cum, pc)) {
-        const int len = clamp_len(a.seq_lens[pc.b], a.plan.max_blocks, P, nullptr);
+        const int len = lens[pc.b];
         const int tok0 = pc.j0 * P;
         const int tok_end = min(pc.j1 * P, len);
         const int hq0 = gk * grp;

@@ -34,15 +34,13 @@ struct MlaMmaCfg {
     static constexpr int kHeads = 16;
     static constexpr int kTile = TILE;                         // tokens per stage
     static constexpr int kHalf = kTile / 2;                    // tokens per QK warp
-    static constexpr int kRowsPerLane = kTile / 32;            // fp8 producer rows per lane
     static constexpr int kTokPerThread = kTile / 16;           // softmax tokens per thread
     static constexpr int kConsumerWarps = 8;
     static constexpr int kConsumers = 32 * kConsumerWarps;
     static constexpr int kThreads = kConsumers + 32;
     static constexpr int kPanels = D / 64;                     // 64-column bf16 panels
     static constexpr int kOpBytes = kPanels * kTile * 128;     // swizzled bf16 operand tile
-    static constexpr int kFp8Stride = D + 16;                  // padded e4m3 staging row
-    static constexpr int kStageBytes = FP8 ? kTile * kFp8Stride : kOpBytes;
+    static constexpr int kStageBytes = kTile * D * (FP8 ? 1 : 2);  // whole cache rows
     static constexpr int kKSteps = D / 16;
     static constexpr int kKq = kKSteps / 4;                    // k-steps per head-dim quarter
     static constexpr int kColsPerWarp = R / kConsumerWarps;    // output columns per warp
@@ -50,18 +48,21 @@ struct MlaMmaCfg {
     static constexpr int kRedStride = kTile + 8;               // floats
     static constexpr int kPStride = kTile + 8;                 // bf16 elements
 
+    static constexpr int kQStride = D * 2 + 16;                // padded smem Q row (bytes)
+    static constexpr int kQBytes = 2 * kHeads * kQStride;      // double-buffered Q slot
     static constexpr int kRedBytes = 4 * kHeads * kRedStride * 4;
     static constexpr int kPBytes = kHeads * kPStride * 2;
     static constexpr int kMiscBytes = kHeads * 4 + kHeads * 8 + 8 * 8 + 16 * 8 + 16;
-    static constexpr int kFixed = 1024 + (FP8 ? kOpBytes : 0) + kRedBytes + kPBytes + kMiscBytes +
-                                  4 * (kMaxBatchSmem + 1) + 1024;
+    static constexpr int kFixed = 1024 + (FP8 ? kOpBytes : 0) + kQBytes + kRedBytes + kPBytes + kMiscBytes +
+                                  4 * (2 * kMaxBatchSmem + 1) + 1024;
     static constexpr int kStagesFit = (227 * 1024 - kFixed) / kStageBytes;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
 
     static constexpr int align1k(int x) { return (x + 1023) & ~1023; }
     static constexpr int kOffStages = 0;
     static constexpr int kOffOp = align1k(kStages * kStageBytes);
-    static constexpr int kOffRed = kOffOp + (FP8 ? kOpBytes : 0);
+    static constexpr int kOffQ = kOffOp + (FP8 ? kOpBytes : 0);
+    static constexpr int kOffRed = kOffQ + kQBytes;
     static constexpr int kOffP = kOffRed + kRedBytes;
     static constexpr int kOffAlpha = kOffP + kPBytes;
     static constexpr int kOffMl = kOffAlpha + kHeads * 4;
@@ -70,14 +71,15 @@ struct MlaMmaCfg {
     static constexpr int kOffFlags = kOffBars + 16 * 8;
     static constexpr int kOffCum = kOffFlags + 16;
     // +1024: the dynamic window is re-aligned to 1024 bytes in the kernel
-    static size_t smem_bytes(int batch) { return 1024 + kOffCum + 4 * (batch + 1); }
+    static size_t smem_bytes(int batch) { return 1024 + kOffCum + 4 * (2 * batch + 1); }
 
     static_assert(kTile == 32 || kTile == 64, "tile of 32 or 64 tokens");
     static_assert(kStages >= 2, "at least two pipeline stages");
     static_assert(D % 64 == 0 && kKSteps % 4 == 0, "head size must split into 4 quarters");
     static_assert(kColsPerWarp % 16 == 0, "P.V columns per warp must be a multiple of 16");
-    static_assert(D % 16 == 0, "bulk copies need 16-byte rows");
-    static_assert(1024 + kOffCum + 4 * (kMaxBatchSmem + 1) <= 227 * 1024, "shared memory budget");
+    static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+    static_assert(kPanels % 2 == 1, "odd panel count keeps ldmatrix conflict free");
+    static_assert(1024 + kOffCum + 4 * (2 * kMaxBatchSmem + 1) <= 227 * 1024, "shared memory budget");
 };
 
 template <int D, int R, bool FP8, int TILE>
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
     uint64_t* empty = full + C::kStages;
     int* abort_s = reinterpret_cast<int*>(smem + C::kOffFlags);
     int* cum = reinterpret_cast<int*>(smem + C::kOffCum);
+    int* lens = cum + a.plan.batch + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_groups = (a.H + C::kHeads - 1) / C::kHeads;
@@ -111,7 +114,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
         }
         *abort_s = 0;
         fence_mbar_init();
-        if constexpr (!FP8) prefetch_tmap(&a.tmap);
+        prefetch_tmap(&a.tmap);
     }
     // Zero the staging ring (and the widened operand tile) once so that rows
     // never written by a copy hold finite values.
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
     // Inputs may come from the previous grid in the stream.
     pdl_wait();
     pdl_launch_dependents();
-    const int T = build_cum(a.plan, a.seq_lens, cum, a.status);  // contains __syncthreads
+    const int T = build_cum(a.plan, a.seq_lens, cum, lens, a.status);  // contains __syncthreads
 
     const int P = a.plan.page;
 
@@ -134,28 +137,25 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
         uint32_t phase = 0;
         int issued[C::kStages];
         for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
-        const int BR = FP8 ? 1 : a.box_rows;          // rows per tensor box (bf16)
-        const int nbox = FP8 ? C::kRowsPerLane : C::kTile / BR;
+        const int BR = a.box_rows;  // rows per tensor box (never straddles a page)
+        const int nbox = C::kTile / BR;
+        constexpr int kRowBytes = D * (FP8 ? 1 : 2);
 
-        // Block ids of the next tile, fetched one tile ahead of their use.
-        // bf16: lane k < nbox holds box k; e4m3: slot k holds row lane + 32k.
-        auto fetch = [&](const TileCursor& tc, int (&blk)[C::kRowsPerLane], bool (&val)[C::kRowsPerLane]) {
-#pragma unroll
-            for (int k = 0; k < C::kRowsPerLane; ++k) {
-                const int tok = FP8 ? tc.t0 + lane + 32 * k : tc.t0 + lane * BR;
-                val[k] = (FP8 || (k == 0 && lane < nbox)) && tok < tc.tok_end;
-                blk[k] = val[k] ? tc.bt[tok / P] : 0;
-            }
+        // Block id of box `lane` of the next tile, fetched one tile ahead.
+        auto fetch = [&](const TileCursor& tc, int& blk, bool& val) {
+            const int tok = tc.t0 + lane * BR;
+            val = lane < nbox && tok < tc.tok_end;
+            blk = val ? tc.bt[tok / P] : 0;
         };
-        bool have = cur.next(a.plan, cum, a.seq_lens, a.block_table);
-        int blk[C::kRowsPerLane];
-        bool val[C::kRowsPerLane];
+        bool have = cur.next(a.plan, cum, lens, a.block_table);
+        int blk = 0;
+        bool val = false;
         int t0 = cur.t0, tend = cur.tok_end;
         if (have) fetch(cur, blk, val);
         while (have) {
-            const bool have_next = cur.next(a.plan, cum, a.seq_lens, a.block_table);
-            int nblk[C::kRowsPerLane];
-            bool nval[C::kRowsPerLane];
+            const bool have_next = cur.next(a.plan, cum, lens, a.block_table);
+            int nblk = 0;
+            bool nval = false;
             if (have_next) fetch(cur, nblk, nval);
 
             if (!mbar_wait(&empty[stage], phase ^ 1)) {
@@ -163,64 +163,27 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
                 break;
             }
             uint8_t* dst = stages + stage * C::kStageBytes;
-#pragma unroll
-            for (int k = 0; k < C::kRowsPerLane; ++k) {
-                if (val[k] && (blk[k] < 0 || blk[k] >= a.num_blocks)) {
-                    report(a.status, MQA_ERR_DEVICE_CHECK);
-                    val[k] = false;
-                }
+            if (val && (blk < 0 || blk >= a.num_blocks)) {
+                report(a.status, MQA_ERR_DEVICE_CHECK);
+                val = false;
             }
+            // One tensor copy per box of BR whole rows.  Rows of a box past
+            // the sequence end arrive too; the consumers mask their logits
+            // and zero their V columns.
+            const uint32_t bm = __ballot_sync(0xffffffffu, val);
             const int n_tok = tend - t0;
-            const uint64_t live = n_tok >= 64 ? ~0ull : ((1ull << n_tok) - 1);
-            if constexpr (FP8) {
-                // one bulk copy per e4m3 row, invalid rows zero-filled here
-                uint64_t vmask = 0;
-#pragma unroll
-                for (int k = 0; k < C::kRowsPerLane; ++k) {
-                    if (!val[k]) {
-                        uint4* row = reinterpret_cast<uint4*>(dst + (lane + 32 * k) * C::kFp8Stride);
-                        for (int c = 0; c < D / 16; ++c) row[c] = make_uint4(0, 0, 0, 0);
-                        fence_proxy_async_smem();
-                    }
-                    vmask |= static_cast<uint64_t>(__ballot_sync(0xffffffffu, val[k])) << (32 * k);
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    mask_s[stage] = vmask;
-                    mbar_arrive_expect_tx(&full[stage], __popcll(vmask) * D);
-                }
-                __syncwarp();
-#pragma unroll
-                for (int k = 0; k < C::kRowsPerLane; ++k) {
-                    if (val[k]) {
-                        const int tok = t0 + lane + 32 * k;
-                        const uint8_t* src = a.kv + (static_cast<long long>(blk[k]) * P + tok % P) * D;
-                        bulk_g2s(dst + (lane + 32 * k) * C::kFp8Stride, src, D, &full[stage], pol);
-                    }
-                }
-            } else {
-                // one tensor copy per (box, 64-column panel); rows of a box
-                // past the sequence end are zeroed by the consumers
-                const uint32_t bm = __ballot_sync(0xffffffffu, val[0]) & ((1u << nbox) - 1);
-                uint64_t boxbits = 0;
-                for (int bx = 0; bx < nbox; ++bx)
-                    if ((bm >> bx) & 1u) boxbits |= (BR == 64 ? ~0ull : ((1ull << BR) - 1)) << (bx * BR);
-                int bblk[4];
-#pragma unroll
-                for (int bx = 0; bx < 4; ++bx) bblk[bx] = __shfl_sync(0xffffffffu, blk[0], bx);
-                if (lane == 0) {
-                    mask_s[stage] = boxbits & live;
-                    mbar_arrive_expect_tx(&full[stage], __popc(bm) * BR * 128 * C::kPanels);
-                }
-                __syncwarp();
-                for (int i = lane; i < nbox * C::kPanels; i += 32) {
-                    const int bx = i / C::kPanels, pn = i % C::kPanels;
-                    if ((bm >> bx) & 1u) {
-                        const int row = bblk[bx] * P + (t0 + bx * BR) % P;
-                        tma_load_2d(dst + pn * C::kTile * 128 + bx * BR * 128, &a.tmap, pn * 64, row,
-                                    &full[stage], pol);
-                    }
-                }
+            uint64_t vmask = n_tok >= 64 ? ~0ull : ((1ull << n_tok) - 1);
+            const uint64_t box_ones = BR == 64 ? ~0ull : ((1ull << BR) - 1);
+            for (int bx = 0; bx < nbox; ++bx)
+                if (!((bm >> bx) & 1u)) vmask &= ~(box_ones << (bx * BR));
+            if (lane == 0) {
+                mask_s[stage] = vmask;
+                mbar_arrive_expect_tx(&full[stage], __popc(bm) * BR * kRowBytes);
+            }
+            __syncwarp();
+            if (val) {
+                const int row = blk * P + (t0 + lane * BR) % P;
+                tma_load_3d(dst + lane * BR * kRowBytes, &a.tmap, 0, 0, row, &full[stage], pol);
             }
             issued[stage] = static_cast<int>(phase);
             if (++stage == C::kStages) {
@@ -230,11 +193,8 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
             have = have_next;
             t0 = cur.t0;
             tend = cur.tok_end;
-#pragma unroll
-            for (int k = 0; k < C::kRowsPerLane; ++k) {
-                blk[k] = nblk[k];
-                val[k] = nval[k];
-            }
+            blk = nblk;
+            val = nval;
         }
         // Never leave copies in flight behind: wait (bounded) for the last
         // fill of every stage.
@@ -252,32 +212,53 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
     constexpr int kTPT = C::kTokPerThread;
     constexpr uint64_t kFullMask = C::kTile == 64 ? ~0ull : ((1ull << C::kTile) - 1);
 
+    // Q rows h0 .. h0+15 of request b are staged into one of two padded smem
+    // slots with cp.async one piece ahead of their use (rows beyond H are
+    // zero-filled); each warp then builds its A fragments with ldmatrix.
+    uint8_t* qslot = smem + C::kOffQ;
+    auto stage_q = [&](int b, int buf) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(a.q + (static_cast<long long>(b) * a.H + h0) * D);
+        uint8_t* dst = qslot + buf * C::kHeads * C::kQStride;
+        for (int i = t; i < C::kHeads * (D / 8); i += C::kConsumers) {
+            const int row = i / (D / 8), ch = i % (D / 8);
+            const bool live = h0 + row < a.H;
+            cp_async_16(dst + row * C::kQStride + ch * 16, live ? src + (row * D + ch * 8) * 2 : src,
+                        live ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    auto load_q = [&](int buf, uint32_t (&qf)[C::kKq][4]) {
+        const uint8_t* base = qslot + buf * C::kHeads * C::kQStride;
+#pragma unroll
+        for (int ks = 0; ks < C::kKq; ++ks) {
+            const int col = (dq * C::kKq + ks) * 16 + (lane >> 4) * 8;
+            ldsm_x4(qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], base + (lane & 15) * C::kQStride + col * 2);
+        }
+    };
+
     PieceIter it;
     it.init(a.plan, cum, T, unit);
     Piece pc;
     int stage = 0;
     uint32_t phase = 0;
     bool aborted = false;
+    bool have = it.next(cum, pc);
+    int qbuf = 0;
+    if (have) stage_q(pc.b, 0);
 
-    while (!aborted && it.next(cum, pc)) {
-        const int len = clamp_len(a.seq_lens[pc.b], a.plan.max_blocks, P, nullptr);
+    while (!aborted && have) {
+        const int len = lens[pc.b];
         const int tok0 = pc.j0 * P;
         const int tok_end = min(pc.j1 * P, len);
-
-        // Q fragments of this warp's head-dim quarter (rows beyond H are zero).
+        Piece nxt;
+        const bool have_next = it.next(cum, nxt);
         uint32_t qa[C::kKq][4];
-        {
-            const __nv_bfloat16* qb = a.q + (static_cast<long long>(pc.b) * a.H + h0) * D;
-            const bool r0 = h0 + g < a.H, r1 = h0 + g + 8 < a.H;
-#pragma unroll
-            for (int ks = 0; ks < C::kKq; ++ks) {
-                const int k0 = (dq * C::kKq + ks) * 16 + 2 * c;
-                qa[ks][0] = r0 ? *reinterpret_cast<const uint32_t*>(qb + g * D + k0) : 0u;
-                qa[ks][1] = r1 ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + k0) : 0u;
-                qa[ks][2] = r0 ? *reinterpret_cast<const uint32_t*>(qb + g * D + k0 + 8) : 0u;
-                qa[ks][3] = r1 ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + k0 + 8) : 0u;
-            }
-        }
+        cp_async_wait_all();
+        named_bar_sync(4, C::kConsumers);  // this piece's Q slot is complete
+        load_q(qbuf, qa);
+        // the other slot held the previous piece's Q, read before its epilogue
+        if (have_next) stage_q(nxt.b, qbuf ^ 1);
+
         float o[C::kNbPV][4];
 #pragma unroll
         for (int i = 0; i < C::kNbPV; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -301,7 +282,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
                     constexpr int kChunks = C::kTile * (D / 16);
                     for (int i = t; i < kChunks; i += C::kConsumers) {
                         const int r = i / (D / 16), cc = i % (D / 16);
-                        const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + r * C::kFp8Stride + cc * 16);
+                        const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + r * D + cc * 16);
                         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                         uint32_t outw[8];
 #pragma unroll
@@ -315,16 +296,17 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
                                 outw[2 * j + hh] = pack_bf16x2(f.x, f.y);
                             }
                         }
-                        *reinterpret_cast<uint4*>(op + swz128(r, 16 * cc, C::kTile)) =
+                        *reinterpret_cast<uint4*>(op + swz_rows(r, 16 * cc, C::kPanels)) =
                             make_uint4(outw[0], outw[1], outw[2], outw[3]);
-                        *reinterpret_cast<uint4*>(op + swz128(r, 16 * cc + 8, C::kTile)) =
+                        *reinterpret_cast<uint4*>(op + swz_rows(r, 16 * cc + 8, C::kPanels)) =
                             make_uint4(outw[4], outw[5], outw[6], outw[7]);
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[stage]);
                 named_bar_sync(3, C::kConsumers);
-            } else if (vmask != kFullMask) {
+            }
+            if (vmask != kFullMask) {
                 // Rows past the sequence end may hold anything (the tail of a
                 // page, or an earlier tile): zero them in the V columns this
                 // warp reads, so P = 0 never meets a NaN.  K columns of those
@@ -334,7 +316,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
                     const int r = i / kChunksPerWarp;
                     if (!((vmask >> r) & 1ull)) {
                         const int col = warp * C::kColsPerWarp + (i % kChunksPerWarp) * 8;
-                        *reinterpret_cast<uint4*>(op + swz128(r, col, C::kTile)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(op + swz_rows(r, col, C::kPanels)) = make_uint4(0, 0, 0, 0);
                     }
                 }
                 zeroed = true;
@@ -354,7 +336,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
                         const int row = th * C::kHalf + nb2 * 16 + (lane & 7) + ((lane >> 4) << 3);
                         const int col = k0 + ((lane >> 3) & 1) * 8;
                         uint32_t b0, b1, b2, b3;
-                        ldsm_x4(b0, b1, b2, b3, op + swz128(row, col, C::kTile));
+                        ldsm_x4(b0, b1, b2, b3, op + swz_rows(row, col, C::kPanels));
                         mma_bf16_16816(sacc[2 * nb2], qa[ks], b0, b1);
                         mma_bf16_16816(sacc[2 * nb2 + 1], qa[ks], b2, b3);
                     }
@@ -444,7 +426,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
                             const int tok = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
                             const int col = warp * C::kColsPerWarp + nb2 * 16 + (lane >> 4) * 8;
                             uint32_t b0, b1, b2, b3;
-                            ldsm_x4_t(b0, b1, b2, b3, op + swz128(tok, col, C::kTile));
+                            ldsm_x4_t(b0, b1, b2, b3, op + swz_rows(tok, col, C::kPanels));
                             mma_bf16_16816(o[2 * nb2], pa, b0, b1);
                             mma_bf16_16816(o[2 * nb2 + 1], pa, b2, b3);
                         }
@@ -506,7 +488,11 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
             }
         }
         named_bar_sync(1, C::kConsumers);
+        pc = nxt;
+        have = have_next;
+        qbuf ^= 1;
     }
+    cp_async_wait_all();
 }
 
 // Tile size (tokens per pipeline stage; 32 or 64).  The number of stages is

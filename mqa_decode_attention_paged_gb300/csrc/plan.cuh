@@ -45,12 +45,14 @@ __device__ __forceinline__ int clamp_len(int n, int max_blocks, int page, int* s
     return n;
 }
 
-// Fill cum[0..B] (shared memory) with the exclusive page prefix; every thread
-// of the block must call this.  Returns T = cum[B].
+// Fill cum[0..B] (shared memory) with the exclusive page prefix and lens[b]
+// with the clamped request lengths; every thread of the block must call this.
+// Returns T = cum[B].
 __device__ __forceinline__ int build_cum(const Plan& p, const int32_t* __restrict__ seq_lens,
-                                         int* cum, int* status) {
+                                         int* cum, int* lens, int* status) {
     for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
         const int n = clamp_len(seq_lens[i], p.max_blocks, p.page, status);
+        lens[i] = n;
         cum[i + 1] = (n + p.page - 1) / p.page;
     }
     if (threadIdx.x == 0) cum[0] = 0;
@@ -172,15 +174,13 @@ struct TileCursor {
         bt = nullptr;
     }
 
-    __device__ __forceinline__ bool next(const Plan& plan, const int* cum,
-                                         const int32_t* __restrict__ seq_lens,
+    __device__ __forceinline__ bool next(const Plan& plan, const int* cum, const int* lens,
                                          const int32_t* __restrict__ block_table) {
         t0 += tile;
         while (t0 >= tok_end) {
             if (!it.next(cum, pc)) return false;
-            const int len = clamp_len(seq_lens[pc.b], plan.max_blocks, plan.page, nullptr);
             t0 = pc.j0 * plan.page;
-            tok_end = min(pc.j1 * plan.page, len);
+            tok_end = min(pc.j1 * plan.page, lens[pc.b]);
             bt = block_table + static_cast<long long>(pc.b) * plan.max_blocks;
         }
         return true;
