@@ -44,10 +44,13 @@ if ROOT not in sys.path:
 METRIC = "MLA decode µs/call, KV GB/s and % of roofline at B×H×seq_len (1 GB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per decode call
-# from one ncu capture, keyed by workload; valid only while the kernel sources
-# hash to `src_sha`.
-NCU_TRAFFIC = {}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one stage-1
+# launch from an ncu capture (summaries under profiles/), keyed by workload;
+# valid only while the kernel sources hash to `src_sha`.
+NCU_TRAFFIC = {
+    "mla_v2lite": {"src_sha": "720d253541ee62e8", "splits": 16, "bytes": 329808128 + 4158208,
+                   "kernel": "mla_decode_mma_kernel<576,512,0,64>"},
+}
 
 
 def kernel_sources_sha() -> str:
@@ -355,8 +358,10 @@ def run_ours(args):
     bound = "hbm" if t_hbm >= t_tc else "tensor"
     traffic = None
     tr = NCU_TRAFFIC.get(args.workload)
+    traffic_kernel = None
     if tr and tr.get("src_sha") == kernel_sources_sha() and tr.get("splits") == splits:
         traffic = tr["bytes"]
+        traffic_kernel = tr["kernel"] + " (stage 1 only)"
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": round(alg_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(alg_gbs / peaks["hbm_gbs"], 4)}
@@ -364,6 +369,7 @@ def run_ours(args):
         roof = {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(tflops / peaks["bf16_tflops"], 4)}
     roof["traffic"] = traffic
+    roof["traffic_kernel"] = traffic_kernel
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     roof["kernel"] = "decode call: split-KV stage-1 kernel + LSE merge"
     roof["alg_bytes_per_call"] = st["alg_bytes"]
