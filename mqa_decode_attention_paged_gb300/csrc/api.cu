@@ -70,11 +70,56 @@ EncodeTiledFn encode_tiled_fn() {
 struct MapKey {
     const void* base;
     long long rows;
-    int cols, box_rows, fp8;
+    int cols, box_rows, kind;  // kind: 0 = 3D bf16 rows, 1 = 3D e4m3 rows, 2 = 2D bf16 panels
     bool operator==(const MapKey& o) const {
-        return base == o.base && rows == o.rows && cols == o.cols && box_rows == o.box_rows && fp8 == o.fp8;
+        return base == o.base && rows == o.rows && cols == o.cols && box_rows == o.box_rows && kind == o.kind;
     }
 };
+
+constexpr int kMapSlots = 32;
+std::mutex g_map_mu;
+MapKey g_map_keys[kMapSlots];
+CUtensorMap g_maps[kMapSlots];
+int g_map_used = 0, g_map_next = 0;
+
+bool map_lookup(const MapKey& key, CUtensorMap* out) {
+    for (int i = 0; i < g_map_used; ++i)
+        if (g_map_keys[i] == key) {
+            *out = g_maps[i];
+            return true;
+        }
+    return false;
+}
+
+void map_store(const MapKey& key, const CUtensorMap& m) {
+    const int slot = g_map_used < kMapSlots ? g_map_used++ : (g_map_next++ % kMapSlots);
+    g_map_keys[slot] = key;
+    g_maps[slot] = m;
+}
+
+// 2D view {cols, rows} of a row-major bf16 matrix with {64, box_rows} boxes and
+// the 128-byte swizzle: one copy lands one 64-column panel of box_rows rows in
+// the canonical K-major layout of the tensor cores.
+bool bf16_panel_map(CUtensorMap* out, const void* base, int cols, long long rows, int box_rows) {
+    const MapKey key{base, rows, cols, box_rows, 2};
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (map_lookup(key, out)) return true;
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof m);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t elem[2] = {1, 1};
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    map_store(key, m);
+    *out = m;
+    return true;
+}
 
 // Encodes (or returns a cached copy of) a 3D view of a row-major MLA cache
 // [rows, cols] whose box is `box_rows` whole rows: bf16 rows are viewed as
@@ -82,18 +127,9 @@ struct MapKey {
 // {inner, cols/inner, rows} (inner <= 256 bytes) without swizzle.  One copy of
 // the box fetches box_rows complete cache rows.
 bool mla_tensor_map(CUtensorMap* out, const void* base, int cols, long long rows, int box_rows, bool fp8) {
-    constexpr int kSlots = 16;
-    static std::mutex mu;
-    static MapKey keys[kSlots];
-    static CUtensorMap maps[kSlots];
-    static int used = 0, next = 0;
     const MapKey key{base, rows, cols, box_rows, fp8 ? 1 : 0};
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < used; ++i)
-        if (keys[i] == key) {
-            *out = maps[i];
-            return true;
-        }
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (map_lookup(key, out)) return true;
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
     CUtensorMap m;
@@ -111,9 +147,7 @@ bool mla_tensor_map(CUtensorMap* out, const void* base, int cols, long long rows
            fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
-    const int slot = used < kSlots ? used++ : (next++ % kSlots);
-    keys[slot] = key;
-    maps[slot] = m;
+    map_store(key, m);
     *out = m;
     return true;
 }
@@ -190,6 +224,54 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
     const bool fp8 = kv_dtype == MQA_KV_FP8_E4M3;
     const int groups = (num_heads + 15) / 16;
 
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t slots_tc = static_cast<size_t>(batch) * num_kv_splits;
+
+    // 65..128 heads over a bf16 cache: 2-CTA tensor-core clusters
+    if (num_heads > 64 && !fp8 && batch <= mqa::kMaxBatchTc) {
+        mqa::MlaTcArgs t{};
+        // boxes never straddle a page and never exceed a pipeline tile
+        int br = (page_size % 64 == 0) ? 64 : (page_size % 32 == 0 ? 32 : 16);
+        if (br > mqa::mla_tc_tile()) br = mqa::mla_tc_tile();
+        t.box_rows = br;
+        if (!bf16_panel_map(&t.kv_map, kv_cache, head_size, static_cast<long long>(num_blocks) * page_size, br) ||
+            !bf16_panel_map(&t.q_map, q, head_size, static_cast<long long>(batch) * num_heads, 128))
+            return cuda_fail(cudaErrorInvalidValue);
+        t.block_table = block_table;
+        t.seq_lens = seq_lens;
+        t.out = static_cast<__nv_bfloat16*>(out);
+        t.lse = lse;
+        t.ws_o = static_cast<float*>(workspace);
+        t.ws_lse = need > 0 ? t.ws_o + slots_tc * num_heads * kv_lora_rank : nullptr;
+        t.status = device_status;
+        t.sl2 = scale * mqa::kLog2e;
+        t.out_scale = 1.0f;
+        t.H = num_heads;
+        t.num_blocks = num_blocks;
+        t.plan.batch = batch;
+        t.plan.page = page_size;
+        t.plan.max_blocks = max_blocks;
+        t.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
+        t.plan.units = t.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms / 2);
+        if (cudaError_t e = mqa::mla_tc_stage1(t, head_size, t.plan.units, st); e != cudaSuccess)
+            return cuda_fail(e);
+        if (!t.plan.per_seq) {
+            mqa::MergeArgs m{};
+            m.ws_o = t.ws_o;
+            m.ws_lse = t.ws_lse;
+            m.seq_lens = seq_lens;
+            m.out = t.out;
+            m.lse = lse;
+            m.status = device_status;
+            m.out_scale = 1.0f;
+            m.H = num_heads;
+            m.R = kv_lora_rank;
+            m.plan = t.plan;
+            if (cudaError_t e = mqa::lse_merge(m, st); e != cudaSuccess) return cuda_fail(e);
+        }
+        return MQA_OK;
+    }
+
     mqa::MlaArgs a{};
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.kv = static_cast<const uint8_t*>(kv_cache);
@@ -224,7 +306,6 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
             return cuda_fail(cudaErrorInvalidValue);
     }
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaError_t e = mqa::mla_mma_stage1(a, head_size, fp8, a.plan.units * groups, st); e != cudaSuccess)
         return cuda_fail(e);
     if (!a.plan.per_seq) {

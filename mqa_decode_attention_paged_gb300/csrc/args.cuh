@@ -36,6 +36,26 @@ struct MlaArgs {
     Plan plan;
 };
 
+// H = 128 tensor-core MLA path (2-CTA clusters split by feature columns).
+struct MlaTcArgs {
+    // bf16 cache as a 2D tensor {D, num_blocks * page}, box {64, box_rows},
+    // 128-byte swizzle; q as {D, B * H}, box {64, 128}, 128-byte swizzle.
+    CUtensorMap kv_map;
+    CUtensorMap q_map;
+    int box_rows;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    __nv_bfloat16* out;
+    float* lse;
+    float* ws_o;
+    float* ws_lse;
+    int* status;
+    float sl2;
+    float out_scale;
+    int H, num_blocks;
+    Plan plan;
+};
+
 struct GqaArgs {
     const __nv_bfloat16* q;
     const uint8_t* kv;
@@ -67,6 +87,9 @@ cudaError_t mla_mma_stage1(const MlaArgs& a, int D, bool fp8, int grid, cudaStre
 size_t mla_mma_smem_bytes(int D, bool fp8, int batch);
 int mla_mma_tile();
 cudaError_t gqa_mma_stage1(const GqaArgs& a, int D, int grid, cudaStream_t stream);
+cudaError_t mla_tc_stage1(const MlaTcArgs& a, int D, int clusters, cudaStream_t stream);
+int mla_tc_tile();
+constexpr int kMaxBatchTc = 512;  // page prefix of the H = 128 path lives in smem
 size_t gqa_mma_smem_bytes(int D, int hkv, int batch);
 cudaError_t lse_merge(const MergeArgs& a, cudaStream_t stream);
 

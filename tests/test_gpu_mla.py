@@ -42,7 +42,34 @@ def test_ragged_shapes(D, page, kv_dtype, splits):
                  what=f"D={D} P={page} {kv_dtype} S={splits}")
 
 
-@pytest.mark.parametrize("H", [1, 5, 16, 40, 128])
+@pytest.mark.parametrize("D", [576, 320])
+@pytest.mark.parametrize("page", [16, 64])
+@pytest.mark.parametrize("splits", [1, 4])
+def test_tensor_core_path_ragged(D, page, splits):
+    # 65..128 heads over a bf16 cache run on the 2-CTA tcgen05 clusters.
+    case = synth.poison(synth.make_mla_case(RAGGED, H=128, D=D, page=page, pool_factor=1.2, seed=8,
+                                            extra_cols=1))
+    out, lse = run_gpu(case, splits)
+    ref_out, ref_lse = run_oracle(case)
+    assert_close(out, lse, ref_out, ref_lse, what=f"tc D={D} P={page} S={splits}")
+
+
+def test_tensor_core_path_multi_tile_and_rescale():
+    # Long pieces (many tiles), and a late key with a much larger logit so the
+    # running max jumps by more than 2^8 mid-sequence (forces the O rescale).
+    case = synth.make_mla_case([1500, 700, 64, 2200], H=128, page=64, seed=9)
+    kv = case.kv.copy()
+    blk = case.block_table[0, 1500 // 64]
+    qf = torch.from_numpy(case.q[0].view(np.int16)).view(torch.bfloat16).float().numpy()
+    kv[blk, 1500 % 64 - 10] = synth.to_bf16_bits(np.clip(qf.mean(axis=0) * 40.0, -200, 200))
+    case = synth.replace(case, kv=kv)
+    ref_out, ref_lse = run_oracle(case)
+    for splits in (1, 5):
+        out, lse = run_gpu(case, splits)
+        assert_close(out, lse, ref_out, ref_lse, what=f"tc rescale S={splits}")
+
+
+@pytest.mark.parametrize("H", [1, 5, 16, 40, 80, 100, 128])
 def test_head_counts(H):
     case = synth.make_mla_case([77, 300, 1], H=H, page=64, seed=11)
     for splits in (1, 3):
