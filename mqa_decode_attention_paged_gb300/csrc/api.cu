@@ -237,6 +237,8 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
         if (!bf16_panel_map(&t.kv_map, kv_cache, head_size, static_cast<long long>(num_blocks) * page_size, br) ||
             !bf16_panel_map(&t.q_map, q, head_size, static_cast<long long>(batch) * num_heads, 128))
             return cuda_fail(cudaErrorInvalidValue);
+        t.q = static_cast<const __nv_bfloat16*>(q);
+        t.kv = static_cast<const uint8_t*>(kv_cache);
         t.block_table = block_table;
         t.seq_lens = seq_lens;
         t.out = static_cast<__nv_bfloat16*>(out);

@@ -43,6 +43,8 @@ struct MlaTcArgs {
     CUtensorMap kv_map;
     CUtensorMap q_map;
     int box_rows;
+    const __nv_bfloat16* q;  // [B, H, D]
+    const uint8_t* kv;       // cache rows of D bf16 values
     const int32_t* block_table;
     const int32_t* seq_lens;
     __nv_bfloat16* out;

@@ -108,6 +108,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16) of global memory at `src` (16-byte
+// aligned) into L2 without waiting for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Tiled 3D tensor copy global -> shared (box given by the tensor map, which
 // lives in kernel parameter space) that completes its bytes on `bar`.  The
 // innermost coordinate x must be a multiple of 16 bytes' worth of elements.

@@ -7,28 +7,31 @@
 // V columns a rank needs are a prefix of the K columns it already loaded (V is
 // the first kv_lora_rank columns of the same row: "Triton と MLA" page,
 // vllm-arch-zh ja/attention/triton-mla, データフロー), so every cache byte is
-// read from HBM once and TMEM holds O[128 x R/2] plus two logit tiles.  The
+// read from HBM once and TMEM holds O[128 x R/2], the logits, P and Q.  The
 // two partial logit tiles are exchanged through distributed shared memory and
 // summed identically in both CTAs, which then run the same online softmax
 // (tutorial page lshu.cn/news/265860, §7).
 //
-// Per CTA (352 threads), for 32-token tiles grouped in pairs:
-//   warp 0      TMA producer: the tile's rows of this CTA's column panels
-//               (tensor-map copies, 128-byte swizzle) into a 4-stage ring laid
-//               out as two 64-row slots, so that a pair of tiles is one
-//               contiguous 64-row operand;
+// The cache streams in 32-token tiles; Q.K^T, the softmax and P.V work on
+// pairs of tiles (64 tokens).  Per CTA (352 threads):
+//   warp 0      TMA producer: each tile's rows of this CTA's column panels
+//               (tensor-map copies, 128-byte swizzle) into a ring of 64-row
+//               slots (two tiles each), so a pair is one contiguous operand;
 //   warp 1      TMEM owner and single-thread MMA issuer:
-//               S[128 x 64] = Q K^T per tile pair (kind::f16, M = 128 heads,
-//               N = 64 tokens) into one of two TMEM logit buffers, then per
-//               tile O[128 x R/2] += P V (N = R/2, V read MN-major);
-//   warps 2..9  two threads per head row (16 tokens of each tile, half of O's
-//               columns each): read S from TMEM, send it to the peer
-//               with asynchronous remote stores (lane-contiguous, double
-//               buffered), add the peer's half, mask, online softmax in base 2
-//               with lazy rescaling of O (only when the running max grows by
-//               more than 2^8), write P (bf16, swizzled K-major; the two halves
-//               of one 64-token tile alternate) and the epilogue;
-//   warp 10     Q loader (the query rows of the current request).
+//               S[128 x 64] = Q K^T per pair (kind::f16, M = 128 heads, N = 64
+//               tokens, A = Q from TMEM), then O[128 x R/2] += P V per pair
+//               (A = P from TMEM, V read MN-major from the slot);
+//   warps 2..9  two softmax groups of four warps (one thread per head row);
+//               group g takes the pairs of parity g, so two pairs are in
+//               flight: read the 64 partial logits of the row, send them to
+//               the peer, add the peer's partial, mask, take the row maximum,
+//               continue the running maximum handed over by the other group
+//               (lazy rescaling of O only when it grows by more than 2^8),
+//               write P (bf16) into TMEM; per piece, the group of the last
+//               pair writes the output; they also write each piece's Q rows
+//               into TMEM;
+//   warp 10     loader of the Q panel that does not fit in TMEM (rank 1, head
+//               576 only).
 // Every wait is bounded; on expiry MQA_ERR_DEVICE_TIMEOUT is recorded and the
 // roles wind down.
 #include "args.cuh"
@@ -41,59 +44,100 @@ namespace mqa {
 template <int D, int R>
 struct MlaTcCfg {
     static constexpr int kHeads = 128;
-    static constexpr int kTile = 32;  // tokens per pipeline stage (a Q.K^T covers two)
+    static constexpr int kTile = 32;  // tokens per pipeline stage; Q.K^T, softmax and P.V take two
+    static constexpr int kPair = 2 * kTile;
     static constexpr int kPanels = D / 64;
     static constexpr int kLoPanels = R / 128;  // rank 0: QK panels = its P.V panels
     static constexpr int kHiPanels = kPanels - kLoPanels;
     static constexpr int kMaxPanels = kHiPanels;
     static constexpr int kOCols = R / 2;  // O columns per CTA
     static constexpr int kPVPanels = kOCols / 64;
-    static constexpr int kStages = 4;
     static constexpr int kQPanelBytes = kHeads * 128;
-    static constexpr int kKvPanelBytes = 2 * kTile * 128;  // one panel of a 64-row slot
-    static constexpr int kQBytes = kMaxPanels * kQPanelBytes;
-    static constexpr int kSlotBytes = kMaxPanels * kKvPanelBytes;  // two stages
-    static constexpr int kPBytes = kHeads * 128;            // 128 rows x 64 tokens: two tile halves
-    static constexpr int kXBytes = kHeads * kTile * 4;      // one fp32 logit tile
-    static constexpr int kSoftmaxWarps = 8;  // two threads per head row
-    static constexpr int kThreads = 32 * (3 + kSoftmaxWarps);
+    static constexpr int kKvPanelBytes = kPair * 128;  // one panel of a 64-row slot
+    // TMEM columns: O [0, 256), S [256, 320), P two buffers [320, 384), Q
+    // [384, 512) (up to 4 panels of 64 dims, two bf16 per column); a rank
+    // with more Q panels keeps the rest in shared memory
     static constexpr int kTmemCols = 512;
-    static constexpr int kTmemS = 256;  // pair logit buffers at columns 256 and 320
+    static constexpr int kTmemS = 256;
+    static constexpr int kTmemP = 320;
+    static constexpr int kTmemQ = 384;
+    static constexpr int kTmemQPanels = 4;
+    static constexpr int kQSmemPanels = kMaxPanels > kTmemQPanels ? kMaxPanels - kTmemQPanels : 0;
+    static constexpr int kQBytes = kQSmemPanels * kQPanelBytes;
+    static constexpr int kSlotBytes = kMaxPanels * kKvPanelBytes;  // two stages
+    static constexpr int kXBytes = kHeads * kPair * 4;              // one fp32 logit pair
+    static constexpr int kGroupWarps = 4;
+    static constexpr int kGroupThreads = 32 * kGroupWarps;
+    static constexpr int kSoftmaxWarps = 2 * kGroupWarps;
+    static constexpr int kThreads = 32 * (3 + kSoftmaxWarps);
 
+    static constexpr int kNumBars = 40;
+    static constexpr int kRedBytes = 4 * kHeads * 4;  // running maxima [2][128], handed-over sums / maxima
+    // everything but the ring: alignment slack, Q panels, X, barriers,
+    // reductions, up to 8 stage masks, the TMEM address, lengths
+    static constexpr int kFixedBytes =
+        1024 + kQBytes + 2 * kXBytes + kNumBars * 8 + kRedBytes + 8 * 8 + 16 + 4 * (2 * kMaxBatchTc + 1);
+    static constexpr int kSlotsFit = (227 * 1024 - kFixedBytes) / kSlotBytes;
+    static constexpr int kSlots = kSlotsFit > 4 ? 4 : kSlotsFit;
+    static constexpr int kStages = 2 * kSlots;
     static constexpr int kOffQ = 0;
     static constexpr int kOffStages = kOffQ + kQBytes;
-    static constexpr int kOffP = kOffStages + (kStages / 2) * kSlotBytes;
-    static constexpr int kOffX = kOffP + kPBytes;
+    static constexpr int kOffX = kOffStages + kSlots * kSlotBytes;
     static constexpr int kOffBars = kOffX + 2 * kXBytes;
-    static constexpr int kNumBars = 32;
-    static constexpr int kOffRed = kOffBars + kNumBars * 8;  // row maxima / sums of the two halves
-    static constexpr int kRedBytes = 6 * kHeads * 4;
+    static constexpr int kOffRed = kOffBars + kNumBars * 8;
     static constexpr int kOffMask = kOffRed + kRedBytes;
     static constexpr int kOffTmem = kOffMask + kStages * 8;
     static constexpr int kOffCum = kOffTmem + 16;
     static size_t smem_bytes(int batch) { return 1024 + kOffCum + 4 * (2 * batch + 1); }
 
     static_assert(kOCols <= 256 && kOCols % 64 == 0, "P.V width");
-    static_assert(kTmemS >= kOCols && kTmemS + 4 * kTile <= kTmemCols, "TMEM layout");
+    static_assert(kOCols <= kTmemS && kTmemS + kPair <= kTmemP && kTmemP + kPair <= kTmemQ &&
+                      kTmemQ + 32 * kTmemQPanels <= kTmemCols,
+                  "TMEM layout");
+    static_assert(kSlots >= 2 && kStages <= 8, "pipeline depth");
     static_assert(1024 + kOffCum + 4 * (2 * kMaxBatchTc + 1) <= 227 * 1024, "shared memory budget");
-    static_assert(kOffStages % 1024 == 0 && kOffP % 1024 == 0 && kSlotBytes % 1024 == 0,
-                  "swizzled operands need 1024-byte alignment");
+    static_assert(kOffStages % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzled operands need 1024-byte alignment");
 };
 
-// barrier slots
+// barrier slots, each range starting where the previous one ends
 enum TcBar {
-    kKvFull = 0,    // [4] tile landed (producer expect_tx + TMA bytes)
-    kKvEmpty = 4,   // [4] P.V of the tile done (tensor-core commit)
-    kQFull = 8,     // Q rows landed
-    kQEmpty = 9,    // every Q.K^T of the piece done
-    kSFull = 10,    // [2] logit tile pair in TMEM
-    kSEmpty = 12,   // [2] both tiles of the pair read out by the softmax rows
-    kPFull = 14,    // [2] P half written (and O rescaled)
-    kPEmpty = 16,   // [2] P.V of that half done
-    kXFull = 18,    // [2] the peer's logit tile has arrived
-    kXFree = 20,    // [2] the peer has consumed the tile we sent it
-    kPair = 22,     // [4] rendezvous of the two softmax warps of a TMEM quadrant
+    kKvFull = 0,             // [8] tile landed (producer expect_tx + TMA bytes)
+    kKvEmpty = kKvFull + 8,  // [8] P.V of the tile's pair done (tensor-core commit)
+    kQFull = kKvEmpty + 8,   // Q panels kept in shared memory landed
+    kQEmpty = kQFull + 1,    // every Q.K^T of the piece done
+    kQTmem = kQEmpty + 1,    // a softmax group has written the piece's Q panels into TMEM
+    kSFull = kQTmem + 1,     // [2] logit pair of parity i in TMEM
+    kSEmpty = kSFull + 2,    // the logit pair read out by its softmax group
+    kPFull = kSEmpty + 1,    // [2] P of a pair in TMEM buffer (pair & 1), O rescaled if needed
+    kPEmpty = kPFull + 2,    // [2] P.V of that pair done
+    kXFull = kPEmpty + 2,    // [2] the peer's logit pair for group g has arrived
+    kXFree = kXFull + 2,     // [2] the peer's group g has consumed the pair we sent it
+    kMReady = kXFree + 2,    // [2] running maximum after a pair of parity i published
+    kLReady = kMReady + 2,   // the group without the piece's last pair handed over its sum
+    kOFree = kLReady + 1,    // the piece's output has been read out of TMEM
+    kDrain = kOFree + 1,     // every tensor-core operation of the CTA has completed
+    kBarCount = kDrain + 1,
 };
+static_assert(kBarCount <= MlaTcCfg<576, 512>::kNumBars && kBarCount <= MlaTcCfg<320, 256>::kNumBars,
+              "barrier slots");
+
+// Q.K^T of one tile pair into TMEM columns d: NQT panels of Q from TMEM
+// (q_tmem), the rest from shared memory (qdesc); kdesc addresses panel 0 of
+// the pair's slot.  Descriptors advance by constant byte offsets >> 4 (the
+// start-address field cannot carry: shared addresses stay below 256 KB).
+template <int NP, int NQT, int KvPanelBytes, int QPanelBytes>
+__device__ __forceinline__ void issue_qk(uint32_t d, uint32_t q_tmem, uint64_t kdesc, uint64_t qdesc,
+                                         uint32_t idesc) {
+#pragma unroll
+    for (int ks = 0; ks < NP * 4; ++ks) {
+        const uint64_t b = kdesc + static_cast<uint64_t>(((ks >> 2) * KvPanelBytes + (ks & 3) * 32) >> 4);
+        if (ks < NQT * 4)
+            umma_bf16_ta(d, q_tmem + ks * 8, b, idesc, ks > 0 ? 1u : 0u);
+        else
+            umma_bf16(d, qdesc + static_cast<uint64_t>((((ks >> 2) - NQT) * QPanelBytes + (ks & 3) * 32) >> 4), b,
+                      idesc, 1u);
+    }
+}
 
 template <int D, int R>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThreads, 1)
@@ -103,7 +147,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* q_s = smem + C::kOffQ;
     uint8_t* stages = smem + C::kOffStages;
-    uint8_t* p_s = smem + C::kOffP;
     uint8_t* x_s = smem + C::kOffX;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
     uint64_t* mask_s = reinterpret_cast<uint64_t*>(smem + C::kOffMask);
@@ -117,6 +160,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
     const int unit = blockIdx.x >> 1;
     const int pbase = rank ? C::kLoPanels : 0;          // first global column panel
     const int np = rank ? C::kHiPanels : C::kLoPanels;  // panels loaded and contracted
+    const int nq_tmem = min(np, C::kTmemQPanels);        // Q panels held in TMEM, the rest in smem
     const int P = a.plan.page;
 
     if (threadIdx.x == 0) {
@@ -126,15 +170,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         }
         mbar_init(&bars[kQFull], 1);
         mbar_init(&bars[kQEmpty], 1);
+        mbar_init(&bars[kQTmem], C::kGroupThreads);
+        mbar_init(&bars[kSEmpty], C::kGroupThreads);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[kSFull + i], 1);
-            mbar_init(&bars[kSEmpty + i], 2 * 32 * C::kSoftmaxWarps);  // both tiles of a pair
-            mbar_init(&bars[kPFull + i], 32 * C::kSoftmaxWarps);
+            mbar_init(&bars[kPFull + i], C::kGroupThreads);
             mbar_init(&bars[kPEmpty + i], 1);
-            mbar_init(&bars[kXFull + i], 1);  // own expect_tx; the bytes come from the peer
-            mbar_init(&bars[kXFree + i], C::kSoftmaxWarps);  // one arrive per peer softmax warp
+            mbar_init(&bars[kXFull + i], 1);                 // own expect_tx; the bytes come from the peer
+            mbar_init(&bars[kXFree + i], C::kGroupWarps);    // one arrive per warp of the peer's group
+            mbar_init(&bars[kMReady + i], C::kGroupThreads);
         }
-        for (int q = 0; q < 4; ++q) mbar_init(&bars[kPair + q], 64);
+        mbar_init(&bars[kLReady], C::kGroupThreads);
+        mbar_init(&bars[kOFree], C::kGroupThreads);
+        mbar_init(&bars[kDrain], 1);
         fence_mbar_init();
         prefetch_tmap(&a.kv_map);
         prefetch_tmap(&a.q_map);
@@ -229,7 +277,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         }
     } else if (warp == 2 + C::kSoftmaxWarps) {
         // ------------------------------------------------------ Q loader
-        if (lane == 0) {
+        if (lane == 0 && np > nq_tmem) {
             const uint64_t pol = l2_policy_evict_last();
             PieceIter it;
             it.init(a.plan, cum, T, unit);
@@ -242,9 +290,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                     report(a.status, MQA_ERR_DEVICE_TIMEOUT);
                     break;
                 }
-                mbar_arrive_expect_tx(&bars[kQFull], np * C::kQPanelBytes);
-                for (int pn = 0; pn < np; ++pn)
-                    tma_load_2d(q_s + pn * C::kQPanelBytes, &a.q_map, (pbase + pn) * 64, pc.b * a.H,
+                mbar_arrive_expect_tx(&bars[kQFull], (np - nq_tmem) * C::kQPanelBytes);
+                for (int pn = nq_tmem; pn < np; ++pn)
+                    tma_load_2d(q_s + (pn - nq_tmem) * C::kQPanelBytes, &a.q_map, (pbase + pn) * 64, pc.b * a.H,
                                 &bars[kQFull], pol);
                 ++qc;
             }
@@ -253,20 +301,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t kIdQK = umma_idesc_bf16(128, 2 * C::kTile, 0);
+            constexpr uint32_t kIdQK = umma_idesc_bf16(128, C::kPair, 0);
             constexpr uint32_t kIdPV = umma_idesc_bf16(128, C::kOCols, 1);
-            const uint32_t q_addr = smem_u32(q_s), st_addr = smem_u32(stages), p_addr = smem_u32(p_s);
+            const uint32_t st_addr = smem_u32(stages);
+            // descriptor bases: K operand rows of the ring (K-major), V operand
+            // (MN-major, panel stride = slot panel), smem Q panel
+            const uint64_t kdesc0 = umma_desc(st_addr, 16, 1024);
+            const uint64_t vdesc0 = umma_desc(st_addr, C::kKvPanelBytes, 1024);
+            const uint64_t qdesc = umma_desc(smem_u32(q_s), 16, 1024);
             bool ok = true;
-            int last_pv = -1;
             // Two independent streams, issued as soon as their inputs are ready:
-            //   Q.K^T per tile pair (needs Q, both stages, a free S buffer),
-            //   P.V per tile (needs its P half).
+            //   Q.K^T per pair (needs Q, both tiles, the S buffer read out),
+            //   P.V per pair (needs its P and, for a piece's first pair, the
+            //   previous piece's output read out of O).
             PieceIter qi, vi;
             qi.init(a.plan, cum, T, unit);
             vi.init(a.plan, cum, T, unit);
             Piece qpc, vpc;
-            int qt = 0, qj = 0, qnt = 0, qc = 0;  // next pair: global tile qt, piece tile qj
-            int vt = 0, vj = 0, vnt = 0;          // next P.V: global tile vt, piece tile vj
+            int qt = 0, qj = 0, qnt = 0, qc = 0;  // next Q.K^T: global tile qt, piece tile qj
+            int vt = 0, vj = 0, vnt = 0, vc = 0;  // next P.V: global tile vt, piece tile vj
             bool q_loaded = false;
             auto next_piece = [&](PieceIter& pi, Piece& pc, int& nt) {
                 int tok0, tok_end;
@@ -282,26 +335,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             while (q_have || v_have) {
                 bool progressed = false;
                 if (q_have) {
-                    if (!q_loaded && mbar_test(&bars[kQFull], qc & 1)) {
+                    if (!q_loaded && mbar_test(&bars[kQTmem], qc & 1) &&
+                        (np == nq_tmem || mbar_test(&bars[kQFull], qc & 1))) {
                         q_loaded = true;
                         tc_fence_after();
                     }
-                    const int sb = (qt >> 1) & 1;
-                    if (q_loaded && mbar_test(&bars[kKvFull + qt % C::kStages], (qt / C::kStages) & 1) &&
-                        mbar_test(&bars[kKvFull + (qt + 1) % C::kStages], ((qt + 1) / C::kStages) & 1) &&
-                        mbar_test(&bars[kSEmpty + sb], ((qt >> 2) & 1) ^ 1)) {
+                    const int qp = qt >> 1;
+                    if (q_loaded && mbar_test(&bars[kSEmpty], (qp & 1) ^ 1) &&
+                        mbar_test(&bars[kKvFull + qt % C::kStages], (qt / C::kStages) & 1) &&
+                        mbar_test(&bars[kKvFull + (qt + 1) % C::kStages], ((qt + 1) / C::kStages) & 1)) {
                         tc_fence_after();
-                        const uint32_t kaddr = st_addr + tile_base(qt);
-                        for (int ks = 0; ks < np * 4; ++ks)
-                            umma_bf16(tbase + C::kTmemS + sb * 2 * C::kTile,
-                                      umma_desc(q_addr + (ks >> 2) * C::kQPanelBytes + (ks & 3) * 32, 16, 1024),
-                                      umma_desc(kaddr + (ks >> 2) * C::kKvPanelBytes + (ks & 3) * 32, 16, 1024),
-                                      kIdQK, ks > 0 ? 1u : 0u);
-                        umma_commit(&bars[kSFull + sb]);
+                        const uint32_t d = tbase + C::kTmemS;
+                        const uint64_t kd = kdesc0 + static_cast<uint64_t>(tile_base(qt) >> 4);
+                        if (rank)
+                            issue_qk<C::kHiPanels, (C::kHiPanels < 4 ? C::kHiPanels : 4), C::kKvPanelBytes,
+                                     C::kQPanelBytes>(d, tbase + C::kTmemQ, kd, qdesc, kIdQK);
+                        else
+                            issue_qk<C::kLoPanels, (C::kLoPanels < 4 ? C::kLoPanels : 4), C::kKvPanelBytes,
+                                     C::kQPanelBytes>(d, tbase + C::kTmemQ, kd, qdesc, kIdQK);
+                        umma_commit(&bars[kSFull + (qp & 1)]);
                         qt += 2;
                         qj += 2;
                         if (qj >= qnt) {
-                            umma_commit(&bars[kQEmpty]);  // Q may be reloaded once these finish
+                            umma_commit(&bars[kQEmpty]);  // Q may be replaced once these finish
                             ++qc;
                             q_loaded = false;
                             qj = 0;
@@ -310,21 +366,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                         progressed = true;
                     }
                 }
-                if (v_have && vt < qt && mbar_test(&bars[kPFull + (vt & 1)], (vt >> 1) & 1)) {
+                const int vp = vt >> 1, pb = vp & 1;
+                if (v_have && vt < qt && mbar_test(&bars[kPFull + pb], (vp >> 1) & 1) &&
+                    (vj > 0 || vc == 0 || mbar_test(&bars[kOFree], (vc - 1) & 1))) {
                     tc_fence_after();
-                    const int pb = vt & 1;
-                    const uint32_t v = st_addr + tile_base(vt);
+                    const uint64_t vd = vdesc0 + static_cast<uint64_t>(tile_base(vt) >> 4);
 #pragma unroll
-                    for (int ks = 0; ks < C::kTile / 16; ++ks)
-                        umma_bf16(tbase, umma_desc(p_addr + pb * 64 + ks * 32, 16, 1024),
-                                  umma_desc(v + ks * 2048, C::kKvPanelBytes, 1024), kIdPV,
-                                  (vj == 0 && ks == 0) ? 0u : 1u);
+                    for (int ks = 0; ks < C::kPair / 16; ++ks)
+                        umma_bf16_ta(tbase, tbase + C::kTmemP + pb * (C::kPair / 2) + ks * 8,
+                                     vd + static_cast<uint64_t>((ks * 16 * 128) >> 4), kIdPV,
+                                     (vj == 0 && ks == 0) ? 0u : 1u);
                     umma_commit(&bars[kPEmpty + pb]);
                     umma_commit(&bars[kKvEmpty + vt % C::kStages]);
-                    last_pv = vt;
-                    ++vt;
-                    if (++vj >= vnt) {
+                    umma_commit(&bars[kKvEmpty + (vt + 1) % C::kStages]);
+                    vt += 2;
+                    vj += 2;
+                    if (vj >= vnt) {
                         vj = 0;
+                        ++vc;
                         v_have = next_piece(vi, vpc, vnt);
                     }
                     progressed = true;
@@ -343,240 +402,295 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             }
             if (!ok) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
             // no tensor-core work may be in flight when the CTA tears down
-            if (last_pv >= 0 && !mbar_wait(&bars[kPEmpty + (last_pv & 1)], (last_pv >> 1) & 1))
-                report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+            umma_commit(&bars[kDrain]);
+            if (!mbar_wait(&bars[kDrain], 0)) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
         }
     } else if (warp >= 2 && warp < 2 + C::kSoftmaxWarps) {
-        // ------------------------------------------------------ softmax rows
-        // Two threads per head row: warps w and w + 4 share TMEM lane quadrant
-        // w % 4 and split every tile's 32 tokens (and O's columns) in halves.
+        // ------------------------------------------------------ softmax groups
+        // Group g (warps 2 + 4 g .. 5 + 4 g, one of each TMEM lane quadrant)
+        // takes the pairs of parity g; thread (quad, lane) owns head row h.
         const int quad = warp & 3;
-        const int hf = (warp - 2) >> 2;
+        const int g = (warp - 2) / C::kGroupWarps;
         const int h = quad * 32 + lane;
-        const int tc0 = hf * (C::kTile / 2);
+        const bool live_row = h < a.H;
         const uint32_t lane_addr = tbase + (static_cast<uint32_t>(quad * 32) << 16);
-        float* mx_s = red_s;                   // [2 tiles][2 halves][128 rows] partial maxima
-        float* ls_s = red_s + 4 * C::kHeads;  // [2 halves][128 rows] partial sums
-        uint64_t* pair_bar = &bars[kPair + quad];
-        uint32_t pair_phase = 0;
-        // logit tiles travel lane-contiguously: chunk c (4 floats) of row
-        // (quad, lane) sits at ((quad * 8 + c) * 32 + lane) * 16 bytes, so every
-        // warp store writes 512 contiguous bytes of the peer's buffer
-        const uint32_t x_remote = map_to_rank(x_s, peer) + (quad * 8 * 32 + lane) * 16;
-        const uint8_t* x_local = x_s + (quad * 8 * 32 + lane) * 16;
-        const uint32_t xfull_remote[2] = {map_to_rank(&bars[kXFull], peer), map_to_rank(&bars[kXFull + 1], peer)};
-        const uint32_t xfree_remote[2] = {map_to_rank(&bars[kXFree], peer), map_to_rank(&bars[kXFree + 1], peer)};
-        uint8_t* p_row = p_s + h * 128;
+        float* m_s = red_s;                        // [2][128] running maximum after a pair of parity i
+        float* lh_s = red_s + 2 * C::kHeads;      // [128] sum handed to the epilogue group
+        float* mh_s = red_s + 3 * C::kHeads;      // [128] maximum that sum is relative to
+        // logit pairs travel lane-contiguously: chunk c (4 floats, c < 16) of
+        // row (quad, lane) sits at ((quad * 16 + c) * 32 + lane) * 16 bytes, so
+        // every warp store writes 512 contiguous bytes of the peer's buffer
+        const uint32_t x_off = (quad * 16 * 32 + lane) * 16;
+        const uint32_t x_remote = map_to_rank(x_s + g * C::kXBytes, peer) + x_off;
+        const uint8_t* x_local = x_s + g * C::kXBytes + x_off;
+        const uint32_t xfull_remote = map_to_rank(&bars[kXFull + g], peer);
+        const uint32_t xfree_remote = map_to_rank(&bars[kXFree + g], peer);
         // warp-uniform bounded waits: TMEM accesses are warp-collective, so a
-        // lane never leaves the tile loop on its own
+        // lane never leaves the loop on its own
         auto wait_all = [&](uint64_t* bar, uint32_t parity, bool cluster_scope) {
             const bool done = cluster_scope ? mbar_wait_cluster(bar, parity) : mbar_wait(bar, parity);
             return __all_sync(0xffffffffu, done);
         };
-        // rendezvous of the two warps that own the same rows
-        auto pair_sync = [&]() {
-            mbar_arrive(pair_bar);
-            const bool done = wait_all(pair_bar, pair_phase, false);
-            pair_phase ^= 1;
-            return done;
+        // Q row h of the next piece that holds tokens (after `from`) into
+        // TMEM, one 32-bit column per pair of consecutive dims (low half = even)
+        auto stage_q = [&](PieceIter from) {
+            Piece nx;
+            int tok0, tok_end;
+            while (from.next(cum, nx)) {
+                if (piece_tiles(nx, tok0, tok_end) == 0) continue;
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    a.q + (static_cast<long long>(nx.b) * a.H + (live_row ? h : 0)) * D + pbase * 64);
+                for (int c = 0; c < 4 * nq_tmem; ++c) {  // 8 columns (16 dims) at a time
+                    const uint4 v0 = live_row ? __ldg(src + 2 * c) : make_uint4(0, 0, 0, 0);
+                    const uint4 v1 = live_row ? __ldg(src + 2 * c + 1) : make_uint4(0, 0, 0, 0);
+                    const uint32_t r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    tmem_st8(lane_addr + C::kTmemQ + c * 8, r);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars[kQTmem]);
+                return;
+            }
         };
+
+        // P.V of this group's own pair p2 (parity g) done.  The group waits on
+        // its own barrier once per own pair, in pair order, so every parity
+        // wait targets the phase after the last one it saw complete.
+        auto wait_own_pv = [&](int p2) { return wait_all(&bars[kPEmpty + g], (p2 >> 1) & 1, false); };
 
         PieceIter it;
         it.init(a.plan, cum, T, unit);
         Piece pc;
-        int t = 0;
+        int gp = 0;      // global index of the current piece's first pair
+        int kpiece = 0;  // pieces with tokens so far
         bool ok = true;
+        if (g == 0) stage_q(it);
         while (ok && it.next(cum, pc)) {
             int tok0, tok_end;
             const int nt = piece_tiles(pc, tok0, tok_end);
-            const bool live_row = h < a.H;
-            const int ocol0 = hf * (C::kOCols / 2);  // this thread's half of O's columns
+            const int npairs = nt >> 1;
             if (nt == 0) {  // empty request (per-request mode): out = 0, lse = -inf
-                if (live_row && pc.whole) {
-                    __nv_bfloat16* o =
-                        a.out + (static_cast<long long>(pc.b) * a.H + h) * R + rank * C::kOCols + ocol0;
-                    for (int c = 0; c < C::kOCols / 2; c += 8)
-                        *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
-                    if (rank == 0 && hf == 0 && a.lse) a.lse[static_cast<long long>(pc.b) * a.H + h] = -INFINITY;
+                if (g == 0 && live_row && pc.whole) {
+                    __nv_bfloat16* o = a.out + (static_cast<long long>(pc.b) * a.H + h) * R + rank * C::kOCols;
+                    for (int c = 0; c < C::kOCols; c += 8) *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
+                    if (rank == 0 && a.lse) a.lse[static_cast<long long>(pc.b) * a.H + h] = -INFINITY;
                 }
                 continue;
             }
-            float m_run = -INFINITY, l_part = 0.f;
-            for (int j = 0; j < nt; ++j, ++t) {
-                const int sb = (t >> 1) & 1, xb = t & 1, pb = t & 1, st = t % C::kStages;
-                constexpr int kHalfTok = C::kTile / 2;
-                float s[kHalfTok];
-                if (!wait_all(&bars[kSFull + sb], (t >> 2) & 1, false)) {
+            // this group's sum of p over its pairs of the piece, relative to m_l
+            float l_part = 0.f, m_l = -INFINITY;
+            for (int j = ((gp & 1) == g) ? 0 : 1; j < npairs; j += 2) {
+                const int p = gp + j, pb = p & 1;
+                const int t0 = 2 * p;
+                // ---- logits of the pair: own partial from TMEM
+                float s[C::kPair];
+                if (!wait_all(&bars[kSFull + pb], (p >> 1) & 1, false)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                {
-                    uint32_t r[16];
-                    tmem_ld16(lane_addr + C::kTmemS + sb * 2 * C::kTile + (t & 1) * C::kTile + tc0, r);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + C::kTmemS + half * 32, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < kHalfTok; ++i) s[i] = __uint_as_float(r[i]);
+                    for (int i = 0; i < 32; ++i) s[half * 32 + i] = __uint_as_float(r[i]);
                 }
                 tc_fence_before();
-                mbar_arrive(&bars[kSEmpty + sb]);
-
-                // send our partial logits, receive and add the peer's
-                if (h == 0 && hf == 0) mbar_arrive_expect_tx(&bars[kXFull + xb], C::kXBytes);
-                if (t >= 2 && !wait_all(&bars[kXFree + xb], ((t >> 1) & 1) ^ 1, true)) {
+                mbar_arrive(&bars[kSEmpty]);
+                // the piece's last logit pair is in: every Q.K^T that read the
+                // TMEM Q panels has completed, so stage the next piece's Q
+                if (j == npairs - 1) stage_q(it);
+                // ---- send the partial to the peer, receive and add the peer's
+                if (h == 0) mbar_arrive_expect_tx(&bars[kXFull + g], C::kXBytes);
+                if (p >= 2 && !wait_all(&bars[kXFree + g], ((p >> 1) & 1) ^ 1, true)) {
                     ok = false;
                     break;
                 }
 #pragma unroll
-                for (int c = 0; c < kHalfTok / 4; ++c)
-                    st_async_v4(x_remote + xb * C::kXBytes + (hf * 4 + c) * 512, s[4 * c], s[4 * c + 1],
-                                s[4 * c + 2], s[4 * c + 3], xfull_remote[xb]);
-                if (!wait_all(&bars[kXFull + xb], (t >> 1) & 1, true)) {
+                for (int c = 0; c < C::kPair / 4; ++c)
+                    st_async_v4(x_remote + c * 512, s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3], xfull_remote);
+                // valid tokens of both tiles (set by the producer before kv_full)
+                if (!wait_all(&bars[kKvFull + t0 % C::kStages], (t0 / C::kStages) & 1, false) ||
+                    !wait_all(&bars[kKvFull + (t0 + 1) % C::kStages], ((t0 + 1) / C::kStages) & 1, false)) {
+                    ok = false;
+                    break;
+                }
+                const uint64_t vm = (mask_s[t0 % C::kStages] & 0xFFFFFFFFull) |
+                                    (mask_s[(t0 + 1) % C::kStages] << 32);
+                if (!wait_all(&bars[kXFull + g], (p >> 1) & 1, true)) {
                     ok = false;
                     break;
                 }
 #pragma unroll
-                for (int c = 0; c < kHalfTok / 4; ++c) {
-                    const float4 v = *reinterpret_cast<const float4*>(x_local + xb * C::kXBytes + (hf * 4 + c) * 512);
+                for (int c = 0; c < C::kPair / 4; ++c) {
+                    const float4 v = *reinterpret_cast<const float4*>(x_local + c * 512);
                     s[4 * c] += v.x;
                     s[4 * c + 1] += v.y;
                     s[4 * c + 2] += v.z;
                     s[4 * c + 3] += v.w;
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster_relaxed(xfree_remote[xb]);
-
-                // valid tokens of this tile (set by the producer before kv_full)
-                if (!wait_all(&bars[kKvFull + st], (t / C::kStages) & 1, false)) {
-                    ok = false;
-                    break;
-                }
-                const uint64_t vmask = mask_s[st];
-                float lm = -INFINITY;
+                if (lane == 0) mbar_arrive_cluster_relaxed(xfree_remote);
+                // ---- mask, scale to base 2, row maximum
 #pragma unroll
-                for (int i = 0; i < kHalfTok; ++i) {
-                    s[i] = ((vmask >> (tc0 + i)) & 1ull) ? s[i] * a.sl2 : -INFINITY;
-                    lm = fmaxf(lm, s[i]);
-                }
-                // row maximum of the tile: combine the two halves
-                mx_s[((t & 1) * 2 + hf) * C::kHeads + h] = lm;
-                if (!pair_sync()) {
-                    ok = false;
-                    break;
-                }
-                float mt = fmaxf(lm, mx_s[((t & 1) * 2 + (1 - hf)) * C::kHeads + h]);
-                // the half of P this tile writes was last read by P.V(t-2)
-                bool half_free = (j == 0) || (t < 2);  // at a piece start the epilogue already waited
-                if (j == 0) {
-                    m_run = mt;
-                } else if (__any_sync(0xffffffffu, mt > m_run + 8.f)) {
-                    // the running max grew by more than 2^8 (decided per warp; the
-                    // partner warp holds the same rows and decides alike; rows
-                    // whose max did not grow rescale by 1): wait for P.V(t-1),
-                    // rescale this thread's half of O and its partial sum
-                    mt = fmaxf(mt, m_run);
-                    const float alpha = ex2(m_run - mt);
-                    if (!wait_all(&bars[kPEmpty + ((t - 1) & 1)], ((t - 1) >> 1) & 1, false)) {
+                for (int i = 0; i < C::kPair; ++i) s[i] = ((vm >> i) & 1ull) ? s[i] * a.sl2 : -INFINITY;
+                float mx[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    mx[i] = fmaxf(fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24])),
+                                  fmaxf(fmaxf(s[i + 32], s[i + 40]), fmaxf(s[i + 48], s[i + 56])));
+                const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                // ---- running maximum: continue the one the other group
+                // published after pair p - 1 (always waited for, so that its
+                // slot is not overwritten before it was read)
+                float m_prev = -INFINITY;
+                if (p >= 1) {
+                    if (!wait_all(&bars[kMReady + ((p - 1) & 1)], ((p - 1) >> 1) & 1, false)) {
                         ok = false;
                         break;
                     }
-                    half_free = true;
+                    m_prev = m_s[((p - 1) & 1) * C::kHeads + h];
+                }
+                float m_run;
+                if (j == 0) {
+                    m_run = mt;
+                } else if (__any_sync(0xffffffffu, mt > m_prev + 8.f)) {
+                    // the running max grew by more than 2^8 (decided per warp;
+                    // rows whose max did not grow rescale by 1): wait for
+                    // P.V(p - 1), then rescale the row of O
+                    m_run = fmaxf(mt, m_prev);
+                    const float alpha = ex2(m_prev - m_run);
+                    // P.V runs in pair order: with the own P.V(p - 2) seen
+                    // complete, the other parity's barrier is at most one
+                    // phase short of P.V(p - 1)
+                    if ((p >= 2 && !wait_own_pv(p - 2)) ||
+                        !wait_all(&bars[kPEmpty + (g ^ 1)], ((p - 1) >> 1) & 1, false)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    for (int c0 = ocol0; c0 < ocol0 + C::kOCols / 2; c0 += 32) {
-                        uint32_t r[32];
-                        tmem_ld32(lane_addr + c0, r);
+                    for (int c0 = 0; c0 < C::kOCols; c0 += 16) {
+                        uint32_t r[16];
+                        tmem_ld16(lane_addr + c0, r);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(lane_addr + c0, r);
+                        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st16(lane_addr + c0, r);
                     }
-                    tmem_wait_st();
-                    l_part *= alpha;
-                    m_run = mt;
+                } else {
+                    m_run = m_prev;
                 }
-                const float m_use = m_run == -INFINITY ? 0.f : m_run;
-                uint32_t pk[kHalfTok / 2];
-                float psum = 0.f;
-#pragma unroll
-                for (int i = 0; i < kHalfTok / 2; ++i) {
-                    const float p0 = ex2(s[2 * i] - m_use), p1 = ex2(s[2 * i + 1] - m_use);
-                    psum += p0 + p1;
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                l_part += psum;
-                if (!half_free && !wait_all(&bars[kPEmpty + pb], ((t >> 1) & 1) ^ 1, false)) {
+                m_s[pb * C::kHeads + h] = m_run;
+                mbar_arrive(&bars[kMReady + pb]);
+                // ---- P of the pair into TMEM buffer pb (last read by P.V(p - 2))
+                if (p >= 2 && !wait_own_pv(p - 2)) {
                     ok = false;
                     break;
                 }
-                // rows past the sequence end: zero their V columns in the stage
-                if (vmask != 0xFFFFFFFFull) {
-                    const int idx = hf * C::kHeads + h;
-                    const int r = idx & (C::kTile - 1), pn = idx / C::kTile;
-                    if (pn < C::kPVPanels && !((vmask >> r) & 1ull)) {
-                        uint8_t* base = stages + tile_base(t) + r * 128 + pn * C::kKvPanelBytes;
+                const float m_use = m_run == -INFINITY ? 0.f : m_run;
+                float psum = 0.f;
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(base + c * 16) = make_uint4(0, 0, 0, 0);
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(s[half * 32 + 2 * i] - m_use);
+                        const float p1 = ex2(s[half * 32 + 2 * i + 1] - m_use);
+                        psum += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(lane_addr + C::kTmemP + pb * (C::kPair / 2) + half * 16, pk);
+                }
+                if (m_l != m_run) {  // re-express this group's sum relative to the new maximum
+                    l_part = m_l == -INFINITY ? 0.f : l_part * ex2(m_l - m_run);
+                    m_l = m_run;
+                }
+                l_part += psum;
+                // rows past the sequence end: zero their V columns in the slot
+                // (thread h clears row h % 64 of V panels h / 64 + 2 k)
+                bool zeroed = false;
+                if (vm != ~0ull) {
+                    const int r = h & (C::kPair - 1);
+                    if (!((vm >> r) & 1ull)) {
+                        for (int pn = h / C::kPair; pn < C::kPVPanels; pn += C::kHeads / C::kPair) {
+                            uint8_t* base = stages + tile_base(t0) + r * 128 + pn * C::kKvPanelBytes;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4*>(base + c * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                        zeroed = true;
                     }
                 }
-                // P row h, K-major with the 128-byte swizzle: this tile fills the
-                // 16-byte chunks 4 * pb .. 4 * pb + 3 of the row, this thread two
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    *reinterpret_cast<uint4*>(p_row + (((4 * pb + 2 * hf + c) ^ (h & 7)) << 4)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                fence_proxy_async_smem();
+                if (__any_sync(0xffffffffu, zeroed)) fence_proxy_async_smem();
+                tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&bars[kPFull + pb]);
             }
             if (!ok) break;
 
-            // epilogue: O / l for this thread's half of the CTA's columns
-            if (!wait_all(&bars[kPEmpty + ((t - 1) & 1)], ((t - 1) >> 1) & 1, false)) {
-                ok = false;
-                break;
-            }
-            ls_s[hf * C::kHeads + h] = l_part;
-            if (!pair_sync()) {
-                ok = false;
-                break;
-            }
-            const float l_run = l_part + ls_s[(1 - hf) * C::kHeads + h];
-            tc_fence_after();
-            const float inv = l_run > 0.f ? a.out_scale / l_run : 0.f;
-            for (int c0 = ocol0; c0 < ocol0 + C::kOCols / 2; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + c0, r);
-                tmem_wait_ld();
-                if (!live_row) continue;
-                const int col = rank * C::kOCols + c0;
-                if (pc.whole) {
-                    __nv_bfloat16* o = a.out + (static_cast<long long>(pc.b) * a.H + h) * R + col;
+            // ---- piece epilogue: the group of the last pair writes the output
+            const int plast = gp + npairs - 1;
+            if ((plast & 1) != g) {
+                // hand this group's sum over (after the previous epilogue read the slot)
+                if (kpiece >= 1 && !wait_all(&bars[kOFree], (kpiece - 1) & 1, false)) {
+                    ok = false;
+                    break;
+                }
+                lh_s[h] = l_part;
+                mh_s[h] = m_l;
+                mbar_arrive(&bars[kLReady]);
+            } else {
+                if (!wait_all(&bars[kLReady], kpiece & 1, false) || !wait_own_pv(plast)) {
+                    ok = false;
+                    break;
+                }
+                const float lo = lh_s[h], mo = mh_s[h];
+                const float l_run = l_part + (mo == -INFINITY ? 0.f : lo * ex2(mo - m_l));
+                const float m_fin = m_l;
+                tc_fence_after();
+                const float inv = l_run > 0.f ? a.out_scale / l_run : 0.f;
+                for (int c0 = 0; c0 < C::kOCols; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + c0, r);
+                    tmem_wait_ld();
+                    if (!live_row) continue;
+                    const int col = rank * C::kOCols + c0;
+                    if (pc.whole) {
+                        __nv_bfloat16* o = a.out + (static_cast<long long>(pc.b) * a.H + h) * R + col;
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(r[i + 4]) * inv, __uint_as_float(r[i + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(r[i + 6]) * inv, __uint_as_float(r[i + 7]) * inv);
-                        *reinterpret_cast<uint4*>(o + i) = w;
+                        for (int i = 0; i < 32; i += 8) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(r[i + 4]) * inv, __uint_as_float(r[i + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(r[i + 6]) * inv, __uint_as_float(r[i + 7]) * inv);
+                            *reinterpret_cast<uint4*>(o + i) = w;
+                        }
+                    } else {
+                        float* o = a.ws_o + (static_cast<long long>(pc.slot) * a.H + h) * R + col;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(o + i) =
+                                make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
+                                            __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
                     }
-                } else {
-                    float* o = a.ws_o + (static_cast<long long>(pc.slot) * a.H + h) * R + col;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(o + i) =
-                            make_float4(__uint_as_float(r[i]) * inv, __uint_as_float(r[i + 1]) * inv,
-                                        __uint_as_float(r[i + 2]) * inv, __uint_as_float(r[i + 3]) * inv);
                 }
-            }
-            if (live_row && rank == 0 && hf == 0) {
-                const float lse = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-                if (pc.whole) {
-                    if (a.lse) a.lse[static_cast<long long>(pc.b) * a.H + h] = lse;
-                } else {
-                    a.ws_lse[static_cast<long long>(pc.slot) * a.H + h] = lse;
+                if (live_row && rank == 0) {
+                    const float lse = l_run > 0.f ? (m_fin + log2f(l_run)) * kLn2 : -INFINITY;
+                    if (pc.whole) {
+                        if (a.lse) a.lse[static_cast<long long>(pc.b) * a.H + h] = lse;
+                    } else {
+                        a.ws_lse[static_cast<long long>(pc.slot) * a.H + h] = lse;
+                    }
                 }
+                tc_fence_before();
+                mbar_arrive(&bars[kOFree]);
             }
+            gp += npairs;
+            ++kpiece;
         }
         if (!ok) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
     }
