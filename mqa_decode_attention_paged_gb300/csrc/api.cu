@@ -121,6 +121,32 @@ bool bf16_panel_map(CUtensorMap* out, const void* base, int cols, long long rows
     return true;
 }
 
+// 3D view {64 elements, rows, cols/64 panels} of a row-major bf16 matrix whose
+// box is {64, 64 rows, box_panels} with the 128-byte swizzle: one copy lands
+// box_panels panels of 64 consecutive rows, panel after panel, which is the
+// K-major operand layout of the tensor cores for each panel.  The panel
+// dimension has the smaller stride (128 bytes) than the row dimension.
+bool bf16_pair_map(CUtensorMap* out, const void* base, int cols, long long rows, int box_panels) {
+    const MapKey key{base, rows, cols, box_panels, 3};
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (map_lookup(key, out)) return true;
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof m);
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
+    const cuuint32_t box[3] = {64, 64, static_cast<cuuint32_t>(box_panels)};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    map_store(key, m);
+    *out = m;
+    return true;
+}
+
 // Encodes (or returns a cached copy of) a 3D view of a row-major MLA cache
 // [rows, cols] whose box is `box_rows` whole rows: bf16 rows are viewed as
 // {64 elements, cols/64 panels, rows} with the 128-byte swizzle, e4m3 rows as
@@ -231,11 +257,20 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
     if (num_heads > 64 && !fp8 && batch <= mqa::kMaxBatchTc) {
         mqa::MlaTcArgs t{};
         // boxes never straddle a page and never exceed a pipeline tile
-        int br = (page_size % 64 == 0) ? 64 : (page_size % 32 == 0 ? 32 : 16);
-        if (br > mqa::mla_tc_tile()) br = mqa::mla_tc_tile();
+        // pages of 64 tokens or more hold whole 64-token pairs: one 3D copy per
+        // pair and rank; smaller pages take one 2D copy per page and panel
+        const int br = (page_size % 64 == 0) ? 64 : (page_size % 32 == 0 ? 32 : 16);
         t.box_rows = br;
-        if (!bf16_panel_map(&t.kv_map, kv_cache, head_size, static_cast<long long>(num_blocks) * page_size, br) ||
-            !bf16_panel_map(&t.q_map, q, head_size, static_cast<long long>(batch) * num_heads, 128))
+        const long long kv_rows = static_cast<long long>(num_blocks) * page_size;
+        const int lo_panels = kv_lora_rank / 128, hi_panels = head_size / 64 - lo_panels;
+        if (br == 64) {
+            if (!bf16_pair_map(&t.kv_pair_map[0], kv_cache, head_size, kv_rows, lo_panels) ||
+                !bf16_pair_map(&t.kv_pair_map[1], kv_cache, head_size, kv_rows, hi_panels))
+                return cuda_fail(cudaErrorInvalidValue);
+        } else if (!bf16_panel_map(&t.kv_map, kv_cache, head_size, kv_rows, br)) {
+            return cuda_fail(cudaErrorInvalidValue);
+        }
+        if (!bf16_panel_map(&t.q_map, q, head_size, static_cast<long long>(batch) * num_heads, 128))
             return cuda_fail(cudaErrorInvalidValue);
         t.q = static_cast<const __nv_bfloat16*>(q);
         t.kv = static_cast<const uint8_t*>(kv_cache);

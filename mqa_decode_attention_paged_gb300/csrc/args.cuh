@@ -38,9 +38,12 @@ struct MlaArgs {
 
 // H = 128 tensor-core MLA path (2-CTA clusters split by feature columns).
 struct MlaTcArgs {
-    // bf16 cache as a 2D tensor {D, num_blocks * page}, box {64, box_rows},
-    // 128-byte swizzle; q as {D, B * H}, box {64, 128}, 128-byte swizzle.
+    // bf16 cache: with box_rows == 64 as 3D tensors {64, num_blocks * page,
+    // D / 64} with boxes {64, 64, panels of rank r} (kv_pair_map[r]), else as a
+    // 2D tensor {D, num_blocks * page} with box {64, box_rows} (kv_map); q as
+    // {D, B * H}, box {64, 128}; all with the 128-byte swizzle.
     CUtensorMap kv_map;
+    CUtensorMap kv_pair_map[2];
     CUtensorMap q_map;
     int box_rows;
     const __nv_bfloat16* q;  // [B, H, D]

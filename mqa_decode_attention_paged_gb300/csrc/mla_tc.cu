@@ -12,11 +12,11 @@
 // summed identically in both CTAs, which then run the same online softmax
 // (tutorial page lshu.cn/news/265860, §7).
 //
-// The cache streams in 32-token tiles; Q.K^T, the softmax and P.V work on
-// pairs of tiles (64 tokens).  Per CTA (352 threads):
-//   warp 0      TMA producer: each tile's rows of this CTA's column panels
+// The cache streams in 64-token pairs (masks are kept per 32-token tile).
+// Per CTA (352 threads):
+//   warp 0      TMA producer: each pair's rows of this CTA's column panels
 //               (tensor-map copies, 128-byte swizzle) into a ring of 64-row
-//               slots (two tiles each), so a pair is one contiguous operand;
+//               slots, one 3D copy per pair when pages hold whole pairs;
 //   warp 1      TMEM owner and single-thread MMA issuer:
 //               S[128 x 64] = Q K^T per pair (kind::f16, M = 128 heads, N = 64
 //               tokens, A = Q from TMEM), then O[128 x R/2] += P V per pair
@@ -44,7 +44,7 @@ namespace mqa {
 template <int D, int R>
 struct MlaTcCfg {
     static constexpr int kHeads = 128;
-    static constexpr int kTile = 32;  // tokens per pipeline stage; Q.K^T, softmax and P.V take two
+    static constexpr int kTile = 32;  // tokens per mask word half; a pair (pipeline stage) is two
     static constexpr int kPair = 2 * kTile;
     static constexpr int kPanels = D / 64;
     static constexpr int kLoPanels = R / 128;  // rank 0: QK panels = its P.V panels
@@ -79,7 +79,7 @@ struct MlaTcCfg {
         1024 + kQBytes + 2 * kXBytes + kNumBars * 8 + kRedBytes + 8 * 8 + 16 + 4 * (2 * kMaxBatchTc + 1);
     static constexpr int kSlotsFit = (227 * 1024 - kFixedBytes) / kSlotBytes;
     static constexpr int kSlots = kSlotsFit > 4 ? 4 : kSlotsFit;
-    static constexpr int kStages = 2 * kSlots;
+    static constexpr int kStages = kSlots;  // one pipeline stage per 64-token pair
     static constexpr int kOffQ = 0;
     static constexpr int kOffStages = kOffQ + kQBytes;
     static constexpr int kOffX = kOffStages + kSlots * kSlotBytes;
@@ -95,14 +95,15 @@ struct MlaTcCfg {
                       kTmemQ + 32 * kTmemQPanels <= kTmemCols,
                   "TMEM layout");
     static_assert(kSlots >= 2 && kStages <= 8, "pipeline depth");
+    static_assert(kSlots == kStages, "one ring slot per stage");
     static_assert(1024 + kOffCum + 4 * (2 * kMaxBatchTc + 1) <= 227 * 1024, "shared memory budget");
     static_assert(kOffStages % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzled operands need 1024-byte alignment");
 };
 
 // barrier slots, each range starting where the previous one ends
 enum TcBar {
-    kKvFull = 0,             // [8] tile landed (producer expect_tx + TMA bytes)
-    kKvEmpty = kKvFull + 8,  // [8] P.V of the tile's pair done (tensor-core commit)
+    kKvFull = 0,             // [8] pair landed (producer expect_tx + TMA bytes)
+    kKvEmpty = kKvFull + 8,  // [8] P.V of the pair done (tensor-core commit)
     kQFull = kKvEmpty + 8,   // Q panels kept in shared memory landed
     kQEmpty = kQFull + 1,    // every Q.K^T of the piece done
     kQTmem = kQEmpty + 1,    // a softmax group has written the piece's Q panels into TMEM
@@ -182,7 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         }
         mbar_init(&bars[kLReady], C::kGroupThreads);
         mbar_init(&bars[kOFree], C::kGroupThreads);
-        mbar_init(&bars[kDrain], 1);
+        mbar_init(&bars[kDrain], 2);  // one commit from each issuing thread
         fence_mbar_init();
         prefetch_tmap(&a.kv_map);
         prefetch_tmap(&a.q_map);
@@ -204,49 +205,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         const int n = tok_end > tok0 ? (tok_end - tok0 + C::kTile - 1) / C::kTile : 0;
         return (n + 1) & ~1;
     };
-    // byte offset of tile t's rows (of panel 0) in the ring
-    auto tile_base = [&](int t) {
-        return ((t % C::kStages) >> 1) * C::kSlotBytes + (t & 1) * (C::kTile * 128);
-    };
+    // byte offset of pair p's slot in the ring
+    auto slot_base = [&](int p) { return (p % C::kStages) * C::kSlotBytes; };
 
     if (warp == 0) {
         // ------------------------------------------------------ KV producer
-        if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            const int BR = a.box_rows, nbox = C::kTile / BR;
-            PieceIter it;
-            it.init(a.plan, cum, T, unit);
-            Piece pc;
-            int t = 0;
-            int issued[C::kStages];
-            for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
-            bool ok = true;
-            while (ok && it.next(cum, pc)) {
-                int tok0, tok_end;
-                const int nt = piece_tiles(pc, tok0, tok_end);
-                const int32_t* bt = a.block_table + static_cast<long long>(pc.b) * a.plan.max_blocks;
-                for (int j = 0; j < nt; ++j, ++t) {
-                    const int t0 = tok0 + j * C::kTile;
-                    int blk[2];
-                    bool val[2];
+        // The whole warp walks the pairs: lane l holds the block id of page
+        // l of the piece's current 32-page chunk (the next chunk is loaded
+        // one chunk ahead, so table reads stay off the issue path); lane 0
+        // waits for ring slots and issues the copies: one 3D copy per pair
+        // when pages hold whole pairs, else one 2D copy per page and panel.
+        const uint64_t pol = l2_policy_evict_first();
+        const int BR = a.box_rows, nbox = C::kPair / BR;  // boxes per pair (1, 2 or 4)
+        const CUtensorMap* pair_map = &a.kv_pair_map[rank];
+        PieceIter it;
+        it.init(a.plan, cum, T, unit);
+        Piece pc;
+        int p = 0;
+        bool ok = true;
+        while (ok && it.next(cum, pc)) {
+            int tok0, tok_end;
+            const int npairs = piece_tiles(pc, tok0, tok_end) >> 1;
+            if (npairs == 0) continue;
+            const int32_t* bt = a.block_table + static_cast<long long>(pc.b) * a.plan.max_blocks + pc.j0;
+            const int npg = pc.j1 - pc.j0;
+            auto load_chunk = [&](int c) {
+                const int pg = c * 32 + lane;
+                return pg < npg ? __ldg(bt + pg) : -1;
+            };
+            int chunk = 0;
+            int blk_cur = load_chunk(0);
+            int blk_nxt = load_chunk(1);
+            for (int jp = 0; jp < npairs; ++jp, ++p) {
+                const int t0 = tok0 + jp * C::kPair;
+                int blk[4];
+                bool val[4];
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const int tok = t0 + k * BR;
-                        val[k] = k < nbox && tok < tok_end;
-                        blk[k] = val[k] ? bt[tok / P] : 0;
+                for (int k = 0; k < 4; ++k) {
+                    const int tok = t0 + k * BR;
+                    val[k] = k < nbox && tok < tok_end;
+                    blk[k] = 0;
+                    if (val[k]) {  // warp-uniform
+                        const int rel = tok / P - pc.j0;  // page within the piece
+                        if ((rel >> 5) != chunk) {        // pairs advance by at most four pages
+                            blk_cur = blk_nxt;
+                            chunk = rel >> 5;
+                            blk_nxt = load_chunk(chunk + 1);
+                        }
+                        blk[k] = __shfl_sync(0xffffffffu, blk_cur, rel & 31);
                     }
-                    const int st = t % C::kStages;
-                    if (!mbar_wait(&bars[kKvEmpty + st], ((t / C::kStages) & 1) ^ 1)) {
-                        report(a.status, MQA_ERR_DEVICE_TIMEOUT);
-                        ok = false;
-                        break;
-                    }
+                }
+                const int st = p % C::kStages;
+                bool got = true;
+                if (lane == 0) got = mbar_wait(&bars[kKvEmpty + st], ((p / C::kStages) & 1) ^ 1);
+                if (!__shfl_sync(0xffffffffu, got, 0)) {
+                    if (lane == 0) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
                     const int n_tok = max(tok_end - t0, 0);
-                    uint64_t vmask = n_tok >= C::kTile ? 0xFFFFFFFFull : ((1ull << n_tok) - 1);
-                    const uint64_t ones = (1ull << BR) - 1;
+                    uint64_t vmask = n_tok >= C::kPair ? ~0ull : ((1ull << n_tok) - 1);
+                    const uint64_t ones = BR == 64 ? ~0ull : ((1ull << BR) - 1);
                     int nvalid = 0;
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
+                    for (int k = 0; k < 4; ++k) {
                         if (k >= nbox) break;
                         if (val[k] && (blk[k] < 0 || blk[k] >= a.num_blocks)) {
                             report(a.status, MQA_ERR_DEVICE_CHECK);
@@ -259,133 +282,86 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                     }
                     mask_s[st] = vmask;
                     mbar_arrive_expect_tx(&bars[kKvFull + st], nvalid * BR * 128 * np);
-                    uint8_t* dst = stages + tile_base(t);
+                    uint8_t* dst = stages + slot_base(p);
+                    if (BR == C::kPair) {
+                        if (val[0])
+                            tma_load_3d(dst, pair_map, 0, blk[0] * P + t0 % P, pbase, &bars[kKvFull + st], pol);
+                    } else {
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        if (k >= nbox || !val[k]) continue;
-                        const int row = blk[k] * P + (t0 + k * BR) % P;
-                        for (int pn = 0; pn < np; ++pn)
-                            tma_load_2d(dst + pn * C::kKvPanelBytes + k * BR * 128, &a.kv_map, (pbase + pn) * 64,
-                                        row, &bars[kKvFull + st], pol);
+                        for (int k = 0; k < 4; ++k) {
+                            if (k >= nbox || !val[k]) continue;
+                            const int row = blk[k] * P + (t0 + k * BR) % P;
+                            for (int pn = 0; pn < np; ++pn)
+                                tma_load_2d(dst + pn * C::kKvPanelBytes + k * BR * 128, &a.kv_map, (pbase + pn) * 64,
+                                            row, &bars[kKvFull + st], pol);
+                        }
                     }
-                    issued[st] = (t / C::kStages) & 1;
                 }
+                __syncwarp();
             }
-            for (int s = 0; s < C::kStages; ++s)
-                if (issued[s] >= 0 && !mbar_wait(&bars[kKvFull + s], static_cast<uint32_t>(issued[s])))
-                    report(a.status, MQA_ERR_DEVICE_TIMEOUT);
         }
+        // every copy issued has landed before the CTA may tear down
+        if (lane == 0)
+            for (int q = max(p - C::kStages, 0); q < p; ++q)
+                if (!mbar_wait(&bars[kKvFull + q % C::kStages], (q / C::kStages) & 1))
+                    report(a.status, MQA_ERR_DEVICE_TIMEOUT);
     } else if (warp == 2 + C::kSoftmaxWarps) {
-        // ------------------------------------------------------ Q loader
-        if (lane == 0 && np > nq_tmem) {
-            const uint64_t pol = l2_policy_evict_last();
-            PieceIter it;
-            it.init(a.plan, cum, T, unit);
-            Piece pc;
-            int qc = 0;
-            while (it.next(cum, pc)) {
-                int tok0, tok_end;
-                if (piece_tiles(pc, tok0, tok_end) == 0) continue;
-                if (!mbar_wait(&bars[kQEmpty], (qc & 1) ^ 1)) {
-                    report(a.status, MQA_ERR_DEVICE_TIMEOUT);
-                    break;
-                }
-                mbar_arrive_expect_tx(&bars[kQFull], (np - nq_tmem) * C::kQPanelBytes);
-                for (int pn = nq_tmem; pn < np; ++pn)
-                    tma_load_2d(q_s + (pn - nq_tmem) * C::kQPanelBytes, &a.q_map, (pbase + pn) * 64, pc.b * a.H,
-                                &bars[kQFull], pol);
-                ++qc;
-            }
-            if (qc > 0 && !mbar_wait(&bars[kQFull], (qc - 1) & 1)) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------ P.V issuer and Q loader
+        // One thread issues O += P V per pair as soon as its P is in TMEM
+        // (and, for a piece's first pair, the previous output was read out),
+        // and loads the Q panel kept in shared memory when its buffer frees.
         if (lane == 0) {
-            constexpr uint32_t kIdQK = umma_idesc_bf16(128, C::kPair, 0);
             constexpr uint32_t kIdPV = umma_idesc_bf16(128, C::kOCols, 1);
-            const uint32_t st_addr = smem_u32(stages);
-            // descriptor bases: K operand rows of the ring (K-major), V operand
-            // (MN-major, panel stride = slot panel), smem Q panel
-            const uint64_t kdesc0 = umma_desc(st_addr, 16, 1024);
-            const uint64_t vdesc0 = umma_desc(st_addr, C::kKvPanelBytes, 1024);
-            const uint64_t qdesc = umma_desc(smem_u32(q_s), 16, 1024);
-            bool ok = true;
-            // Two independent streams, issued as soon as their inputs are ready:
-            //   Q.K^T per pair (needs Q, both tiles, the S buffer read out),
-            //   P.V per pair (needs its P and, for a piece's first pair, the
-            //   previous piece's output read out of O).
-            PieceIter qi, vi;
-            qi.init(a.plan, cum, T, unit);
+            const uint64_t vdesc0 = umma_desc(smem_u32(stages), C::kKvPanelBytes, 1024);
+            const uint64_t pol = l2_policy_evict_last();
+            PieceIter vi, qi;
             vi.init(a.plan, cum, T, unit);
-            Piece qpc, vpc;
-            int qt = 0, qj = 0, qnt = 0, qc = 0;  // next Q.K^T: global tile qt, piece tile qj
-            int vt = 0, vj = 0, vnt = 0, vc = 0;  // next P.V: global tile vt, piece tile vj
-            bool q_loaded = false;
-            auto next_piece = [&](PieceIter& pi, Piece& pc, int& nt) {
+            qi.init(a.plan, cum, T, unit);
+            Piece vpc, qpc;
+            int vp = 0, vj = 0, vnp = 0, vc = 0;  // next P.V: pair vp, pair vj of piece vc (vnp pairs)
+            int qc = 0;                           // Q panel loads issued
+            auto next_piece = [&](PieceIter& pi, Piece& pc, int& npairs) {
                 int tok0, tok_end;
                 while (pi.next(cum, pc)) {
-                    nt = piece_tiles(pc, tok0, tok_end);
-                    if (nt > 0) return true;
+                    npairs = piece_tiles(pc, tok0, tok_end) >> 1;
+                    if (npairs > 0) return true;
                 }
                 return false;
             };
-            bool q_have = next_piece(qi, qpc, qnt);
-            bool v_have = next_piece(vi, vpc, vnt);
+            bool v_have = next_piece(vi, vpc, vnp);
+            int qnp = 0;
+            bool q_have = np > nq_tmem && next_piece(qi, qpc, qnp);
+            bool ok = true;
             unsigned long long idle_since = 0;
-            while (q_have || v_have) {
+            while (v_have || q_have) {
                 bool progressed = false;
-                if (q_have) {
-                    if (!q_loaded && mbar_test(&bars[kQTmem], qc & 1) &&
-                        (np == nq_tmem || mbar_test(&bars[kQFull], qc & 1))) {
-                        q_loaded = true;
-                        tc_fence_after();
-                    }
-                    const int qp = qt >> 1;
-                    if (q_loaded && mbar_test(&bars[kSEmpty], (qp & 1) ^ 1) &&
-                        mbar_test(&bars[kKvFull + qt % C::kStages], (qt / C::kStages) & 1) &&
-                        mbar_test(&bars[kKvFull + (qt + 1) % C::kStages], ((qt + 1) / C::kStages) & 1)) {
-                        tc_fence_after();
-                        const uint32_t d = tbase + C::kTmemS;
-                        const uint64_t kd = kdesc0 + static_cast<uint64_t>(tile_base(qt) >> 4);
-                        if (rank)
-                            issue_qk<C::kHiPanels, (C::kHiPanels < 4 ? C::kHiPanels : 4), C::kKvPanelBytes,
-                                     C::kQPanelBytes>(d, tbase + C::kTmemQ, kd, qdesc, kIdQK);
-                        else
-                            issue_qk<C::kLoPanels, (C::kLoPanels < 4 ? C::kLoPanels : 4), C::kKvPanelBytes,
-                                     C::kQPanelBytes>(d, tbase + C::kTmemQ, kd, qdesc, kIdQK);
-                        umma_commit(&bars[kSFull + (qp & 1)]);
-                        qt += 2;
-                        qj += 2;
-                        if (qj >= qnt) {
-                            umma_commit(&bars[kQEmpty]);  // Q may be replaced once these finish
-                            ++qc;
-                            q_loaded = false;
-                            qj = 0;
-                            q_have = next_piece(qi, qpc, qnt);
-                        }
-                        progressed = true;
-                    }
-                }
-                const int vp = vt >> 1, pb = vp & 1;
-                if (v_have && vt < qt && mbar_test(&bars[kPFull + pb], (vp >> 1) & 1) &&
+                const int pb = vp & 1;
+                if (v_have && mbar_test(&bars[kPFull + pb], (vp >> 1) & 1) &&
                     (vj > 0 || vc == 0 || mbar_test(&bars[kOFree], (vc - 1) & 1))) {
                     tc_fence_after();
-                    const uint64_t vd = vdesc0 + static_cast<uint64_t>(tile_base(vt) >> 4);
+                    const uint64_t vd = vdesc0 + static_cast<uint64_t>(slot_base(vp) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < C::kPair / 16; ++ks)
                         umma_bf16_ta(tbase, tbase + C::kTmemP + pb * (C::kPair / 2) + ks * 8,
                                      vd + static_cast<uint64_t>((ks * 16 * 128) >> 4), kIdPV,
                                      (vj == 0 && ks == 0) ? 0u : 1u);
                     umma_commit(&bars[kPEmpty + pb]);
-                    umma_commit(&bars[kKvEmpty + vt % C::kStages]);
-                    umma_commit(&bars[kKvEmpty + (vt + 1) % C::kStages]);
-                    vt += 2;
-                    vj += 2;
-                    if (vj >= vnt) {
+                    umma_commit(&bars[kKvEmpty + vp % C::kStages]);
+                    ++vp;
+                    if (++vj >= vnp) {
                         vj = 0;
                         ++vc;
-                        v_have = next_piece(vi, vpc, vnt);
+                        v_have = next_piece(vi, vpc, vnp);
                     }
+                    progressed = true;
+                }
+                if (q_have && mbar_test(&bars[kQEmpty], (qc & 1) ^ 1)) {
+                    mbar_arrive_expect_tx(&bars[kQFull], (np - nq_tmem) * C::kQPanelBytes);
+                    for (int pn = nq_tmem; pn < np; ++pn)
+                        tma_load_2d(q_s + (pn - nq_tmem) * C::kQPanelBytes, &a.q_map, (pbase + pn) * 64,
+                                    qpc.b * a.H, &bars[kQFull], pol);
+                    ++qc;
+                    q_have = next_piece(qi, qpc, qnp);
                     progressed = true;
                 }
                 if (progressed) {
@@ -401,7 +377,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 }
             }
             if (!ok) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
-            // no tensor-core work may be in flight when the CTA tears down
+            if (qc > 0 && !mbar_wait(&bars[kQFull], (qc - 1) & 1)) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+            // no tensor-core work of this thread may be in flight at teardown
+            umma_commit(&bars[kDrain]);
+            if (!mbar_wait(&bars[kDrain], 0)) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ Q.K^T issuer
+        // One thread issues S = Q K^T per pair, in pair order, once Q is in
+        // TMEM (and the shared-memory panel, if any), the previous pair's
+        // logits were read out and the pair's rows landed.
+        if (lane == 0) {
+            constexpr uint32_t kIdQK = umma_idesc_bf16(128, C::kPair, 0);
+            const uint64_t kdesc0 = umma_desc(smem_u32(stages), 16, 1024);
+            const uint64_t qdesc = umma_desc(smem_u32(q_s), 16, 1024);
+            PieceIter qi;
+            qi.init(a.plan, cum, T, unit);
+            Piece qpc;
+            int qp = 0, qc = 0;
+            bool ok = true;
+            while (ok && qi.next(cum, qpc)) {
+                int tok0, tok_end;
+                const int npairs = piece_tiles(qpc, tok0, tok_end) >> 1;
+                if (npairs == 0) continue;
+                if (!mbar_wait(&bars[kQTmem], qc & 1) ||
+                    (np > nq_tmem && !mbar_wait(&bars[kQFull], qc & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int j = 0; j < npairs; ++j, ++qp) {
+                    if (!mbar_wait(&bars[kSEmpty], (qp & 1) ^ 1) ||
+                        !mbar_wait(&bars[kKvFull + qp % C::kStages], (qp / C::kStages) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tbase + C::kTmemS;
+                    const uint64_t kd = kdesc0 + static_cast<uint64_t>(slot_base(qp) >> 4);
+                    if (rank)
+                        issue_qk<C::kHiPanels, (C::kHiPanels < 4 ? C::kHiPanels : 4), C::kKvPanelBytes,
+                                 C::kQPanelBytes>(d, tbase + C::kTmemQ, kd, qdesc, kIdQK);
+                    else
+                        issue_qk<C::kLoPanels, (C::kLoPanels < 4 ? C::kLoPanels : 4), C::kKvPanelBytes,
+                                 C::kQPanelBytes>(d, tbase + C::kTmemQ, kd, qdesc, kIdQK);
+                    umma_commit(&bars[kSFull + (qp & 1)]);
+                }
+                umma_commit(&bars[kQEmpty]);  // Q may be replaced once these finish
+                ++qc;
+            }
+            if (!ok) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
             umma_commit(&bars[kDrain]);
             if (!mbar_wait(&bars[kDrain], 0)) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
         }
@@ -481,7 +506,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             float l_part = 0.f, m_l = -INFINITY;
             for (int j = ((gp & 1) == g) ? 0 : 1; j < npairs; j += 2) {
                 const int p = gp + j, pb = p & 1;
-                const int t0 = 2 * p;
                 // ---- logits of the pair: own partial from TMEM
                 float s[C::kPair];
                 if (!wait_all(&bars[kSFull + pb], (p >> 1) & 1, false)) {
@@ -511,14 +535,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
 #pragma unroll
                 for (int c = 0; c < C::kPair / 4; ++c)
                     st_async_v4(x_remote + c * 512, s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3], xfull_remote);
-                // valid tokens of both tiles (set by the producer before kv_full)
-                if (!wait_all(&bars[kKvFull + t0 % C::kStages], (t0 / C::kStages) & 1, false) ||
-                    !wait_all(&bars[kKvFull + (t0 + 1) % C::kStages], ((t0 + 1) / C::kStages) & 1, false)) {
+                // valid tokens of the pair (set by the producer before kv_full)
+                if (!wait_all(&bars[kKvFull + p % C::kStages], (p / C::kStages) & 1, false)) {
                     ok = false;
                     break;
                 }
-                const uint64_t vm = (mask_s[t0 % C::kStages] & 0xFFFFFFFFull) |
-                                    (mask_s[(t0 + 1) % C::kStages] << 32);
+                const uint64_t vm = mask_s[p % C::kStages];
                 if (!wait_all(&bars[kXFull + g], (p >> 1) & 1, true)) {
                     ok = false;
                     break;
@@ -616,7 +638,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                     const int r = h & (C::kPair - 1);
                     if (!((vm >> r) & 1ull)) {
                         for (int pn = h / C::kPair; pn < C::kPVPanels; pn += C::kHeads / C::kPair) {
-                            uint8_t* base = stages + tile_base(t0) + r * 128 + pn * C::kKvPanelBytes;
+                            uint8_t* base = stages + slot_base(p) + r * 128 + pn * C::kKvPanelBytes;
 #pragma unroll
                             for (int c = 0; c < 8; ++c)
                                 *reinterpret_cast<uint4*>(base + c * 16) = make_uint4(0, 0, 0, 0);
