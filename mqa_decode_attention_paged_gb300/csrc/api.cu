@@ -147,6 +147,51 @@ bool bf16_pair_map(CUtensorMap* out, const void* base, int cols, long long rows,
     return true;
 }
 
+// e4m3 counterparts of the two views above, unswizzled: {64 bytes, rows,
+// cols/64 panels} with box {64, 64, box_panels} (one pair, panel after panel,
+// 64 bytes per row), and {cols, rows} with box {64, box_rows}.
+bool e4m3_pair_map(CUtensorMap* out, const void* base, int cols, long long rows, int box_panels) {
+    const MapKey key{base, rows, cols, box_panels, 4};
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (map_lookup(key, out)) return true;
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof m);
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), 64};
+    const cuuint32_t box[3] = {64, 64, static_cast<cuuint32_t>(box_panels)};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, elem,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    map_store(key, m);
+    *out = m;
+    return true;
+}
+
+bool e4m3_panel_map(CUtensorMap* out, const void* base, int cols, long long rows, int box_rows) {
+    const MapKey key{base, rows, cols, box_rows, 5};
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (map_lookup(key, out)) return true;
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof m);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t elem[2] = {1, 1};
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, elem,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    map_store(key, m);
+    *out = m;
+    return true;
+}
+
 // Encodes (or returns a cached copy of) a 3D view of a row-major MLA cache
 // [rows, cols] whose box is `box_rows` whole rows: bf16 rows are viewed as
 // {64 elements, cols/64 panels, rows} with the 128-byte swizzle, e4m3 rows as
@@ -253,8 +298,9 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t slots_tc = static_cast<size_t>(batch) * num_kv_splits;
 
-    // 65..128 heads over a bf16 cache: 2-CTA tensor-core clusters
-    if (num_heads > 64 && !fp8 && batch <= mqa::kMaxBatchTc) {
+    // 65..128 heads: 2-CTA tensor-core clusters (an e4m3 cache is widened to
+    // f16 in shared memory)
+    if (num_heads > 64 && batch <= mqa::kMaxBatchTc) {
         mqa::MlaTcArgs t{};
         // boxes never straddle a page and never exceed a pipeline tile
         // pages of 64 tokens or more hold whole 64-token pairs: one 3D copy per
@@ -263,11 +309,13 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
         t.box_rows = br;
         const long long kv_rows = static_cast<long long>(num_blocks) * page_size;
         const int lo_panels = kv_lora_rank / 128, hi_panels = head_size / 64 - lo_panels;
+        auto pair_map = fp8 ? e4m3_pair_map : bf16_pair_map;
+        auto panel_map = fp8 ? e4m3_panel_map : bf16_panel_map;
         if (br == 64) {
-            if (!bf16_pair_map(&t.kv_pair_map[0], kv_cache, head_size, kv_rows, lo_panels) ||
-                !bf16_pair_map(&t.kv_pair_map[1], kv_cache, head_size, kv_rows, hi_panels))
+            if (!pair_map(&t.kv_pair_map[0], kv_cache, head_size, kv_rows, lo_panels) ||
+                !pair_map(&t.kv_pair_map[1], kv_cache, head_size, kv_rows, hi_panels))
                 return cuda_fail(cudaErrorInvalidValue);
-        } else if (!bf16_panel_map(&t.kv_map, kv_cache, head_size, kv_rows, br)) {
+        } else if (!panel_map(&t.kv_map, kv_cache, head_size, kv_rows, br)) {
             return cuda_fail(cudaErrorInvalidValue);
         }
         if (!bf16_panel_map(&t.q_map, q, head_size, static_cast<long long>(batch) * num_heads, 128))
@@ -281,8 +329,10 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
         t.ws_o = static_cast<float*>(workspace);
         t.ws_lse = need > 0 ? t.ws_o + slots_tc * num_heads * kv_lora_rank : nullptr;
         t.status = device_status;
-        t.sl2 = scale * mqa::kLog2e;
-        t.out_scale = 1.0f;
+        // an e4m3 cache holds K / k_scale: k_scale scales the logits and, as
+        // V's scale, the output
+        t.sl2 = scale * (fp8 ? k_scale : 1.0f) * mqa::kLog2e;
+        t.out_scale = fp8 ? k_scale : 1.0f;
         t.H = num_heads;
         t.num_blocks = num_blocks;
         t.plan.batch = batch;
@@ -290,7 +340,7 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
         t.plan.max_blocks = max_blocks;
         t.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
         t.plan.units = t.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms / 2);
-        if (cudaError_t e = mqa::mla_tc_stage1(t, head_size, t.plan.units, st); e != cudaSuccess)
+        if (cudaError_t e = mqa::mla_tc_stage1(t, head_size, fp8, t.plan.units, st); e != cudaSuccess)
             return cuda_fail(e);
         if (!t.plan.per_seq) {
             mqa::MergeArgs m{};

@@ -92,7 +92,7 @@ cudaError_t mla_mma_stage1(const MlaArgs& a, int D, bool fp8, int grid, cudaStre
 size_t mla_mma_smem_bytes(int D, bool fp8, int batch);
 int mla_mma_tile();
 cudaError_t gqa_mma_stage1(const GqaArgs& a, int D, int grid, cudaStream_t stream);
-cudaError_t mla_tc_stage1(const MlaTcArgs& a, int D, int clusters, cudaStream_t stream);
+cudaError_t mla_tc_stage1(const MlaTcArgs& a, int D, bool fp8, int clusters, cudaStream_t stream);
 int mla_tc_tile();
 constexpr int kMaxBatchTc = 512;  // page prefix of the H = 128 path lives in smem
 size_t gqa_mma_smem_bytes(int D, int hkv, int batch);

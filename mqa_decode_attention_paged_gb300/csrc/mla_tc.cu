@@ -116,7 +116,8 @@ enum TcBar {
     kMReady = kXFree + 2,    // [2] running maximum after a pair of parity i published
     kLReady = kMReady + 2,   // the group without the piece's last pair handed over its sum
     kOFree = kLReady + 1,    // the piece's output has been read out of TMEM
-    kDrain = kOFree + 1,     // every tensor-core operation of the CTA has completed
+    kConv = kOFree + 1,      // [2] fp8 cache: the pair of parity i was widened to f16 in its slot
+    kDrain = kConv + 2,      // every tensor-core operation of the CTA has completed
     kBarCount = kDrain + 1,
 };
 static_assert(kBarCount <= MlaTcCfg<576, 512>::kNumBars && kBarCount <= MlaTcCfg<320, 256>::kNumBars,
@@ -140,7 +141,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d, uint32_t q_tmem, uint64_t k
     }
 }
 
-template <int D, int R>
+template <int D, int R, bool FP8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThreads, 1)
     mla_decode_tc_kernel(const __grid_constant__ MlaTcArgs a) {
     using C = MlaTcCfg<D, R>;
@@ -182,6 +183,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             mbar_init(&bars[kMReady + i], C::kGroupThreads);
         }
         mbar_init(&bars[kLReady], C::kGroupThreads);
+        for (int i = 0; i < 2; ++i) mbar_init(&bars[kConv + i], C::kGroupThreads);
         mbar_init(&bars[kOFree], C::kGroupThreads);
         mbar_init(&bars[kDrain], 2);  // one commit from each issuing thread
         fence_mbar_init();
@@ -207,6 +209,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
     };
     // byte offset of pair p's slot in the ring
     auto slot_base = [&](int p) { return (p % C::kStages) * C::kSlotBytes; };
+    // fp8 cache: the pair's e4m3 panels (64 rows x 64 bytes each, unswizzled)
+    // land at the end of the slot and are widened in place to f16 panels
+    constexpr int kF8PanelBytes = C::kPair * 64;
+    const int f8_off = FP8 ? C::kSlotBytes - np * kF8PanelBytes : 0;
+    constexpr int kRowBytes = FP8 ? 64 : 128;  // bytes per cache row and panel as copied
 
     if (warp == 0) {
         // ------------------------------------------------------ KV producer
@@ -281,8 +288,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                             vmask &= ~(ones << (k * BR));
                     }
                     mask_s[st] = vmask;
-                    mbar_arrive_expect_tx(&bars[kKvFull + st], nvalid * BR * 128 * np);
-                    uint8_t* dst = stages + slot_base(p);
+                    mbar_arrive_expect_tx(&bars[kKvFull + st], nvalid * BR * kRowBytes * np);
+                    uint8_t* dst = stages + slot_base(p) + f8_off;
                     if (BR == C::kPair) {
                         if (val[0])
                             tma_load_3d(dst, pair_map, 0, blk[0] * P + t0 % P, pbase, &bars[kKvFull + st], pol);
@@ -292,8 +299,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                             if (k >= nbox || !val[k]) continue;
                             const int row = blk[k] * P + (t0 + k * BR) % P;
                             for (int pn = 0; pn < np; ++pn)
-                                tma_load_2d(dst + pn * C::kKvPanelBytes + k * BR * 128, &a.kv_map, (pbase + pn) * 64,
-                                            row, &bars[kKvFull + st], pol);
+                                tma_load_2d(dst + pn * (C::kPair * kRowBytes) + k * BR * kRowBytes, &a.kv_map,
+                                            (pbase + pn) * 64, row, &bars[kKvFull + st], pol);
                         }
                     }
                 }
@@ -311,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         // (and, for a piece's first pair, the previous output was read out),
         // and loads the Q panel kept in shared memory when its buffer frees.
         if (lane == 0) {
-            constexpr uint32_t kIdPV = umma_idesc_bf16(128, C::kOCols, 1);
+            constexpr uint32_t kIdPV = FP8 ? umma_idesc_f16(128, C::kOCols, 1) : umma_idesc_bf16(128, C::kOCols, 1);
             const uint64_t vdesc0 = umma_desc(smem_u32(stages), C::kKvPanelBytes, 1024);
             const uint64_t pol = l2_policy_evict_last();
             PieceIter vi, qi;
@@ -330,7 +337,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             };
             bool v_have = next_piece(vi, vpc, vnp);
             int qnp = 0;
-            bool q_have = np > nq_tmem && next_piece(qi, qpc, qnp);
+            // (the fp8 kernel's softmax rows write that panel themselves, in f16)
+            bool q_have = !FP8 && np > nq_tmem && next_piece(qi, qpc, qnp);
             bool ok = true;
             unsigned long long idle_since = 0;
             while (v_have || q_have) {
@@ -388,7 +396,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         // TMEM (and the shared-memory panel, if any), the previous pair's
         // logits were read out and the pair's rows landed.
         if (lane == 0) {
-            constexpr uint32_t kIdQK = umma_idesc_bf16(128, C::kPair, 0);
+            constexpr uint32_t kIdQK = FP8 ? umma_idesc_f16(128, C::kPair, 0) : umma_idesc_bf16(128, C::kPair, 0);
             const uint64_t kdesc0 = umma_desc(smem_u32(stages), 16, 1024);
             const uint64_t qdesc = umma_desc(smem_u32(q_s), 16, 1024);
             PieceIter qi;
@@ -401,14 +409,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 const int npairs = piece_tiles(qpc, tok0, tok_end) >> 1;
                 if (npairs == 0) continue;
                 if (!mbar_wait(&bars[kQTmem], qc & 1) ||
-                    (np > nq_tmem && !mbar_wait(&bars[kQFull], qc & 1))) {
+                    (!FP8 && np > nq_tmem && !mbar_wait(&bars[kQFull], qc & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int j = 0; j < npairs; ++j, ++qp) {
-                    if (!mbar_wait(&bars[kSEmpty], (qp & 1) ^ 1) ||
-                        !mbar_wait(&bars[kKvFull + qp % C::kStages], (qp / C::kStages) & 1)) {
+                    // bf16: the pair's rows landed; fp8: they were also widened to f16
+                    const bool ready = FP8 ? mbar_wait(&bars[kConv + (qp & 1)], (qp >> 1) & 1)
+                                           : mbar_wait(&bars[kKvFull + qp % C::kStages], (qp / C::kStages) & 1);
+                    if (!mbar_wait(&bars[kSEmpty], (qp & 1) ^ 1) || !ready) {
                         ok = false;
                         break;
                     }
@@ -468,8 +478,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 for (int c = 0; c < 4 * nq_tmem; ++c) {  // 8 columns (16 dims) at a time
                     const uint4 v0 = live_row ? __ldg(src + 2 * c) : make_uint4(0, 0, 0, 0);
                     const uint4 v1 = live_row ? __ldg(src + 2 * c + 1) : make_uint4(0, 0, 0, 0);
-                    const uint32_t r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    uint32_t r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    if constexpr (FP8) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) r[i] = bf16x2_to_f16x2(r[i]);
+                    }
                     tmem_st8(lane_addr + C::kTmemQ + c * 8, r);
+                }
+                if constexpr (FP8) {
+                    // panels past the TMEM ones, f16, as the K-major swizzled smem operand
+                    for (int pn = nq_tmem; pn < np; ++pn) {
+                        uint8_t* row = q_s + (pn - nq_tmem) * C::kQPanelBytes + h * 128;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            uint4 v = live_row ? __ldg(src + pn * 8 + c) : make_uint4(0, 0, 0, 0);
+                            v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                                           bf16x2_to_f16x2(v.w));
+                            *reinterpret_cast<uint4*>(row + ((c ^ (h & 7)) << 4)) = v;
+                        }
+                    }
+                    fence_proxy_async_smem();
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -506,6 +534,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             float l_part = 0.f, m_l = -INFINITY;
             for (int j = ((gp & 1) == g) ? 0 : 1; j < npairs; j += 2) {
                 const int p = gp + j, pb = p & 1;
+                if constexpr (FP8) {
+                    // ---- widen the pair's e4m3 panels to f16 in place: thread t
+                    // takes row t / 2, bytes 32 (t % 2) .. + 31 of each panel; all
+                    // reads of a panel precede its writes (the f16 panel overlaps
+                    // its own e4m3 source, never a later panel's)
+                    if (!wait_all(&bars[kKvFull + p % C::kStages], (p / C::kStages) & 1, false)) {
+                        ok = false;
+                        break;
+                    }
+                    const int t = quad * 32 + lane, r = t >> 1, hb = t & 1;
+                    uint8_t* slot = stages + slot_base(p);
+                    for (int pn = 0; pn < np; ++pn) {
+                        const uint8_t* srcp = slot + f8_off + pn * kF8PanelBytes + r * 64 + hb * 32;
+                        const uint4 w0 = *reinterpret_cast<const uint4*>(srcp);
+                        const uint4 w1 = *reinterpret_cast<const uint4*>(srcp + 16);
+                        named_bar_sync(1 + g, C::kGroupThreads);
+                        const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        uint8_t* dstp = slot + pn * C::kKvPanelBytes + r * 128;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t o[4];
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                o[2 * i] = e4m3x2_to_f16x2(w[2 * c + i] & 0xffffu);
+                                o[2 * i + 1] = e4m3x2_to_f16x2(w[2 * c + i] >> 16);
+                            }
+                            *reinterpret_cast<uint4*>(dstp + (((hb * 4 + c) ^ (r & 7)) << 4)) =
+                                make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[kConv + pb]);
+                }
                 // ---- logits of the pair: own partial from TMEM
                 float s[C::kPair];
                 if (!wait_all(&bars[kSFull + pb], (p >> 1) & 1, false)) {
@@ -536,7 +597,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 for (int c = 0; c < C::kPair / 4; ++c)
                     st_async_v4(x_remote + c * 512, s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3], xfull_remote);
                 // valid tokens of the pair (set by the producer before kv_full)
-                if (!wait_all(&bars[kKvFull + p % C::kStages], (p / C::kStages) & 1, false)) {
+                if (!FP8 && !wait_all(&bars[kKvFull + p % C::kStages], (p / C::kStages) & 1, false)) {
                     ok = false;
                     break;
                 }
@@ -622,7 +683,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                         const float p0 = ex2(s[half * 32 + 2 * i] - m_use);
                         const float p1 = ex2(s[half * 32 + 2 * i + 1] - m_use);
                         psum += p0 + p1;
-                        pk[i] = pack_bf16x2(p0, p1);
+                        pk[i] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                     }
                     tmem_st16(lane_addr + C::kTmemP + pb * (C::kPair / 2) + half * 16, pk);
                 }
@@ -728,11 +789,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
     }
 }
 
-template <int D, int R>
+template <int D, int R, bool FP8>
 static cudaError_t launch_mla_tc(const MlaTcArgs& a, int clusters, cudaStream_t stream) {
     using C = MlaTcCfg<D, R>;
     const size_t smem = C::smem_bytes(a.plan.batch);
-    auto kern = mla_decode_tc_kernel<D, R>;
+    auto kern = mla_decode_tc_kernel<D, R, FP8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -741,9 +802,10 @@ static cudaError_t launch_mla_tc(const MlaTcArgs& a, int clusters, cudaStream_t 
     return cudaGetLastError();
 }
 
-cudaError_t mla_tc_stage1(const MlaTcArgs& a, int D, int clusters, cudaStream_t stream) {
-    if (D == 576) return launch_mla_tc<576, 512>(a, clusters, stream);
-    return launch_mla_tc<320, 256>(a, clusters, stream);
+cudaError_t mla_tc_stage1(const MlaTcArgs& a, int D, bool fp8, int clusters, cudaStream_t stream) {
+    if (D == 576) return fp8 ? launch_mla_tc<576, 512, true>(a, clusters, stream)
+                             : launch_mla_tc<576, 512, false>(a, clusters, stream);
+    return fp8 ? launch_mla_tc<320, 256, true>(a, clusters, stream) : launch_mla_tc<320, 256, false>(a, clusters, stream);
 }
 
 int mla_tc_tile() { return MlaTcCfg<576, 512>::kTile; }

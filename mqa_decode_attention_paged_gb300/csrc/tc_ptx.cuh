@@ -5,7 +5,29 @@
 
 #include "common.cuh"
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 namespace mqa {
+
+// Two e4m3 values (low byte first) widened to two f16 values (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xffffu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Two bf16 values (low half first) as two f16 values (round to nearest; exact
+// for values that f16 represents).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 // ---- shared-memory matrix descriptor (K-major or MN-major, 128-byte swizzle)
 // bits 0-13 start address >> 4, 16-29 leading-dimension byte offset >> 4,
@@ -27,6 +49,12 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
 // bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
 // 15 / 16 A / B major-ness (0 = K-major, 1 = MN-major), 17-22 N >> 3,
 // 24-28 M >> 4.
+// Same layout with f16 A and B (format 0) instead of bf16.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int b_mn_major) {
+    return (1u << 4) | (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);

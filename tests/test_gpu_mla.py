@@ -54,6 +54,19 @@ def test_tensor_core_path_ragged(D, page, splits):
     assert_close(out, lse, ref_out, ref_lse, what=f"tc D={D} P={page} S={splits}")
 
 
+@pytest.mark.parametrize("D", [576, 320])
+@pytest.mark.parametrize("page", [16, 64])
+@pytest.mark.parametrize("splits", [1, 4])
+def test_tensor_core_path_fp8_ragged(D, page, splits):
+    # The e4m3 cache on the tensor-core clusters: the tile is widened to f16 in
+    # shared memory and k_scale scales the logits and the output.
+    case = synth.poison(synth.make_mla_case(RAGGED, H=128, D=D, page=page, kv_dtype="fp8_e4m3", k_scale=0.05,
+                                            pool_factor=1.2, seed=18, extra_cols=1))
+    out, lse = run_gpu(case, splits)
+    ref_out, ref_lse = run_oracle(case)
+    assert_close(out, lse, ref_out, ref_lse, fp8=True, what=f"tc fp8 D={D} P={page} S={splits}")
+
+
 def test_tensor_core_path_multi_tile_and_rescale():
     # Long pieces (many tiles), and a late key with a much larger logit so the
     # running max jumps by more than 2^8 mid-sequence (forces the O rescale).
