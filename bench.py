@@ -46,17 +46,23 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one stage-1
 # launch from an ncu capture (summaries under profiles/), keyed by workload;
-# valid only while the kernel sources hash to `src_sha`.
+# valid only while the sources that kernel is built from hash to `src_sha`.
+MMA_FILES = ("mla_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
+TC_FILES = ("mla_tc.cu", "tc_ptx.cuh", "common.cuh", "plan.cuh", "args.cuh")
 NCU_TRAFFIC = {
-    "mla_v2lite": {"src_sha": "720d253541ee62e8", "splits": 16, "bytes": 329808128 + 4158208,
+    "mla_v2lite": {"files": MMA_FILES, "src_sha": "f0c5aa8c76fa033a", "splits": 16, "bytes": 329797120 + 3693568,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64>"},
+    "mla_longctx": {"files": TC_FILES, "src_sha": "d40fee9a247ef998", "splits": 256, "bytes": 478712576 + 3590400,
+                    "kernel": "mla_decode_tc_kernel<576,512,0>"},
+    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "d40fee9a247ef998", "splits": 64, "bytes": 1403810304 + 5198848,
+                   "kernel": "mla_decode_tc_kernel<576,512,1>"},
 }
 
 
-def kernel_sources_sha() -> str:
+def kernel_sources_sha(files=None) -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "mqa_decode_attention_paged_gb300", "csrc")
-    for fn in sorted(os.listdir(d)):
+    for fn in sorted(files if files is not None else os.listdir(d)):
         with open(os.path.join(d, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -193,6 +199,22 @@ def time_oracle(case, budget_s=12.0, min_reps=1):
     sample = (f"{rows_used} of {case.batch} requests (all heads, {done_tokens} tokens) in {elapsed:.1f} s "
               f"of fp64 oracle work on {cores} host threads")
     return gbs, cores, sample, elapsed, done_tokens
+
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Each value's maximum over all ranks (the values themselves without a
+    process group): step times are reported as the slowest rank's."""
+    import torch
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput_gbs(world, bytes_per_rank, ms):
+    """Whole-job throughput in GB/s: every rank decodes its own replica of the
+    workload (weak scaling), all within the slowest rank's `ms`."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
 
 
 def dist_env():
@@ -344,13 +366,10 @@ def run_ours(args):
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
     # ---- max over ranks
-    t = torch.tensor([mean_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    mean_ms, e2e_ms = float(t[0]), float(t[1])
+    mean_ms, e2e_ms = max_over_ranks([mean_ms, e2e_ms], dist, dev)
 
     peaks, peak_src = load_peaks()
-    kv_gbs = world * st["kv_bytes"] / (mean_ms * 1e-3) / 1e9
+    kv_gbs = job_throughput_gbs(world, st["kv_bytes"], mean_ms)
     alg_gbs = st["alg_bytes"] / (mean_ms * 1e-3) / 1e9
     tflops = st["flops"] / (mean_ms * 1e-3) / 1e12
     t_hbm = st["alg_bytes"] / (peaks["hbm_gbs"] * 1e9)
@@ -359,7 +378,7 @@ def run_ours(args):
     traffic = None
     tr = NCU_TRAFFIC.get(args.workload)
     traffic_kernel = None
-    if tr and tr.get("src_sha") == kernel_sources_sha() and tr.get("splits") == splits:
+    if tr and tr.get("src_sha") == kernel_sources_sha(tr["files"]) and tr.get("splits") == splits:
         traffic = tr["bytes"]
         traffic_kernel = tr["kernel"] + " (stage 1 only)"
     if bound == "hbm":
@@ -393,7 +412,7 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1) q/KV, random block permutation)",
         "config": workload_config(case, args.workload, splits),
         "roofline": roof, "cpu_baseline": cpu,
-        "e2e": {"value": round(world * st["kv_bytes"] / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_throughput_gbs(world, st["kv_bytes"], e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "per step: q, block_table, seq_lens host->device and out, lse device->host "
                         "(pinned host buffers); the KV cache is decode state resident in HBM"},

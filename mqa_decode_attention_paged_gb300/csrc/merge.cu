@@ -112,15 +112,24 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergeArg
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         const float* base = a.ws_o + (static_cast<long long>(gf + b) * a.H + h) * R + 4 * c4;
         const long long step = static_cast<long long>(a.H) * R;
-#pragma unroll 4
-        for (int i = 0; i < np; ++i) {
-            const float w = s_w[i];
-            if (w == 0.f) continue;
-            const float4 v = *reinterpret_cast<const float4*>(base + i * step);
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+        // eight partial rows in flight per thread; a segment with weight 0
+        // (empty, never written) contributes by selection, not by product
+        for (int i0 = 0; i0 < np; i0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                v[k] = i0 + k < np ? __ldcs(reinterpret_cast<const float4*>(base + (i0 + k) * step))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float w = i0 + k < np ? s_w[i0 + k] : 0.f;
+                if (w != 0.f) {
+                    acc.x += w * v[k].x;
+                    acc.y += w * v[k].y;
+                    acc.z += w * v[k].z;
+                    acc.w += w * v[k].w;
+                }
+            }
         }
         uint2 packed;
         packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);

@@ -1,0 +1,98 @@
+"""Host-side logic of bench.py for N > 1 ranks, on the CPU with gloo.
+
+The GPU bench runs one replica of the workload per rank (weak scaling) and
+reports the slowest rank's step time; these tests cover that reduction with
+two gloo processes, the whole-job throughput, and the reference arm's rank
+handling (only rank 0 runs the oracle and prints)."""
+import json
+import os
+import socket
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r took (r + 1) ms per step and 10 - r ms end to end
+        got = bench.max_over_ranks([rank + 1.0, 10.0 - rank], dist)
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+            json.dump(got, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_processes(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       start_method="spawn", join=True)
+    for r in range(world):
+        with open(tmp_path / f"rank{r}.json") as f:
+            assert json.load(f) == [2.0, 10.0]
+
+
+def test_max_over_ranks_without_a_group_is_identity():
+    assert bench.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]
+
+
+def test_whole_job_throughput_scales_with_ranks():
+    one = bench.job_throughput_gbs(1, 1e9, 10.0)
+    assert one == pytest.approx(100.0)
+    assert bench.job_throughput_gbs(4, 1e9, 10.0) == pytest.approx(4 * one)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+
+    class Args:
+        workload = "tiny_mla"
+        splits = 0
+        steps = 1
+        warmup = 0
+        gpus = 2
+        ref_budget = 0.05
+
+    assert bench.run_reference(Args()) is None
+    assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_rank_zero_prints_one_line(monkeypatch, capsys):
+    pytest.importorskip("numpy")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("LOCAL_RANK", "0")
+
+    class Args:
+        workload = "tiny_mla"
+        splits = 0
+        steps = 1
+        warmup = 0
+        gpus = 1
+        ref_budget = 0.05
+
+    bench.run_reference(Args())
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["gpu_launches"] == 0
