@@ -192,6 +192,32 @@ bool e4m3_panel_map(CUtensorMap* out, const void* base, int cols, long long rows
     return true;
 }
 
+// 2D view {cols, rows} of the cache with box {32, box_rows}: the 32-column
+// rope halves, with the 64-byte swizzle for bf16 (the K-major operand layout
+// of 64-byte rows) and unswizzled for e4m3.
+bool rope_half_map(CUtensorMap* out, const void* base, int cols, long long rows, int box_rows, bool fp8) {
+    const MapKey key{base, rows, cols, box_rows, fp8 ? 7 : 6};
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (map_lookup(key, out)) return true;
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof m);
+    const int elt = fp8 ? 1 : 2;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elt};
+    const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t elem[2] = {1, 1};
+    if (fn(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+           dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    map_store(key, m);
+    *out = m;
+    return true;
+}
+
 // Encodes (or returns a cached copy of) a 3D view of a row-major MLA cache
 // [rows, cols] whose box is `box_rows` whole rows: bf16 rows are viewed as
 // {64 elements, cols/64 panels, rows} with the 128-byte swizzle, e4m3 rows as
@@ -308,17 +334,18 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
         const int br = (page_size % 64 == 0) ? 64 : (page_size % 32 == 0 ? 32 : 16);
         t.box_rows = br;
         const long long kv_rows = static_cast<long long>(num_blocks) * page_size;
-        const int lo_panels = kv_lora_rank / 128, hi_panels = head_size / 64 - lo_panels;
+        // each rank holds kv_lora_rank / 128 full 64-column panels and one
+        // 32-column half of the rope part
+        const int rank_panels = kv_lora_rank / 128;
         auto pair_map = fp8 ? e4m3_pair_map : bf16_pair_map;
         auto panel_map = fp8 ? e4m3_panel_map : bf16_panel_map;
         if (br == 64) {
-            if (!pair_map(&t.kv_pair_map[0], kv_cache, head_size, kv_rows, lo_panels) ||
-                !pair_map(&t.kv_pair_map[1], kv_cache, head_size, kv_rows, hi_panels))
+            if (!pair_map(&t.kv_pair_map[0], kv_cache, head_size, kv_rows, rank_panels))
                 return cuda_fail(cudaErrorInvalidValue);
         } else if (!panel_map(&t.kv_map, kv_cache, head_size, kv_rows, br)) {
             return cuda_fail(cudaErrorInvalidValue);
         }
-        if (!bf16_panel_map(&t.q_map, q, head_size, static_cast<long long>(batch) * num_heads, 128))
+        if (!rope_half_map(&t.kv_rope_map, kv_cache, head_size, kv_rows, br, fp8))
             return cuda_fail(cudaErrorInvalidValue);
         t.q = static_cast<const __nv_bfloat16*>(q);
         t.kv = static_cast<const uint8_t*>(kv_cache);

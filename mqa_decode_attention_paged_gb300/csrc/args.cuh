@@ -38,13 +38,15 @@ struct MlaArgs {
 
 // H = 128 tensor-core MLA path (2-CTA clusters split by feature columns).
 struct MlaTcArgs {
-    // bf16 cache: with box_rows == 64 as 3D tensors {64, num_blocks * page,
-    // D / 64} with boxes {64, 64, panels of rank r} (kv_pair_map[r]), else as a
-    // 2D tensor {D, num_blocks * page} with box {64, box_rows} (kv_map); q as
-    // {D, B * H}, box {64, 128}; all with the 128-byte swizzle.
+    // The cache (bf16, or e4m3 unswizzled): with box_rows == 64 as a 3D
+    // tensor {64, num_blocks * page, D / 64} with box {64, 64, R / 128}
+    // (kv_pair_map[0]: one rank's kv_c panels of a 64-token pair), else as a
+    // 2D tensor {D, num_blocks * page} with box {64, box_rows} (kv_map); the
+    // rope halves as a 2D tensor with box {32, box_rows} (kv_rope_map).  bf16
+    // panels use the 128-byte swizzle, bf16 rope halves the 64-byte one.
     CUtensorMap kv_map;
     CUtensorMap kv_pair_map[2];
-    CUtensorMap q_map;
+    CUtensorMap kv_rope_map;
     int box_rows;
     const __nv_bfloat16* q;  // [B, H, D]
     const uint8_t* kv;       // cache rows of D bf16 values

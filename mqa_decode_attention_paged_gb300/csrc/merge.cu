@@ -112,16 +112,18 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(const MergeArg
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         const float* base = a.ws_o + (static_cast<long long>(gf + b) * a.H + h) * R + 4 * c4;
         const long long step = static_cast<long long>(a.H) * R;
-        // eight partial rows in flight per thread; a segment with weight 0
-        // (empty, never written) contributes by selection, not by product
-        for (int i0 = 0; i0 < np; i0 += 8) {
-            float4 v[8];
+        // up to 24 partial rows in flight per thread (one round for most
+        // requests); a segment with weight 0 (empty, never written)
+        // contributes by selection, not by product
+        constexpr int kBatch = 24;
+        for (int i0 = 0; i0 < np; i0 += kBatch) {
+            float4 v[kBatch];
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
+            for (int k = 0; k < kBatch; ++k)
                 v[k] = i0 + k < np ? __ldcs(reinterpret_cast<const float4*>(base + (i0 + k) * step))
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < kBatch; ++k) {
                 const float w = i0 + k < np ? s_w[i0 + k] : 0.f;
                 if (w != 0.f) {
                     acc.x += w * v[k].x;

@@ -46,26 +46,25 @@ struct MlaTcCfg {
     static constexpr int kHeads = 128;
     static constexpr int kTile = 32;  // tokens per mask word half; a pair (pipeline stage) is two
     static constexpr int kPair = 2 * kTile;
-    static constexpr int kPanels = D / 64;
-    static constexpr int kLoPanels = R / 128;  // rank 0: QK panels = its P.V panels
-    static constexpr int kHiPanels = kPanels - kLoPanels;
-    static constexpr int kMaxPanels = kHiPanels;
-    static constexpr int kOCols = R / 2;  // O columns per CTA
-    static constexpr int kPVPanels = kOCols / 64;
-    static constexpr int kQPanelBytes = kHeads * 128;
-    static constexpr int kKvPanelBytes = kPair * 128;  // one panel of a 64-row slot
+    // Column split between the two ranks: rank r holds the 64-column kv_c
+    // panels [r * kFull, (r + 1) * kFull) (its V columns) and the 32-column
+    // half r of the 64-column rope part, so both ranks contract over the same
+    // number of columns and hold slots of the same size.
+    static constexpr int kFull = R / 128;  // full 64-column panels per rank
+    static constexpr int kOCols = R / 2;   // O columns per CTA
+    static constexpr int kPVPanels = kFull;
+    static constexpr int kRopeCols = (D - R) / 2;  // 32
+    static constexpr int kKvPanelBytes = kPair * 128;  // one full panel of a slot (128-byte rows, 128-byte swizzle)
+    static constexpr int kRopeBytes = kPair * 64;      // the slot's rope half (64-byte rows, 64-byte swizzle)
+    static constexpr int kSlotBytes = kFull * kKvPanelBytes + kRopeBytes;
+    static constexpr int kQRopeBytes = kHeads * 64;    // Q's rope half in shared memory (64-byte swizzle)
     // TMEM columns: O [0, 256), S [256, 320), P two buffers [320, 384), Q
-    // [384, 512) (up to 4 panels of 64 dims, two bf16 per column); a rank
-    // with more Q panels keeps the rest in shared memory
+    // [384, 384 + 32 * kFull) (the rank's kv_c panels as packed 16-bit pairs)
     static constexpr int kTmemCols = 512;
     static constexpr int kTmemS = 256;
     static constexpr int kTmemP = 320;
     static constexpr int kTmemQ = 384;
-    static constexpr int kTmemQPanels = 4;
-    static constexpr int kQSmemPanels = kMaxPanels > kTmemQPanels ? kMaxPanels - kTmemQPanels : 0;
-    static constexpr int kQBytes = kQSmemPanels * kQPanelBytes;
-    static constexpr int kSlotBytes = kMaxPanels * kKvPanelBytes;  // two stages
-    static constexpr int kXBytes = kHeads * kPair * 4;              // one fp32 logit pair
+    static constexpr int kXBytes = kHeads * kPair * 4;  // one fp32 logit pair
     static constexpr int kGroupWarps = 4;
     static constexpr int kGroupThreads = 32 * kGroupWarps;
     static constexpr int kSoftmaxWarps = 2 * kGroupWarps;
@@ -73,15 +72,15 @@ struct MlaTcCfg {
 
     static constexpr int kNumBars = 40;
     static constexpr int kRedBytes = 4 * kHeads * 4;  // running maxima [2][128], handed-over sums / maxima
-    // everything but the ring: alignment slack, Q panels, X, barriers,
+    // everything but the ring: alignment slack, Q rope half, X, barriers,
     // reductions, up to 8 stage masks, the TMEM address, lengths
     static constexpr int kFixedBytes =
-        1024 + kQBytes + 2 * kXBytes + kNumBars * 8 + kRedBytes + 8 * 8 + 16 + 4 * (2 * kMaxBatchTc + 1);
+        1024 + kQRopeBytes + 2 * kXBytes + kNumBars * 8 + kRedBytes + 8 * 8 + 16 + 4 * (2 * kMaxBatchTc + 1);
     static constexpr int kSlotsFit = (227 * 1024 - kFixedBytes) / kSlotBytes;
-    static constexpr int kSlots = kSlotsFit > 4 ? 4 : kSlotsFit;
+    static constexpr int kSlots = kSlotsFit > 6 ? 6 : kSlotsFit;
     static constexpr int kStages = kSlots;  // one pipeline stage per 64-token pair
     static constexpr int kOffQ = 0;
-    static constexpr int kOffStages = kOffQ + kQBytes;
+    static constexpr int kOffStages = kOffQ + kQRopeBytes;
     static constexpr int kOffX = kOffStages + kSlots * kSlotBytes;
     static constexpr int kOffBars = kOffX + 2 * kXBytes;
     static constexpr int kOffRed = kOffBars + kNumBars * 8;
@@ -90,23 +89,21 @@ struct MlaTcCfg {
     static constexpr int kOffCum = kOffTmem + 16;
     static size_t smem_bytes(int batch) { return 1024 + kOffCum + 4 * (2 * batch + 1); }
 
-    static_assert(kOCols <= 256 && kOCols % 64 == 0, "P.V width");
+    static_assert(kOCols <= 256 && kOCols % 64 == 0 && kRopeCols == 32, "column split");
     static_assert(kOCols <= kTmemS && kTmemS + kPair <= kTmemP && kTmemP + kPair <= kTmemQ &&
-                      kTmemQ + 32 * kTmemQPanels <= kTmemCols,
+                      kTmemQ + 32 * kFull <= kTmemCols,
                   "TMEM layout");
     static_assert(kSlots >= 2 && kStages <= 8, "pipeline depth");
-    static_assert(kSlots == kStages, "one ring slot per stage");
     static_assert(1024 + kOffCum + 4 * (2 * kMaxBatchTc + 1) <= 227 * 1024, "shared memory budget");
-    static_assert(kOffStages % 1024 == 0 && kSlotBytes % 1024 == 0, "swizzled operands need 1024-byte alignment");
+    static_assert(kOffStages % 1024 == 0 && kSlotBytes % 1024 == 0 && (kFull * kKvPanelBytes) % 512 == 0,
+                  "swizzled operands need 1024-byte (128-byte swizzle) / 512-byte (64-byte swizzle) alignment");
 };
 
 // barrier slots, each range starting where the previous one ends
 enum TcBar {
     kKvFull = 0,             // [8] pair landed (producer expect_tx + TMA bytes)
     kKvEmpty = kKvFull + 8,  // [8] P.V of the pair done (tensor-core commit)
-    kQFull = kKvEmpty + 8,   // Q panels kept in shared memory landed
-    kQEmpty = kQFull + 1,    // every Q.K^T of the piece done
-    kQTmem = kQEmpty + 1,    // a softmax group has written the piece's Q panels into TMEM
+    kQTmem = kKvEmpty + 8,   // a softmax group has written the piece's Q (TMEM panels, smem rope half)
     kSFull = kQTmem + 1,     // [2] logit pair of parity i in TMEM
     kSEmpty = kSFull + 2,    // the logit pair read out by its softmax group
     kPFull = kSEmpty + 1,    // [2] P of a pair in TMEM buffer (pair & 1), O rescaled if needed
@@ -116,29 +113,31 @@ enum TcBar {
     kMReady = kXFree + 2,    // [2] running maximum after a pair of parity i published
     kLReady = kMReady + 2,   // the group without the piece's last pair handed over its sum
     kOFree = kLReady + 1,    // the piece's output has been read out of TMEM
-    kConv = kOFree + 1,      // [2] fp8 cache: the pair of parity i was widened to f16 in its slot
-    kDrain = kConv + 2,      // every tensor-core operation of the CTA has completed
+    kConv = kOFree + 1,      // [4] fp8 cache: pair q (q % 4 = i) was widened to f16 in its slot
+    kDrain = kConv + 4,      // every tensor-core operation of the CTA has completed
     kBarCount = kDrain + 1,
 };
 static_assert(kBarCount <= MlaTcCfg<576, 512>::kNumBars && kBarCount <= MlaTcCfg<320, 256>::kNumBars,
               "barrier slots");
 
-// Q.K^T of one tile pair into TMEM columns d: NQT panels of Q from TMEM
-// (q_tmem), the rest from shared memory (qdesc); kdesc addresses panel 0 of
-// the pair's slot.  Descriptors advance by constant byte offsets >> 4 (the
-// start-address field cannot carry: shared addresses stay below 256 KB).
-template <int NP, int NQT, int KvPanelBytes, int QPanelBytes>
-__device__ __forceinline__ void issue_qk(uint32_t d, uint32_t q_tmem, uint64_t kdesc, uint64_t qdesc,
+// Q.K^T of one pair into TMEM columns d: NF full panels with Q from TMEM
+// (q_tmem) and K from the slot's 128-byte-swizzled panels (kdesc = panel 0),
+// then the 32-column rope half with Q from shared memory (qrope) and K from
+// the slot (krope), both 64-byte swizzled.  Descriptors advance by constant
+// byte offsets >> 4 (the start-address field cannot carry: shared addresses
+// stay below 256 KB).
+template <int NF, int KvPanelBytes>
+__device__ __forceinline__ void issue_qk(uint32_t d, uint32_t q_tmem, uint64_t kdesc, uint64_t qrope, uint64_t krope,
                                          uint32_t idesc) {
 #pragma unroll
-    for (int ks = 0; ks < NP * 4; ++ks) {
-        const uint64_t b = kdesc + static_cast<uint64_t>(((ks >> 2) * KvPanelBytes + (ks & 3) * 32) >> 4);
-        if (ks < NQT * 4)
-            umma_bf16_ta(d, q_tmem + ks * 8, b, idesc, ks > 0 ? 1u : 0u);
-        else
-            umma_bf16(d, qdesc + static_cast<uint64_t>((((ks >> 2) - NQT) * QPanelBytes + (ks & 3) * 32) >> 4), b,
-                      idesc, 1u);
-    }
+    for (int ks = 0; ks < NF * 4; ++ks)
+        umma_bf16_ta(d, q_tmem + ks * 8,
+                     kdesc + static_cast<uint64_t>(((ks >> 2) * KvPanelBytes + (ks & 3) * 32) >> 4), idesc,
+                     ks > 0 ? 1u : 0u);
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks)
+        umma_bf16(d, qrope + static_cast<uint64_t>((ks * 32) >> 4), krope + static_cast<uint64_t>((ks * 32) >> 4),
+                  idesc, 1u);
 }
 
 template <int D, int R, bool FP8>
@@ -160,9 +159,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
     const int unit = blockIdx.x >> 1;
-    const int pbase = rank ? C::kLoPanels : 0;          // first global column panel
-    const int np = rank ? C::kHiPanels : C::kLoPanels;  // panels loaded and contracted
-    const int nq_tmem = min(np, C::kTmemQPanels);        // Q panels held in TMEM, the rest in smem
+    const int pbase = rank * C::kFull;             // first global 64-column panel of the rank
+    const int rope0 = R + rank * C::kRopeCols;     // first column of the rank's rope half
     const int P = a.plan.page;
 
     if (threadIdx.x == 0) {
@@ -170,8 +168,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             mbar_init(&bars[kKvFull + s], 1);
             mbar_init(&bars[kKvEmpty + s], 1);
         }
-        mbar_init(&bars[kQFull], 1);
-        mbar_init(&bars[kQEmpty], 1);
         mbar_init(&bars[kQTmem], C::kGroupThreads);
         mbar_init(&bars[kSEmpty], C::kGroupThreads);
         for (int i = 0; i < 2; ++i) {
@@ -183,12 +179,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             mbar_init(&bars[kMReady + i], C::kGroupThreads);
         }
         mbar_init(&bars[kLReady], C::kGroupThreads);
-        for (int i = 0; i < 2; ++i) mbar_init(&bars[kConv + i], C::kGroupThreads);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[kConv + i], C::kGroupThreads);
         mbar_init(&bars[kOFree], C::kGroupThreads);
         mbar_init(&bars[kDrain], 2);  // one commit from each issuing thread
         fence_mbar_init();
         prefetch_tmap(&a.kv_map);
-        prefetch_tmap(&a.q_map);
+        prefetch_tmap(&a.kv_pair_map[0]);
+        prefetch_tmap(&a.kv_rope_map);
     }
     if (warp == 1) tmem_alloc(tmem_base_s, C::kTmemCols);
     pdl_wait();
@@ -209,11 +206,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
     };
     // byte offset of pair p's slot in the ring
     auto slot_base = [&](int p) { return (p % C::kStages) * C::kSlotBytes; };
-    // fp8 cache: the pair's e4m3 panels (64 rows x 64 bytes each, unswizzled)
-    // land at the end of the slot and are widened in place to f16 panels
+    // fp8 cache: the pair's e4m3 full panels (64 rows x 64 bytes each) and
+    // rope half (64 rows x 32 bytes), unswizzled, land at the end of the slot
+    // and are widened in place to f16 in the operand layouts
     constexpr int kF8PanelBytes = C::kPair * 64;
-    const int f8_off = FP8 ? C::kSlotBytes - np * kF8PanelBytes : 0;
-    constexpr int kRowBytes = FP8 ? 64 : 128;  // bytes per cache row and panel as copied
+    constexpr int kF8RopeBytes = C::kPair * 32;
+    constexpr int kF8Bytes = C::kFull * kF8PanelBytes + kF8RopeBytes;
+    constexpr int f8_off = FP8 ? C::kSlotBytes - kF8Bytes : 0;
+    constexpr int kRowBytes = FP8 ? 64 : 128;      // bytes per cache row and full panel as copied
+    constexpr int kRopeRowBytes = FP8 ? 32 : 64;   // bytes per cache row of the rope half as copied
+    // as-copied offsets within the slot of the full panels and of the rope half
+    constexpr int kCopyPanelBytes = C::kPair * kRowBytes;
+    constexpr int kCopyRopeOff = f8_off + C::kFull * kCopyPanelBytes;
 
     if (warp == 0) {
         // ------------------------------------------------------ KV producer
@@ -224,7 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         // when pages hold whole pairs, else one 2D copy per page and panel.
         const uint64_t pol = l2_policy_evict_first();
         const int BR = a.box_rows, nbox = C::kPair / BR;  // boxes per pair (1, 2 or 4)
-        const CUtensorMap* pair_map = &a.kv_pair_map[rank];
+        const CUtensorMap* pair_map = &a.kv_pair_map[0];
         PieceIter it;
         it.init(a.plan, cum, T, unit);
         Piece pc;
@@ -288,19 +292,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                             vmask &= ~(ones << (k * BR));
                     }
                     mask_s[st] = vmask;
-                    mbar_arrive_expect_tx(&bars[kKvFull + st], nvalid * BR * kRowBytes * np);
+                    mbar_arrive_expect_tx(&bars[kKvFull + st],
+                                          nvalid * BR * (C::kFull * kRowBytes + kRopeRowBytes));
                     uint8_t* dst = stages + slot_base(p) + f8_off;
+                    uint8_t* rope_dst = stages + slot_base(p) + kCopyRopeOff;
                     if (BR == C::kPair) {
-                        if (val[0])
-                            tma_load_3d(dst, pair_map, 0, blk[0] * P + t0 % P, pbase, &bars[kKvFull + st], pol);
+                        if (val[0]) {
+                            const int row = blk[0] * P + t0 % P;
+                            tma_load_3d(dst, pair_map, 0, row, pbase, &bars[kKvFull + st], pol);
+                            tma_load_2d(rope_dst, &a.kv_rope_map, rope0, row, &bars[kKvFull + st], pol);
+                        }
                     } else {
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             if (k >= nbox || !val[k]) continue;
                             const int row = blk[k] * P + (t0 + k * BR) % P;
-                            for (int pn = 0; pn < np; ++pn)
-                                tma_load_2d(dst + pn * (C::kPair * kRowBytes) + k * BR * kRowBytes, &a.kv_map,
+                            for (int pn = 0; pn < C::kFull; ++pn)
+                                tma_load_2d(dst + pn * kCopyPanelBytes + k * BR * kRowBytes, &a.kv_map,
                                             (pbase + pn) * 64, row, &bars[kKvFull + st], pol);
+                            tma_load_2d(rope_dst + k * BR * kRopeRowBytes, &a.kv_rope_map, rope0, row,
+                                        &bars[kKvFull + st], pol);
                         }
                     }
                 }
@@ -313,92 +324,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 if (!mbar_wait(&bars[kKvFull + q % C::kStages], (q / C::kStages) & 1))
                     report(a.status, MQA_ERR_DEVICE_TIMEOUT);
     } else if (warp == 2 + C::kSoftmaxWarps) {
-        // ------------------------------------------------------ P.V issuer and Q loader
-        // One thread issues O += P V per pair as soon as its P is in TMEM
-        // (and, for a piece's first pair, the previous output was read out),
-        // and loads the Q panel kept in shared memory when its buffer frees.
+        // ------------------------------------------------------ P.V issuer
+        // One thread issues O += P V per pair, in pair order, as soon as its P
+        // is in TMEM (and, for a piece's first pair, the previous piece's
+        // output has been read out of O).
         if (lane == 0) {
             constexpr uint32_t kIdPV = FP8 ? umma_idesc_f16(128, C::kOCols, 1) : umma_idesc_bf16(128, C::kOCols, 1);
             const uint64_t vdesc0 = umma_desc(smem_u32(stages), C::kKvPanelBytes, 1024);
-            const uint64_t pol = l2_policy_evict_last();
-            PieceIter vi, qi;
+            PieceIter vi;
             vi.init(a.plan, cum, T, unit);
-            qi.init(a.plan, cum, T, unit);
-            Piece vpc, qpc;
-            int vp = 0, vj = 0, vnp = 0, vc = 0;  // next P.V: pair vp, pair vj of piece vc (vnp pairs)
-            int qc = 0;                           // Q panel loads issued
-            auto next_piece = [&](PieceIter& pi, Piece& pc, int& npairs) {
-                int tok0, tok_end;
-                while (pi.next(cum, pc)) {
-                    npairs = piece_tiles(pc, tok0, tok_end) >> 1;
-                    if (npairs > 0) return true;
-                }
-                return false;
-            };
-            bool v_have = next_piece(vi, vpc, vnp);
-            int qnp = 0;
-            // (the fp8 kernel's softmax rows write that panel themselves, in f16)
-            bool q_have = !FP8 && np > nq_tmem && next_piece(qi, qpc, qnp);
+            Piece vpc;
+            int vp = 0, vc = 0;  // next pair, pieces with tokens begun
             bool ok = true;
-            unsigned long long idle_since = 0;
-            while (v_have || q_have) {
-                bool progressed = false;
-                const int pb = vp & 1;
-                if (v_have && mbar_test(&bars[kPFull + pb], (vp >> 1) & 1) &&
-                    (vj > 0 || vc == 0 || mbar_test(&bars[kOFree], (vc - 1) & 1))) {
+            while (ok && vi.next(cum, vpc)) {
+                int tok0, tok_end;
+                const int npairs = piece_tiles(vpc, tok0, tok_end) >> 1;
+                if (npairs == 0) continue;
+                for (int j = 0; j < npairs; ++j, ++vp) {
+                    const int pb = vp & 1;
+                    if (!mbar_wait(&bars[kPFull + pb], (vp >> 1) & 1) ||
+                        (j == 0 && vc > 0 && !mbar_wait(&bars[kOFree], (vc - 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     const uint64_t vd = vdesc0 + static_cast<uint64_t>(slot_base(vp) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < C::kPair / 16; ++ks)
                         umma_bf16_ta(tbase, tbase + C::kTmemP + pb * (C::kPair / 2) + ks * 8,
                                      vd + static_cast<uint64_t>((ks * 16 * 128) >> 4), kIdPV,
-                                     (vj == 0 && ks == 0) ? 0u : 1u);
+                                     (j == 0 && ks == 0) ? 0u : 1u);
                     umma_commit(&bars[kPEmpty + pb]);
                     umma_commit(&bars[kKvEmpty + vp % C::kStages]);
-                    ++vp;
-                    if (++vj >= vnp) {
-                        vj = 0;
-                        ++vc;
-                        v_have = next_piece(vi, vpc, vnp);
-                    }
-                    progressed = true;
                 }
-                if (q_have && mbar_test(&bars[kQEmpty], (qc & 1) ^ 1)) {
-                    mbar_arrive_expect_tx(&bars[kQFull], (np - nq_tmem) * C::kQPanelBytes);
-                    for (int pn = nq_tmem; pn < np; ++pn)
-                        tma_load_2d(q_s + (pn - nq_tmem) * C::kQPanelBytes, &a.q_map, (pbase + pn) * 64,
-                                    qpc.b * a.H, &bars[kQFull], pol);
-                    ++qc;
-                    q_have = next_piece(qi, qpc, qnp);
-                    progressed = true;
-                }
-                if (progressed) {
-                    idle_since = 0;
-                } else {
-                    const unsigned long long now = global_timer_ns();
-                    if (idle_since == 0) {
-                        idle_since = now;
-                    } else if (now - idle_since > kWaitLimitNs) {
-                        ok = false;
-                        break;
-                    }
-                }
+                ++vc;
             }
             if (!ok) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
-            if (qc > 0 && !mbar_wait(&bars[kQFull], (qc - 1) & 1)) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
             // no tensor-core work of this thread may be in flight at teardown
             umma_commit(&bars[kDrain]);
             if (!mbar_wait(&bars[kDrain], 0)) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ Q.K^T issuer
-        // One thread issues S = Q K^T per pair, in pair order, once Q is in
-        // TMEM (and the shared-memory panel, if any), the previous pair's
-        // logits were read out and the pair's rows landed.
+        // One thread issues S = Q K^T per pair, in pair order, once the
+        // piece's Q is in TMEM and shared memory, the previous pair's logits
+        // were read out and the pair's rows landed (fp8: and were widened).
         if (lane == 0) {
             constexpr uint32_t kIdQK = FP8 ? umma_idesc_f16(128, C::kPair, 0) : umma_idesc_bf16(128, C::kPair, 0);
             const uint64_t kdesc0 = umma_desc(smem_u32(stages), 16, 1024);
-            const uint64_t qdesc = umma_desc(smem_u32(q_s), 16, 1024);
+            const uint64_t krope0 = umma_desc_sw64(smem_u32(stages) + C::kFull * C::kKvPanelBytes);
+            const uint64_t qrope = umma_desc_sw64(smem_u32(q_s));
             PieceIter qi;
             qi.init(a.plan, cum, T, unit);
             Piece qpc;
@@ -408,15 +383,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 int tok0, tok_end;
                 const int npairs = piece_tiles(qpc, tok0, tok_end) >> 1;
                 if (npairs == 0) continue;
-                if (!mbar_wait(&bars[kQTmem], qc & 1) ||
-                    (!FP8 && np > nq_tmem && !mbar_wait(&bars[kQFull], qc & 1))) {
+                if (!mbar_wait(&bars[kQTmem], qc & 1)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int j = 0; j < npairs; ++j, ++qp) {
                     // bf16: the pair's rows landed; fp8: they were also widened to f16
-                    const bool ready = FP8 ? mbar_wait(&bars[kConv + (qp & 1)], (qp >> 1) & 1)
+                    const bool ready = FP8 ? mbar_wait(&bars[kConv + (qp & 3)], (qp >> 2) & 1)
                                            : mbar_wait(&bars[kKvFull + qp % C::kStages], (qp / C::kStages) & 1);
                     if (!mbar_wait(&bars[kSEmpty], (qp & 1) ^ 1) || !ready) {
                         ok = false;
@@ -424,16 +398,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                     }
                     tc_fence_after();
                     const uint32_t d = tbase + C::kTmemS;
-                    const uint64_t kd = kdesc0 + static_cast<uint64_t>(slot_base(qp) >> 4);
-                    if (rank)
-                        issue_qk<C::kHiPanels, (C::kHiPanels < 4 ? C::kHiPanels : 4), C::kKvPanelBytes,
-                                 C::kQPanelBytes>(d, tbase + C::kTmemQ, kd, qdesc, kIdQK);
-                    else
-                        issue_qk<C::kLoPanels, (C::kLoPanels < 4 ? C::kLoPanels : 4), C::kKvPanelBytes,
-                                 C::kQPanelBytes>(d, tbase + C::kTmemQ, kd, qdesc, kIdQK);
+                    const uint64_t sb = static_cast<uint64_t>(slot_base(qp) >> 4);
+                    issue_qk<C::kFull, C::kKvPanelBytes>(d, tbase + C::kTmemQ, kdesc0 + sb, qrope, krope0 + sb, kIdQK);
                     umma_commit(&bars[kSFull + (qp & 1)]);
                 }
-                umma_commit(&bars[kQEmpty]);  // Q may be replaced once these finish
                 ++qc;
             }
             if (!ok) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
@@ -473,9 +441,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             int tok0, tok_end;
             while (from.next(cum, nx)) {
                 if (piece_tiles(nx, tok0, tok_end) == 0) continue;
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    a.q + (static_cast<long long>(nx.b) * a.H + (live_row ? h : 0)) * D + pbase * 64);
-                for (int c = 0; c < 4 * nq_tmem; ++c) {  // 8 columns (16 dims) at a time
+                const __nv_bfloat16* qrow = a.q + (static_cast<long long>(nx.b) * a.H + (live_row ? h : 0)) * D;
+                const uint4* src = reinterpret_cast<const uint4*>(qrow + pbase * 64);
+                for (int c = 0; c < 4 * C::kFull; ++c) {  // 8 columns (16 dims) at a time
                     const uint4 v0 = live_row ? __ldg(src + 2 * c) : make_uint4(0, 0, 0, 0);
                     const uint4 v1 = live_row ? __ldg(src + 2 * c + 1) : make_uint4(0, 0, 0, 0);
                     uint32_t r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -485,17 +453,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                     }
                     tmem_st8(lane_addr + C::kTmemQ + c * 8, r);
                 }
-                if constexpr (FP8) {
-                    // panels past the TMEM ones, f16, as the K-major swizzled smem operand
-                    for (int pn = nq_tmem; pn < np; ++pn) {
-                        uint8_t* row = q_s + (pn - nq_tmem) * C::kQPanelBytes + h * 128;
+                {
+                    // the rank's rope half (32 dims = 64 bytes), the K-major
+                    // operand in shared memory with the 64-byte swizzle
+                    const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + rope0);
+                    uint8_t* row = q_s + h * 64;
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            uint4 v = live_row ? __ldg(src + pn * 8 + c) : make_uint4(0, 0, 0, 0);
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 v = live_row ? __ldg(rsrc + c) : make_uint4(0, 0, 0, 0);
+                        if constexpr (FP8)
                             v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
                                            bf16x2_to_f16x2(v.w));
-                            *reinterpret_cast<uint4*>(row + ((c ^ (h & 7)) << 4)) = v;
-                        }
+                        *reinterpret_cast<uint4*>(row + ((c ^ ((h >> 1) & 3)) << 4)) = v;
                     }
                     fence_proxy_async_smem();
                 }
@@ -511,6 +480,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         // wait targets the phase after the last one it saw complete.
         auto wait_own_pv = [&](int p2) { return wait_all(&bars[kPEmpty + g], (p2 >> 1) & 1, false); };
 
+        // fp8 cache: widen pair q's e4m3 panels to f16 in place, then let
+        // Q.K^T(q) go.  The group that owns pair q - 1 widens q (group 0 also
+        // widens pair 0), one step ahead of its Q.K^T.  Pair q arrives on
+        // barrier q % 4: a group starts the step that widens q + 4 only after
+        // Q.K^T(q + 1) could run, i.e. after every thread that widened q did,
+        // so one barrier's phases never overlap.
+        auto widen = [&](int q) -> bool {
+            // ---- widen the pair's e4m3 panels to f16 in place: thread t
+            // takes row t / 2, bytes 32 (t % 2) .. + 31 of each full
+            // panel, then bytes 16 (t % 2) .. + 15 of the rope half; all
+            // reads of a panel precede its writes (the f16 panel overlaps
+            // its own e4m3 source and earlier ones, never a later one)
+            if (!wait_all(&bars[kKvFull + q % C::kStages], (q / C::kStages) & 1, false)) return false;
+            const int t = quad * 32 + lane, r = t >> 1, hb = t & 1;
+            uint8_t* slot = stages + slot_base(q);
+            for (int pn = 0; pn < C::kFull; ++pn) {
+                const uint8_t* srcp = slot + f8_off + pn * kF8PanelBytes + r * 64 + hb * 32;
+                const uint4 w0 = *reinterpret_cast<const uint4*>(srcp);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(srcp + 16);
+                named_bar_sync(1 + g, C::kGroupThreads);
+                const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                uint8_t* dstp = slot + pn * C::kKvPanelBytes + r * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[4];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        o[2 * i] = e4m3x2_to_f16x2(w[2 * c + i] & 0xffffu);
+                        o[2 * i + 1] = e4m3x2_to_f16x2(w[2 * c + i] >> 16);
+                    }
+                    *reinterpret_cast<uint4*>(dstp + (((hb * 4 + c) ^ (r & 7)) << 4)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            {
+                const uint4 w0 = *reinterpret_cast<const uint4*>(slot + f8_off + C::kFull * kF8PanelBytes +
+                                                                  r * 32 + hb * 16);
+                named_bar_sync(1 + g, C::kGroupThreads);
+                const uint32_t w[4] = {w0.x, w0.y, w0.z, w0.w};
+                uint8_t* dstp = slot + C::kFull * C::kKvPanelBytes + r * 64;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t o[4];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        o[2 * i] = e4m3x2_to_f16x2(w[2 * c + i] & 0xffffu);
+                        o[2 * i + 1] = e4m3x2_to_f16x2(w[2 * c + i] >> 16);
+                    }
+                    *reinterpret_cast<uint4*>(dstp + (((hb * 2 + c) ^ ((r >> 1) & 3)) << 4)) =
+                        make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[kConv + (q & 3)]);
+            return true;
+        };
+        // pairs of the whole unit (for the look-ahead widening)
+        int total_pairs = 0;
+        {
+            PieceIter ti;
+            ti.init(a.plan, cum, T, unit);
+            Piece tp;
+            int t0_, te_;
+            while (ti.next(cum, tp)) total_pairs += piece_tiles(tp, t0_, te_) >> 1;
+        }
+
         PieceIter it;
         it.init(a.plan, cum, T, unit);
         Piece pc;
@@ -518,6 +553,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         int kpiece = 0;  // pieces with tokens so far
         bool ok = true;
         if (g == 0) stage_q(it);
+        if (FP8 && g == 0 && total_pairs > 0 && !widen(0)) ok = false;
         while (ok && it.next(cum, pc)) {
             int tok0, tok_end;
             const int nt = piece_tiles(pc, tok0, tok_end);
@@ -534,38 +570,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             float l_part = 0.f, m_l = -INFINITY;
             for (int j = ((gp & 1) == g) ? 0 : 1; j < npairs; j += 2) {
                 const int p = gp + j, pb = p & 1;
-                if constexpr (FP8) {
-                    // ---- widen the pair's e4m3 panels to f16 in place: thread t
-                    // takes row t / 2, bytes 32 (t % 2) .. + 31 of each panel; all
-                    // reads of a panel precede its writes (the f16 panel overlaps
-                    // its own e4m3 source, never a later panel's)
-                    if (!wait_all(&bars[kKvFull + p % C::kStages], (p / C::kStages) & 1, false)) {
-                        ok = false;
-                        break;
-                    }
-                    const int t = quad * 32 + lane, r = t >> 1, hb = t & 1;
-                    uint8_t* slot = stages + slot_base(p);
-                    for (int pn = 0; pn < np; ++pn) {
-                        const uint8_t* srcp = slot + f8_off + pn * kF8PanelBytes + r * 64 + hb * 32;
-                        const uint4 w0 = *reinterpret_cast<const uint4*>(srcp);
-                        const uint4 w1 = *reinterpret_cast<const uint4*>(srcp + 16);
-                        named_bar_sync(1 + g, C::kGroupThreads);
-                        const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                        uint8_t* dstp = slot + pn * C::kKvPanelBytes + r * 128;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t o[4];
-#pragma unroll
-                            for (int i = 0; i < 2; ++i) {
-                                o[2 * i] = e4m3x2_to_f16x2(w[2 * c + i] & 0xffffu);
-                                o[2 * i + 1] = e4m3x2_to_f16x2(w[2 * c + i] >> 16);
-                            }
-                            *reinterpret_cast<uint4*>(dstp + (((hb * 4 + c) ^ (r & 7)) << 4)) =
-                                make_uint4(o[0], o[1], o[2], o[3]);
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    mbar_arrive(&bars[kConv + pb]);
+                if (FP8 && p + 1 < total_pairs && !widen(p + 1)) {
+                    ok = false;
+                    break;
                 }
                 // ---- logits of the pair: own partial from TMEM
                 float s[C::kPair];
@@ -597,7 +604,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 for (int c = 0; c < C::kPair / 4; ++c)
                     st_async_v4(x_remote + c * 512, s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3], xfull_remote);
                 // valid tokens of the pair (set by the producer before kv_full)
-                if (!FP8 && !wait_all(&bars[kKvFull + p % C::kStages], (p / C::kStages) & 1, false)) {
+                if (!wait_all(&bars[kKvFull + p % C::kStages], (p / C::kStages) & 1, false)) {
                     ok = false;
                     break;
                 }

@@ -45,6 +45,19 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
     return d;
 }
 
+// K-major operand with 64-byte rows and the 64-byte swizzle (mode 4): 16-byte
+// chunk c of row r sits at r * 64 + ((c ^ ((r / 2) % 4)) * 16); eight-row
+// groups are 512 bytes apart.  K steps of 16 elements advance by 32 bytes.
+__device__ __forceinline__ uint64_t umma_desc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(512 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(4) << 61;
+    return d;
+}
+
 // ---- instruction descriptor for kind::f16 with bf16 A/B and fp32 D:
 // bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
 // 15 / 16 A / B major-ness (0 = K-major, 1 = MN-major), 17-22 N >> 3,
