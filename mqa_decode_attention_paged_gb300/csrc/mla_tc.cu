@@ -221,13 +221,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
 
     if (warp == 0) {
         // ------------------------------------------------------ KV producer
-        // The whole warp walks the pairs: lane l holds the block id of page
-        // l of the piece's current 32-page chunk (the next chunk is loaded
-        // one chunk ahead, so table reads stay off the issue path); lane 0
-        // waits for ring slots and issues the copies: one 3D copy per pair
-        // when pages hold whole pairs, else one 2D copy per page and panel.
+        // The whole warp walks the pairs.  Lane l holds the block id of page l
+        // of the piece's current 32-page chunk (the next chunk is loaded one
+        // chunk ahead, so table reads stay off the issue path); lane k < nbox
+        // takes box k of the pair (BR tokens of one page).  Everything for a
+        // pair is worked out before its ring slot frees; then lane 0 stores
+        // the token mask and arms kv_full, and the lanes issue the copies:
+        // one 3D copy of the pair's panels (lane 0) and one of its rope half
+        // (lane 1) when pages hold whole pairs, else one 2D copy per panel
+        // and one for the rope half per box (lane k).
         const uint64_t pol = l2_policy_evict_first();
         const int BR = a.box_rows, nbox = C::kPair / BR;  // boxes per pair (1, 2 or 4)
+        const uint32_t box_bytes = BR * (C::kFull * kRowBytes + kRopeRowBytes);
+        const uint64_t box_ones = BR == 64 ? ~0ull : ((1ull << BR) - 1);
         const CUtensorMap* pair_map = &a.kv_pair_map[0];
         PieceIter it;
         it.init(a.plan, cum, T, unit);
@@ -249,71 +255,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             int blk_nxt = load_chunk(1);
             for (int jp = 0; jp < npairs; ++jp, ++p) {
                 const int t0 = tok0 + jp * C::kPair;
-                int blk[4];
-                bool val[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int tok = t0 + k * BR;
-                    val[k] = k < nbox && tok < tok_end;
-                    blk[k] = 0;
-                    if (val[k]) {  // warp-uniform
-                        const int rel = tok / P - pc.j0;  // page within the piece
-                        if ((rel >> 5) != chunk) {        // pairs advance by at most four pages
-                            blk_cur = blk_nxt;
-                            chunk = rel >> 5;
-                            blk_nxt = load_chunk(chunk + 1);
-                        }
-                        blk[k] = __shfl_sync(0xffffffffu, blk_cur, rel & 31);
-                    }
+                // box `lane` of the pair (pages of one pair span at most one
+                // chunk boundary: boxes before it read blk_cur, after it blk_nxt)
+                const int tok = t0 + lane * BR;
+                const bool inbox = lane < nbox && tok < tok_end;
+                const int rel = inbox ? tok / P - pc.j0 : 0;  // page within the piece
+                const int bc = __shfl_sync(0xffffffffu, blk_cur, rel & 31);
+                const int bn = __shfl_sync(0xffffffffu, blk_nxt, rel & 31);
+                const int blk = (rel >> 5) == chunk ? bc : bn;
+                bool v = inbox;
+                if (v && (blk < 0 || blk >= a.num_blocks)) {
+                    report(a.status, MQA_ERR_DEVICE_CHECK);
+                    v = false;
                 }
+                const int last_rel = __reduce_max_sync(0xffffffffu, rel);
+                if ((last_rel >> 5) != chunk) {  // the pair reached the next chunk
+                    blk_cur = blk_nxt;
+                    ++chunk;
+                    blk_nxt = load_chunk(chunk + 1);
+                }
+                const unsigned vball = __ballot_sync(0xffffffffu, v);
+                const int n_tok = max(tok_end - t0, 0);
+                uint64_t vmask = n_tok >= C::kPair ? ~0ull : ((1ull << n_tok) - 1);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (k < nbox && !((vball >> k) & 1u)) vmask &= ~(box_ones << (k * BR));
+                const int row = v ? blk * P + tok % P : 0;
                 const int st = p % C::kStages;
-                bool got = true;
-                if (lane == 0) got = mbar_wait(&bars[kKvEmpty + st], ((p / C::kStages) & 1) ^ 1);
-                if (!__shfl_sync(0xffffffffu, got, 0)) {
+                uint8_t* dst = stages + slot_base(p) + f8_off;
+                uint8_t* rope_dst = stages + slot_base(p) + kCopyRopeOff;
+                // every issuing lane observes the slot free (P.V of its last pair done)
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars[kKvEmpty + st], ((p / C::kStages) & 1) ^ 1))) {
                     if (lane == 0) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
-                    const int n_tok = max(tok_end - t0, 0);
-                    uint64_t vmask = n_tok >= C::kPair ? ~0ull : ((1ull << n_tok) - 1);
-                    const uint64_t ones = BR == 64 ? ~0ull : ((1ull << BR) - 1);
-                    int nvalid = 0;
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        if (k >= nbox) break;
-                        if (val[k] && (blk[k] < 0 || blk[k] >= a.num_blocks)) {
-                            report(a.status, MQA_ERR_DEVICE_CHECK);
-                            val[k] = false;
-                        }
-                        if (val[k])
-                            ++nvalid;
-                        else
-                            vmask &= ~(ones << (k * BR));
-                    }
                     mask_s[st] = vmask;
-                    mbar_arrive_expect_tx(&bars[kKvFull + st],
-                                          nvalid * BR * (C::kFull * kRowBytes + kRopeRowBytes));
-                    uint8_t* dst = stages + slot_base(p) + f8_off;
-                    uint8_t* rope_dst = stages + slot_base(p) + kCopyRopeOff;
-                    if (BR == C::kPair) {
-                        if (val[0]) {
-                            const int row = blk[0] * P + t0 % P;
-                            tma_load_3d(dst, pair_map, 0, row, pbase, &bars[kKvFull + st], pol);
-                            tma_load_2d(rope_dst, &a.kv_rope_map, rope0, row, &bars[kKvFull + st], pol);
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            if (k >= nbox || !val[k]) continue;
-                            const int row = blk[k] * P + (t0 + k * BR) % P;
-                            for (int pn = 0; pn < C::kFull; ++pn)
-                                tma_load_2d(dst + pn * kCopyPanelBytes + k * BR * kRowBytes, &a.kv_map,
-                                            (pbase + pn) * 64, row, &bars[kKvFull + st], pol);
-                            tma_load_2d(rope_dst + k * BR * kRopeRowBytes, &a.kv_rope_map, rope0, row,
-                                        &bars[kKvFull + st], pol);
-                        }
+                    mbar_arrive_expect_tx(&bars[kKvFull + st], __popc(vball) * box_bytes);
+                }
+                if (BR == C::kPair) {
+                    const int row0 = __shfl_sync(0xffffffffu, row, 0);
+                    if (vball & 1u) {
+                        if (lane == 0) tma_load_3d(dst, pair_map, 0, row0, pbase, &bars[kKvFull + st], pol);
+                        if (lane == 1) tma_load_2d(rope_dst, &a.kv_rope_map, rope0, row0, &bars[kKvFull + st], pol);
                     }
+                } else if (v) {
+                    for (int pn = 0; pn < C::kFull; ++pn)
+                        tma_load_2d(dst + pn * kCopyPanelBytes + lane * BR * kRowBytes, &a.kv_map, (pbase + pn) * 64,
+                                    row, &bars[kKvFull + st], pol);
+                    tma_load_2d(rope_dst + lane * BR * kRopeRowBytes, &a.kv_rope_map, rope0, row, &bars[kKvFull + st],
+                                pol);
                 }
                 __syncwarp();
             }
