@@ -234,6 +234,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         const int BR = a.box_rows, nbox = C::kPair / BR;  // boxes per pair (1, 2 or 4)
         const uint32_t box_bytes = BR * (C::kFull * kRowBytes + kRopeRowBytes);
         const uint64_t box_ones = BR == 64 ? ~0ull : ((1ull << BR) - 1);
+        // boxes are whole pages (16- or 32-token pages) or pairs are whole
+        // page parts (pages of a multiple of 64 tokens): pages are tracked
+        // without division; other page sizes divide
+        const bool pages_fit = BR == P || BR == C::kPair;
         const CUtensorMap* pair_map = &a.kv_pair_map[0];
         PieceIter it;
         it.init(a.plan, cum, T, unit);
@@ -253,13 +257,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             int chunk = 0;
             int blk_cur = load_chunk(0);
             int blk_nxt = load_chunk(1);
+            // page (within the piece) and row offset in it of the pair's first
+            // token, advanced without division: pages of less than 64 tokens
+            // hold whole boxes (BR = P), larger pages hold whole pairs
+            int pg0 = 0, off0 = 0;
             for (int jp = 0; jp < npairs; ++jp, ++p) {
                 const int t0 = tok0 + jp * C::kPair;
                 // box `lane` of the pair (pages of one pair span at most one
                 // chunk boundary: boxes before it read blk_cur, after it blk_nxt)
                 const int tok = t0 + lane * BR;
                 const bool inbox = lane < nbox && tok < tok_end;
-                const int rel = inbox ? tok / P - pc.j0 : 0;  // page within the piece
+                const int rel = !inbox ? 0 : pages_fit ? pg0 + (BR == P ? lane : 0) : tok / P - pc.j0;
                 const int bc = __shfl_sync(0xffffffffu, blk_cur, rel & 31);
                 const int bn = __shfl_sync(0xffffffffu, blk_nxt, rel & 31);
                 const int blk = (rel >> 5) == chunk ? bc : bn;
@@ -280,7 +288,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     if (k < nbox && !((vball >> k) & 1u)) vmask &= ~(box_ones << (k * BR));
-                const int row = v ? blk * P + tok % P : 0;
+                const int row = !v ? 0 : blk * P + (pages_fit ? off0 : tok % P);
+                if (BR == P) {
+                    pg0 += nbox;
+                } else if ((off0 += C::kPair) == P) {
+                    off0 = 0;
+                    ++pg0;
+                }
                 const int st = p % C::kStages;
                 uint8_t* dst = stages + slot_base(p) + f8_off;
                 uint8_t* rope_dst = stages + slot_base(p) + kCopyRopeOff;

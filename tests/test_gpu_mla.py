@@ -54,6 +54,19 @@ def test_tensor_core_path_ragged(D, page, splits):
     assert_close(out, lse, ref_out, ref_lse, what=f"tc D={D} P={page} S={splits}")
 
 
+@pytest.mark.parametrize("page", [32, 48, 128])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_tensor_core_path_other_page_sizes(page, kv_dtype):
+    # Pages of 32 tokens (one box each), 48 (boxes straddle no page, pairs do)
+    # and 128 (two pairs per page) on the tensor-core clusters.
+    case = synth.poison(synth.make_mla_case(RAGGED + [300, 1000], H=128, D=576, page=page, kv_dtype=kv_dtype,
+                                            k_scale=0.05, pool_factor=1.2, seed=19, extra_cols=1))
+    for splits in (1, 3):
+        out, lse = run_gpu(case, splits)
+        ref_out, ref_lse = run_oracle(case)
+        assert_close(out, lse, ref_out, ref_lse, fp8=kv_dtype != "bf16", what=f"tc P={page} {kv_dtype} S={splits}")
+
+
 @pytest.mark.parametrize("D", [576, 320])
 @pytest.mark.parametrize("page", [16, 64])
 @pytest.mark.parametrize("splits", [1, 4])
