@@ -298,6 +298,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 const int st = p % C::kStages;
                 uint8_t* dst = stages + slot_base(p) + f8_off;
                 uint8_t* rope_dst = stages + slot_base(p) + kCopyRopeOff;
+                // while the slot is still busy, pull the box's whole cache rows
+                // (both ranks' columns) towards L2 so the copies below hit it
+                if (rank == 0 && v)
+                    bulk_prefetch_l2(a.kv + static_cast<long long>(row) * (D * (FP8 ? 1 : 2)),
+                                     static_cast<uint32_t>(BR * D * (FP8 ? 1 : 2)));
                 // every issuing lane observes the slot free (P.V of its last pair done)
                 if (!__all_sync(0xffffffffu, mbar_wait(&bars[kKvEmpty + st], ((p / C::kStages) & 1) ^ 1))) {
                     if (lane == 0) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
