@@ -248,6 +248,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             int tok0, tok_end;
             const int npairs = piece_tiles(pc, tok0, tok_end) >> 1;
             if (npairs == 0) continue;
+            // the piece's query rows (this rank's half of the heads) towards
+            // L2: a softmax group loads them into TMEM once the pairs before
+            // the piece have been read out, several pairs from now
+            if (lane == 0) {
+                const int hh = (a.H + 1) >> 1, h0 = rank * hh, nh = min(a.H, h0 + hh) - h0;
+                if (nh > 0)
+                    bulk_prefetch_l2(a.q + (static_cast<long long>(pc.b) * a.H + h0) * D,
+                                     static_cast<uint32_t>(nh * D * 2));
+            }
             const int32_t* bt = a.block_table + static_cast<long long>(pc.b) * a.plan.max_blocks + pc.j0;
             const int npg = pc.j1 - pc.j0;
             auto load_chunk = [&](int c) {
@@ -454,15 +463,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 if (piece_tiles(nx, tok0, tok_end) == 0) continue;
                 const __nv_bfloat16* qrow = a.q + (static_cast<long long>(nx.b) * a.H + (live_row ? h : 0)) * D;
                 const uint4* src = reinterpret_cast<const uint4*>(qrow + pbase * 64);
-                for (int c = 0; c < 4 * C::kFull; ++c) {  // 8 columns (16 dims) at a time
-                    const uint4 v0 = live_row ? __ldg(src + 2 * c) : make_uint4(0, 0, 0, 0);
-                    const uint4 v1 = live_row ? __ldg(src + 2 * c + 1) : make_uint4(0, 0, 0, 0);
-                    uint32_t r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                    if constexpr (FP8) {
+                // 8 columns (16 dims) per TMEM store
+                if constexpr (FP8) {
+                    for (int c = 0; c < 4 * C::kFull; ++c) {
+                        const uint4 v0 = live_row ? __ldg(src + 2 * c) : make_uint4(0, 0, 0, 0);
+                        const uint4 v1 = live_row ? __ldg(src + 2 * c + 1) : make_uint4(0, 0, 0, 0);
+                        uint32_t r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
                         for (int i = 0; i < 8; ++i) r[i] = bf16x2_to_f16x2(r[i]);
+                        tmem_st8(lane_addr + C::kTmemQ + c * 8, r);
                     }
-                    tmem_st8(lane_addr + C::kTmemQ + c * 8, r);
+                } else {
+                    // the loads of four stores are issued before any of them
+                    // (a TMEM store orders memory); the e4m3 kernel above keeps
+                    // one store's loads at a time, which times faster there
+                    constexpr int kBatch = 4;
+                    for (int c0 = 0; c0 < 4 * C::kFull; c0 += kBatch) {
+                        uint4 v[2 * kBatch];
+#pragma unroll
+                        for (int i = 0; i < 2 * kBatch; ++i)
+                            v[i] = live_row ? __ldg(src + 2 * c0 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int c = 0; c < kBatch; ++c) {
+                            uint32_t r[8] = {v[2 * c].x, v[2 * c].y, v[2 * c].z, v[2 * c].w,
+                                             v[2 * c + 1].x, v[2 * c + 1].y, v[2 * c + 1].z, v[2 * c + 1].w};
+                            tmem_st8(lane_addr + C::kTmemQ + (c0 + c) * 8, r);
+                        }
+                    }
                 }
                 {
                     // the rank's rope half (32 dims = 64 bytes), the K-major
