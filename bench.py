@@ -50,11 +50,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 MMA_FILES = ("mla_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
 TC_FILES = ("mla_tc.cu", "tc_ptx.cuh", "common.cuh", "plan.cuh", "args.cuh")
 NCU_TRAFFIC = {
-    "mla_v2lite": {"files": MMA_FILES, "src_sha": "f0c5aa8c76fa033a", "splits": 16, "bytes": 329797120 + 3693568,
+    "mla_v2lite": {"files": MMA_FILES, "src_sha": "b12888e065c4399c", "splits": 16, "bytes": 329795584 + 3415040,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64>"},
-    "mla_longctx": {"files": TC_FILES, "src_sha": "d40fee9a247ef998", "splits": 256, "bytes": 478712576 + 3590400,
+    "mla_longctx": {"files": TC_FILES, "src_sha": "36e8adbe4251c80b", "splits": 256, "bytes": 485617152 + 4000768,
                     "kernel": "mla_decode_tc_kernel<576,512,0>"},
-    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "d40fee9a247ef998", "splits": 64, "bytes": 1403810304 + 5198848,
+    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "36e8adbe4251c80b", "splits": 64, "bytes": 1423701760 + 25652736,
                    "kernel": "mla_decode_tc_kernel<576,512,1>"},
 }
 
