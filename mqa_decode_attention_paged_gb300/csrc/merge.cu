@@ -9,25 +9,37 @@
 // lse_s = -inf get weight 0.  The merge order is fixed (ascending segment), so
 // the result is reproducible run to run.
 //
-// One warp per (request, head), four heads per block: the lse maximum and
-// the weight sum are warp reductions, and lane l owns the float4 column groups
-// l, l + 32, l + 64, l + 96 of the row that exist (R / 4 groups, R <= 512).  It is launched as a
-// programmatic dependent of stage 1 and kept small (no shared memory, few
-// registers) so that its blocks fit beside the stage-1 CTAs and wait there:
-// the page prefix (from seq_lens only) is computed before waiting for stage
-// 1 to finish, the partials after.
+// One warp per (request, head) row, or per 128-column quarter of a row when
+// the requests are summed from many partials (long sequences over many
+// units: the host picks by the mean number of partials per request), four
+// warps per block.  The lse maximum and the weight sum are warp reductions
+// over the partials; lane l owns the float4 column groups l, l + 32, ... of
+// its columns, and the loads of several partials are in flight together.  It
+// is launched as a programmatic dependent of stage 1 and kept small (no
+// shared memory) so that its blocks fit beside the stage-1 CTAs and wait
+// there: the page prefix (from seq_lens only) is computed before waiting for
+// stage 1 to finish, the partials after.
 #include "common.cuh"
 #include "plan.cuh"
 #include "args.cuh"
 
 namespace mqa {
 
-constexpr int kMergeWarps = 4;  // heads per block
+constexpr int kMergeWarps = 4;  // warps per block
 
-__global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_kernel(const MergeArgs a) {
+// G float4 column groups per lane: a warp covers 128 G columns of a row, with
+// the loads of 8 (G = 1) or 4 (G = 4) partials in flight together.  The
+// row-per-warp form is held to 128 registers so that its blocks fit beside
+// the 16-head stage-1 CTAs while they wait.
+template <int G>
+__global__ void __launch_bounds__(32 * kMergeWarps, G == 4 ? 4 : 1) lse_merge_kernel(const MergeArgs a) {
+    constexpr int kMergeCols = 128 * G;
+    constexpr int kMergeBatch = G == 1 ? 8 : 4;
     const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x;
-    const int h = blockIdx.y * kMergeWarps + (threadIdx.x >> 5);
+    const int b = blockIdx.y;
+    const int nq = (a.R + kMergeCols - 1) / kMergeCols;  // warps per row
+    const int item = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    const int h = item / nq, q = item - h * nq;
     const int P = a.plan.page;
     if (h >= a.H) return;
 
@@ -48,6 +60,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_kernel(const Merge
     const int n_b = (clamp_len(a.seq_lens[b], a.plan.max_blocks, P, nullptr) + P - 1) / P;
     const int R = a.R;
     const long long orow = (static_cast<long long>(b) * a.H + h) * R;
+    const int col = q * kMergeCols + 4 * lane;  // first column of the lane's group k: col + 128 k
 
     int gf = 0, gl = 0;
     if (n_b > 0) {
@@ -57,8 +70,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_kernel(const Merge
     }
     pdl_wait();  // stage-1 partials (and the outputs' previous readers) are done
     if (n_b == 0) {  // empty request: out = 0, lse = -inf
-        for (int i = lane; i < R / 2; i += 32) reinterpret_cast<uint32_t*>(a.out + orow)[i] = 0u;
-        if (a.lse && lane == 0) a.lse[static_cast<long long>(b) * a.H + h] = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < G; ++k)
+            if (col + 128 * k < R) *reinterpret_cast<uint2*>(a.out + orow + col + 128 * k) = make_uint2(0u, 0u);
+        if (a.lse && q == 0 && lane == 0) a.lse[static_cast<long long>(b) * a.H + h] = -INFINITY;
         return;
     }
 
@@ -76,11 +91,10 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_kernel(const Merge
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
 
-    const int ng = R / 4;  // float4 column groups of the row
-    float4 acc[4];
+    float4 acc[G];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float* base = a.ws_o + (static_cast<long long>(gf + b) * a.H + h) * R + 4 * lane;
+    for (int k = 0; k < G; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* base = a.ws_o + (static_cast<long long>(gf + b) * a.H + h) * R + col;
     const long long step = static_cast<long long>(a.H) * R;
     float wsum = 0.f;
     for (int j0 = 0; j0 < np; j0 += 32) {
@@ -90,21 +104,21 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_kernel(const Merge
         const float wl = (l == -INFINITY || m == -INFINITY) ? 0.f : __expf(l - m);
         wsum += wl;
         const int nu = min(32, np - j0);
-        for (int i0 = 0; i0 < nu; i0 += 4) {
-            float4 v[4][4];
+        for (int i0 = 0; i0 < nu; i0 += kMergeBatch) {
+            float4 v[kMergeBatch][G];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < kMergeBatch; ++u)
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    v[u][k] = (i0 + u < nu && lane + 32 * k < ng)
+                for (int k = 0; k < G; ++k)
+                    v[u][k] = (i0 + u < nu && col + 128 * k < R)
                                   ? __ldcs(reinterpret_cast<const float4*>(base + (j0 + i0 + u) * step + 128 * k))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kMergeBatch; ++u) {
                 const float w = __shfl_sync(0xffffffffu, wl, (i0 + u) & 31);
                 if (i0 + u < nu && w != 0.f) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                    for (int k = 0; k < G; ++k) {
                         acc[k].x += w * v[u][k].x;
                         acc[k].y += w * v[u][k].y;
                         acc[k].z += w * v[u][k].z;
@@ -118,22 +132,32 @@ __global__ void __launch_bounds__(32 * kMergeWarps) lse_merge_kernel(const Merge
     for (int o = 16; o >= 1; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     const float inv = wsum > 0.f ? a.out_scale / wsum : 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        if (lane + 32 * k >= ng) break;
+    for (int k = 0; k < G; ++k) {
+        if (col + 128 * k >= R) break;
         uint2 packed;
         packed.x = pack_bf16x2(acc[k].x * inv, acc[k].y * inv);
         packed.y = pack_bf16x2(acc[k].z * inv, acc[k].w * inv);
-        *reinterpret_cast<uint2*>(a.out + orow + 4 * lane + 128 * k) = packed;
+        *reinterpret_cast<uint2*>(a.out + orow + col + 128 * k) = packed;
     }
-    if (lane == 0 && a.lse)
+    if (q == 0 && lane == 0 && a.lse)
         a.lse[static_cast<long long>(b) * a.H + h] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
 }
 
-cudaError_t lse_merge(const MergeArgs& a, cudaStream_t stream) {
-    cudaError_t e = launch_with_pdl(lse_merge_kernel, dim3(a.plan.batch, (a.H + kMergeWarps - 1) / kMergeWarps),
+template <int G>
+static cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
+    const int items = a.H * ((a.R + 128 * G - 1) / (128 * G));  // warps per request
+    cudaError_t e = launch_with_pdl(lse_merge_kernel<G>, dim3((items + kMergeWarps - 1) / kMergeWarps, a.plan.batch),
                                     dim3(32 * kMergeWarps), 0, stream, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+cudaError_t lse_merge(const MergeArgs& a, cudaStream_t stream) {
+    // a request is summed from about (units + batch) / batch partials: with
+    // more than 4 on average, a warp per 128 columns (more warps, fewer
+    // loads each) beats a warp per row
+    const bool many = a.plan.units > 3 * a.plan.batch;
+    return many ? launch_merge<1>(a, stream) : launch_merge<4>(a, stream);
 }
 
 }  // namespace mqa
