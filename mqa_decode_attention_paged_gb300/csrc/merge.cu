@@ -28,13 +28,13 @@ namespace mqa {
 constexpr int kMergeWarps = 4;  // warps per block
 
 // G float4 column groups per lane: a warp covers 128 G columns of a row, with
-// the loads of 8 (G = 1) or 4 (G = 4) partials in flight together.  The
-// row-per-warp form is held to 128 registers so that its blocks fit beside
-// the 16-head stage-1 CTAs while they wait.
+// the loads of 8 (G = 1) or 2 (G = 4) partials in flight together.  The
+// row-per-warp form is held to 80 registers so that its blocks fit beside
+// the stage-1 CTAs while they wait.
 template <int G>
-__global__ void __launch_bounds__(32 * kMergeWarps, G == 4 ? 4 : 1) lse_merge_kernel(const MergeArgs a) {
+__global__ void __launch_bounds__(32 * kMergeWarps, G == 4 ? 6 : 1) lse_merge_kernel(const MergeArgs a) {
     constexpr int kMergeCols = 128 * G;
-    constexpr int kMergeBatch = G == 1 ? 8 : 4;
+    constexpr int kMergeBatch = G == 1 ? 8 : 2;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.y;
     const int nq = (a.R + kMergeCols - 1) / kMergeCols;  // warps per row
