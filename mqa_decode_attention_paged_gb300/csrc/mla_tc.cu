@@ -661,16 +661,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster_relaxed(xfree_remote);
-                // ---- mask, scale to base 2, row maximum
+                // ---- mask, row maximum in base 2.  With a bf16 cache a pair
+                // of valid tokens keeps the raw sums: the base-2 scale k2 =
+                // sl2 (> 0) goes into the maximum and into the exponent (P =
+                // 2^(s k2 - m), one FMA per logit); otherwise (and always for
+                // the e4m3 kernel, whose registers are at their limit) the
+                // sums are masked and scaled here and k2 = 1.
+                float k2 = FP8 ? 1.f : a.sl2;
+                if (FP8 || vm != ~0ull || !(a.sl2 > 0.f)) {
 #pragma unroll
-                for (int i = 0; i < C::kPair; ++i) s[i] = ((vm >> i) & 1ull) ? s[i] * a.sl2 : -INFINITY;
+                    for (int i = 0; i < C::kPair; ++i) s[i] = ((vm >> i) & 1ull) ? s[i] * a.sl2 : -INFINITY;
+                    k2 = 1.f;
+                }
                 float mx[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     mx[i] = fmaxf(fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24])),
                                   fmaxf(fmaxf(s[i + 32], s[i + 40]), fmaxf(s[i + 48], s[i + 56])));
                 const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * k2;
                 // ---- running maximum: continue the one the other group
                 // published after pair p - 1 (always waited for, so that its
                 // slot is not overwritten before it was read)
@@ -725,8 +734,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(s[half * 32 + 2 * i] - m_use);
-                        const float p1 = ex2(s[half * 32 + 2 * i + 1] - m_use);
+                        const float p0 = ex2(fmaf(s[half * 32 + 2 * i], k2, -m_use));
+                        const float p1 = ex2(fmaf(s[half * 32 + 2 * i + 1], k2, -m_use));
                         psum += p0 + p1;
                         pk[i] = FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
                     }
