@@ -1,37 +1,41 @@
 // MLA decode, stage 1, fifth-generation tensor-core path for 65..128 heads.
 //
 // A thread-block cluster of two CTAs owns one work unit (plan.cuh) and splits
-// the 576 (or 320) latent columns: rank 0 contracts Q.K^T over the first R/2
-// columns and accumulates O[:, 0:R/2]; rank 1 contracts over the remaining
-// columns (the rest of kv_c and all of k_pe) and accumulates O[:, R/2:R].  The
-// V columns a rank needs are a prefix of the K columns it already loaded (V is
-// the first kv_lora_rank columns of the same row: "Triton と MLA" page,
-// vllm-arch-zh ja/attention/triton-mla, データフロー), so every cache byte is
-// read from HBM once and TMEM holds O[128 x R/2], the logits, P and Q.  The
-// two partial logit tiles are exchanged through distributed shared memory and
-// summed identically in both CTAs, which then run the same online softmax
+// the 576 (or 320) latent columns so that both ranks contract over the same
+// number: rank r holds the kv_c panels [r R/128, (r + 1) R/128) (64 columns
+// each; they are also its V columns) and the 32-column half r of k_pe, and
+// accumulates O[:, r R/2 : (r + 1) R/2].  V is the first kv_lora_rank columns
+// of the same cache row ("Triton と MLA" page, vllm-arch-zh
+// ja/attention/triton-mla, データフロー), so every cache byte is read from
+// HBM once and TMEM holds O[128 x R/2], the logits, P and the rank's Q panels.
+// The two partial logit tiles are exchanged through distributed shared memory
+// and summed identically in both CTAs, which then run the same online softmax
 // (tutorial page lshu.cn/news/265860, §7).
 //
 // The cache streams in 64-token pairs (masks are kept per 32-token tile).
 // Per CTA (352 threads):
-//   warp 0      TMA producer: each pair's rows of this CTA's column panels
-//               (tensor-map copies, 128-byte swizzle) into a ring of 64-row
-//               slots, one 3D copy per pair when pages hold whole pairs;
-//   warp 1      TMEM owner and single-thread MMA issuer:
-//               S[128 x 64] = Q K^T per pair (kind::f16, M = 128 heads, N = 64
-//               tokens, A = Q from TMEM), then O[128 x R/2] += P V per pair
-//               (A = P from TMEM, V read MN-major from the slot);
+//   warp 0      TMA producer: the lanes work out a pair's boxes (page, block
+//               id, validity) before its ring slot frees; then one 3D copy of
+//               the pair's panels and one of its rope half when pages hold
+//               whole pairs (else per-box 2D copies), 128-byte (panels) and
+//               64-byte (rope) swizzle; L2 prefetches of the rows and of each
+//               piece's query rows;
+//   warp 1      TMEM owner and single-thread Q.K^T issuer: S[128 x 64] per
+//               pair (kind::f16, M = 128 heads, N = 64 tokens, A = Q from
+//               TMEM for the kv_c panels and from shared memory for the rope
+//               half);
 //   warps 2..9  two softmax groups of four warps (one thread per head row);
 //               group g takes the pairs of parity g, so two pairs are in
 //               flight: read the 64 partial logits of the row, send them to
 //               the peer, add the peer's partial, mask, take the row maximum,
 //               continue the running maximum handed over by the other group
 //               (lazy rescaling of O only when it grows by more than 2^8),
-//               write P (bf16) into TMEM; per piece, the group of the last
-//               pair writes the output; they also write each piece's Q rows
-//               into TMEM;
-//   warp 10     loader of the Q panel that does not fit in TMEM (rank 1, head
-//               576 only).
+//               write P into TMEM; the group of a piece's last pair writes the
+//               output, and the group that reads a piece's last logits loads
+//               the next piece's Q; with an e4m3 cache, the group owning pair
+//               q - 1 first widens pair q to f16 in place;
+//   warp 10     single-thread P.V issuer: O += P V per pair in pair order
+//               (A = P from TMEM, V read MN-major from the slot).
 // Every wait is bounded; on expiry MQA_ERR_DEVICE_TIMEOUT is recorded and the
 // roles wind down.
 #include "args.cuh"
