@@ -453,7 +453,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         const uint32_t xfull_remote = map_to_rank(&bars[kXFull + g], peer);
         const uint32_t xfree_remote = map_to_rank(&bars[kXFree + g], peer);
         // warp-uniform bounded waits: TMEM accesses are warp-collective, so a
-        // lane never leaves the loop on its own
+        // lane never leaves the loop on its own.  (A warp whose wait expires
+        // does leave it; in the e4m3 kernel the other warps of its group can
+        // then block in the widening's named barrier, which has no time
+        // limit.  Waits expire only on a broken hand-off or a GPU stalled for
+        // seconds, never on caller input: bad block ids and lengths are
+        // masked before any wait.)
         auto wait_all = [&](uint64_t* bar, uint32_t parity, bool cluster_scope) {
             const bool done = cluster_scope ? mbar_wait_cluster(bar, parity) : mbar_wait(bar, parity);
             return __all_sync(0xffffffffu, done);
