@@ -52,9 +52,9 @@ TC_FILES = ("mla_tc.cu", "tc_ptx.cuh", "common.cuh", "plan.cuh", "args.cuh")
 NCU_TRAFFIC = {
     "mla_v2lite": {"files": MMA_FILES, "src_sha": "b12888e065c4399c", "splits": 16, "bytes": 329834496 + 3723520,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64>"},
-    "mla_longctx": {"files": TC_FILES, "src_sha": "9b58e5fd839cf7f1", "splits": 256, "bytes": 485191168 + 4390144,
+    "mla_longctx": {"files": TC_FILES, "src_sha": "3a3417efce472d21", "splits": 256, "bytes": 485191168 + 4390144,
                     "kernel": "mla_decode_tc_kernel<576,512,0>"},
-    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "9b58e5fd839cf7f1", "splits": 64, "bytes": 1423319040 + 25654784,
+    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "3a3417efce472d21", "splits": 64, "bytes": 1423319040 + 25654784,
                    "kernel": "mla_decode_tc_kernel<576,512,1>"},
 }
 
