@@ -77,6 +77,8 @@ def _load():
         lib.oracle_mla_decode_streaming.argtypes = mla + [I]
         lib.oracle_mla_decode_split.restype = I
         lib.oracle_mla_decode_split.argtypes = mla + [I]
+        lib.oracle_mla_decode_multi.restype = I
+        lib.oracle_mla_decode_multi.argtypes = [P, P, I, P, P, D, D, P, P, I, I, I, I, I, I, I, I]
         lib.oracle_gqa_paged_decode.restype = I
         lib.oracle_gqa_paged_decode.argtypes = [P, P, I, P, P, D, D, D, P, P, I, I, I, I, I, I, I]
         _lib = lib
@@ -180,6 +182,27 @@ def mla_decode_split(q, kv, kv_dtype, block_table, seq_lens, scale, k_scale=1.0,
     R = D - 64 if kv_lora_rank is None else kv_lora_rank
     return _run_mla("oracle_mla_decode_split", q, kv, kv_dtype, block_table, seq_lens, scale,
                     k_scale, R, [int(num_splits)])
+
+
+def mla_decode_multi(q, kv, kv_dtype, block_table, seq_lens, scale, k_scale=1.0, kv_lora_rank=None):
+    """Multi-token decode: q [B, q_len, H, D]; query i of request b sees the
+    first seq_lens[b] - q_len + i + 1 tokens.  Returns (out [B, q_len, H, R],
+    lse [B, q_len, H])."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    if q.ndim != 4:
+        raise ValueError("q must be [batch, q_len, heads, head_size]")
+    B, Lq, H, D = q.shape
+    R = D - 64 if kv_lora_rank is None else int(kv_lora_rank)
+    _, kv, bt, sl, code, _, _, _, nb, P = _mla_args(q.reshape(B, Lq * H, D), kv, kv_dtype, block_table,
+                                                     seq_lens)
+    out = np.zeros((B, Lq, H, R), dtype=np.float64)
+    lse = np.zeros((B, Lq, H), dtype=np.float64)
+    rc = _load().oracle_mla_decode_multi(_ptr(q), _ptr(kv), code, _ptr(bt), _ptr(sl), float(scale),
+                                         float(k_scale), _ptr(out), _ptr(lse), B, Lq, H, D, R, nb, P,
+                                         bt.shape[1])
+    if rc != 0:
+        raise ValueError("oracle: block table entry out of range or too short for a sequence")
+    return out, lse
 
 
 def gqa_paged_decode(q, kv, kv_dtype, block_table, seq_lens, scale, k_scale=1.0, v_scale=1.0):

@@ -34,6 +34,15 @@
  *   in batch-invariant mode.  Source: "Triton と MLA" page, 主要ファイル
  *   (_compute_num_kv_splits) and データフロー (VLLM_BATCH_INVARIANT branch).
  *
+ *   Multi-token decode (several new positions of a request verified in one
+ *   call): query i of q_len sits at absolute position
+ *   context_length + i, context_length = kv_length - q_len, and sees the keys
+ *   at positions <= its own: a full rectangle over the history plus a
+ *   q_len x q_len lower triangle.  Source: tutorial page §10
+ *   ("多 Token 验证时的 Attention 结构": query_abs_position =
+ *   context_length + query_local_position, mask = key_position <=
+ *   query_abs_position).
+ *
  *   GQA paged decode over a [num_blocks, 2, page, num_kv_heads, head_size]
  *   cache.  Source: "AttentionBackend" page (vllm-arch-zh, fr/attention/backend),
  *   section "Motivation de conception" (FlashAttention cache layout).
@@ -43,6 +52,9 @@
  *   - bf16 caches ignore k_scale (the page's "is_fp8 check is a no-op").
  *   - fp8 caches are OCP e4m3fn; value = k_scale * e4m3(code) for K and V.
  *   - a sequence of length 0 gives out = 0 and lse = -inf.
+ *   - multi-token decode: seq_lens[b] is kv_length (history plus the q_len
+ *     new tokens, whose keys are already in the cache); a query that sees no
+ *     key (kv_length < q_len - i) gives out = 0 and lse = -inf.
  *   - GQA query head h reads KV head h / (Hq / Hkv).
  *   - split s of a sequence with n tokens covers the page-aligned token range
  *     [s*L, min((s+1)*L, n)), L = ceil(ceil(n/page)/S) * page.
@@ -388,6 +400,32 @@ int oracle_mla_decode_split(const uint16_t* q, const void* kv, int kv_dtype,
                             int num_blocks, int P, int max_blocks, int num_splits) {
     token_view tv = mla_view(kv, kv_dtype, block_table, k_scale, D, R, num_blocks, P, max_blocks);
     return run_heads(&tv, q, seq_lens, scale, B, H, H, D, out, lse, FORM_SPLIT, num_splits);
+}
+
+/* Multi-token MLA decode.  q: bf16 bits [B, q_len, H, D]; out: [B, q_len, H, R];
+ * lse: [B, q_len, H].  Query i of request b attends the first
+ * seq_lens[b] - q_len + i + 1 tokens (the direct definition over them). */
+int oracle_mla_decode_multi(const uint16_t* q, const void* kv, int kv_dtype, const int32_t* block_table,
+                            const int32_t* seq_lens, double scale, double k_scale, double* out,
+                            double* lse, int B, int q_len, int H, int D, int R, int num_blocks, int P,
+                            int max_blocks) {
+    if (q_len < 1) return -1;
+    token_view tv = mla_view(kv, kv_dtype, block_table, k_scale, D, R, num_blocks, P, max_blocks);
+    int failed = 0;
+    int64_t rows = (int64_t)B * q_len * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int64_t row = 0; row < rows; ++row) {
+        int b = (int)(row / ((int64_t)q_len * H));
+        int i = (int)((row / H) % q_len);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+        for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_value(q[row * D + d]);
+        int n = seq_lens[b] - q_len + i + 1; /* keys at positions <= context_length + i */
+        if (n > seq_lens[b]) n = seq_lens[b];
+        if (n < 0) n = 0;
+        failed |= attend_direct(&tv, b, n, qd, scale, out + row * R, lse + row) != 0;
+        free(qd);
+    }
+    return failed ? -1 : 0;
 }
 
 /* q: bf16 bits [B, Hq, D]; kv: [num_blocks, 2, P, Hkv, D] (plane 0 = K,
