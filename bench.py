@@ -108,6 +108,10 @@ def workload_config(case, name, splits):
                  "outside the timed events"}
     if case.kind == "mla":
         cfg["kv_lora_rank"] = case.kv_lora_rank
+        if case.meta.get("q_len", 1) > 1:
+            cfg["q_len"] = case.meta["q_len"]
+            cfg["num_heads"] = case.num_heads // case.meta["q_len"]
+            cfg["query_rows"] = case.num_heads
     else:
         cfg["num_kv_heads"] = case.num_kv_heads
     return cfg
@@ -181,7 +185,13 @@ def time_oracle(case, budget_s=12.0, min_reps=1):
         sub = synth.replace(case, q=case.q[rows], block_table=case.block_table[rows],
                             seq_lens=case.seq_lens[rows])
         t0 = time.perf_counter()
-        if case.kind == "mla":
+        q_len = case.meta.get("q_len", 1)
+        if case.kind == "mla" and q_len > 1:
+            nb_, rows_, d_ = sub.q.shape
+            oracle.mla_decode_multi(sub.q.reshape(nb_, q_len, rows_ // q_len, d_), sub.kv, sub.kv_dtype,
+                                    sub.block_table, sub.seq_lens, sub.scale, k_scale=sub.k_scale,
+                                    kv_lora_rank=sub.kv_lora_rank)
+        elif case.kind == "mla":
             oracle.mla_decode(sub.q, sub.kv, sub.kv_dtype, sub.block_table, sub.seq_lens, sub.scale,
                               k_scale=sub.k_scale, kv_lora_rank=sub.kv_lora_rank)
         else:
@@ -305,8 +315,15 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     launches_per_call = 1 if splits == 1 else 2
 
+    q_len = case.meta.get("q_len", 1)
+
     def call(qq=q, btt=bt, sll=sl, oo=out, ll=lse):
-        if case.kind == "mla":
+        if case.kind == "mla" and q_len > 1:  # rows are q_len x heads, token-major
+            hh = H // q_len
+            mqa.mla_decode_multi(qq.view(B, q_len, hh, D), kv, btt, sll, case.scale, case.k_scale,
+                                 out=oo.view(B, q_len, hh, R), lse=ll.view(B, q_len, hh),
+                                 num_kv_splits=splits, workspace=ws, kv_lora_rank=R, stream=stream)
+        elif case.kind == "mla":
             mqa.mla_decode(qq, kv, btt, sll, case.scale, case.k_scale, out=oo, lse=ll,
                            num_kv_splits=splits, workspace=ws, kv_lora_rank=R, stream=stream)
         else:

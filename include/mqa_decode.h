@@ -141,6 +141,31 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
                       int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
                       void* workspace, size_t workspace_bytes, int* device_status, void* stream);
 
+/* Multi-token MLA decode: q_len new positions of each request verified in
+ * one call (speculative decoding).  The tutorial page (lshu.cn/news/265860)
+ * §10 gives the structure: query i of q_len sits at absolute position
+ * context_length + i and sees the keys at positions <= its own, i.e. the
+ * whole history plus a q_len x q_len lower triangle over the new tokens.
+ *
+ *   q        bf16 [batch, q_len, num_heads, head_size] (contiguous).
+ *   seq_lens int32 [batch]: kv_length, the history plus the q_len new tokens,
+ *            whose cache rows are already written; query i attends the first
+ *            seq_lens[b] - q_len + i + 1 tokens (none when that is <= 0:
+ *            out = 0, lse = -inf).
+ *   out      bf16 [batch, q_len, num_heads, kv_lora_rank], fully written.
+ *   lse      fp32 [batch, q_len, num_heads] or NULL.
+ *   q_len >= 1 and q_len * num_heads <= 128 (else MQA_ERR_UNSUPPORTED);
+ *   workspace: mla_decode_workspace_bytes(batch, q_len * num_heads,
+ *   kv_lora_rank, num_kv_splits) bytes.  The rows q_len * num_heads share the
+ *   cache exactly as query heads do; q_len = 1 is mla_decode.  Other
+ *   arguments, results and errors are those of mla_decode. */
+mqa_status mla_decode_multi(const void* q, const void* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                            int batch, int q_len, int num_heads, int head_size, int kv_lora_rank,
+                            int num_blocks, int page_size, int max_blocks, mqa_kv_dtype kv_dtype,
+                            int num_kv_splits, void* workspace, size_t workspace_bytes, int* device_status,
+                            void* stream);
+
 /* Size of the library-owned scratch array used by mla_decode_noalloc. */
 #define MQA_NOALLOC_SCRATCH_BYTES (64u << 20)
 

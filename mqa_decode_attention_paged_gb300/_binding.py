@@ -60,6 +60,8 @@ def _load() -> ctypes.CDLL:
     lib.gqa_paged_decode_workspace_bytes.argtypes = [I, I, I, I]
     lib.mla_decode.restype = I
     lib.mla_decode.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
+    lib.mla_decode_multi.restype = I
+    lib.mla_decode_multi.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
     lib.mla_decode_noalloc.restype = I
     lib.mla_decode_noalloc.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, P]
     lib.gqa_paged_decode.restype = I
@@ -143,6 +145,36 @@ def mla_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *, out=No
                         _ptr(device_status), _stream(stream))
     if rc != OK:
         raise MqaError(rc, "mla_decode")
+    return out, lse
+
+
+def mla_decode_multi(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *, out=None, lse=None,
+                     num_kv_splits=1, workspace=None, kv_lora_rank=None, kv_dtype=None,
+                     device_status=None, stream=None, return_lse=True):
+    """Multi-token MLA decode through the C ABI.  q [B, q_len, H, D] bf16 (query i of
+    request b sits at position seq_lens[b] - q_len + i and sees the keys up to it);
+    returns out [B, q_len, H, R] bf16 and lse [B, q_len, H] fp32."""
+    import torch
+    B, Lq, H, D = q.shape
+    nb, page, D2 = kv_cache.shape
+    if D2 != D:
+        raise ValueError("q and kv_cache head sizes differ")
+    R = (D - 64) if kv_lora_rank is None else int(kv_lora_rank)
+    code = _kv_code(kv_cache, kv_dtype)
+    if out is None:
+        out = torch.empty((B, Lq, H, R), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Lq, H), dtype=torch.float32, device=q.device)
+    need = mla_decode_workspace_bytes(B, Lq * H, R, num_kv_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.mla_decode_multi(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), float(scale),
+                              float(k_scale), _ptr(out), _ptr(lse), B, Lq, H, D, R, nb, page,
+                              block_table.shape[1], code, int(num_kv_splits), _ptr(workspace), ws_bytes,
+                              _ptr(device_status), _stream(stream))
+    if rc != OK:
+        raise MqaError(rc, "mla_decode_multi")
     return out, lse
 
 

@@ -251,51 +251,13 @@ bool mla_tensor_map(CUtensorMap* out, const void* base, int cols, long long rows
 
 }  // namespace
 
-extern "C" {
-
-int mqa_abi_version(void) { return MQA_ABI_VERSION; }
-
-const char* mqa_status_string(int status) {
-    switch (status) {
-        case MQA_OK: return "ok";
-        case MQA_ERR_INVALID_ARG: return "invalid argument";
-        case MQA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
-        case MQA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
-        case MQA_ERR_CUDA: return "CUDA error";
-        case MQA_ERR_DEVICE_CHECK: return "device check failed (block id or sequence length)";
-        case MQA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
-        default: return "unknown status";
-    }
-}
-
-int mqa_device_sm_count(void) { return sm_count_current(); }
-
-int mqa_last_cuda_error(void) { return static_cast<int>(g_last_cuda_error); }
-
-const char* mqa_last_cuda_error_string(void) { return cudaGetErrorString(g_last_cuda_error); }
-
-int mqa_num_kv_splits(int max_seq_len, int sm_count, int batch_invariant) {
-    if (batch_invariant) return 1;
-    long long s = max_seq_len <= 0 ? 1 : (static_cast<long long>(max_seq_len) + 511) / 512;
-    const long long cap = 2LL * sm_count;
-    if (cap >= 1 && s > cap) s = cap;
-    if (s < 1) s = 1;
-    return static_cast<int>(s);
-}
-
-size_t mla_decode_workspace_bytes(int batch, int num_heads, int kv_lora_rank, int num_kv_splits) {
-    return partial_bytes(batch, num_heads, kv_lora_rank, num_kv_splits);
-}
-
-size_t gqa_paged_decode_workspace_bytes(int batch, int num_q_heads, int head_size, int num_kv_splits) {
-    return partial_bytes(batch, num_q_heads, head_size, num_kv_splits);
-}
-
-mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+static mqa_status mla_decode_rows(const void* q, const void* kv_cache, const int32_t* block_table,
                       const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
                       int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
                       int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
-                      void* workspace, size_t workspace_bytes, int* device_status, void* stream) {
+                      void* workspace, size_t workspace_bytes, int* device_status, void* stream,
+                      int q_len) {
+    // num_heads counts rows here: q_len query tokens x heads, token-major
     if (!q || !kv_cache || !block_table || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
         !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (device_status && !aligned(device_status, 4)))
@@ -361,6 +323,8 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
         t.sl2 = scale * (fp8 ? k_scale : 1.0f) * mqa::kLog2e;
         t.out_scale = fp8 ? k_scale : 1.0f;
         t.H = num_heads;
+        t.q_len = q_len;
+        t.heads = num_heads / q_len;
         t.num_blocks = num_blocks;
         t.plan.batch = batch;
         t.plan.page = page_size;
@@ -401,6 +365,8 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
     a.sl2 = scale * ks * mqa::kLog2e;
     a.out_scale = ks;
     a.H = num_heads;
+    a.q_len = q_len;
+    a.heads = num_heads / q_len;
     a.num_blocks = num_blocks;
     a.plan.batch = batch;
     a.plan.page = page_size;
@@ -437,6 +403,69 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
         if (cudaError_t e = mqa::lse_merge(m, st); e != cudaSuccess) return cuda_fail(e);
     }
     return MQA_OK;
+}
+
+extern "C" {
+
+int mqa_abi_version(void) { return MQA_ABI_VERSION; }
+
+const char* mqa_status_string(int status) {
+    switch (status) {
+        case MQA_OK: return "ok";
+        case MQA_ERR_INVALID_ARG: return "invalid argument";
+        case MQA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case MQA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MQA_ERR_CUDA: return "CUDA error";
+        case MQA_ERR_DEVICE_CHECK: return "device check failed (block id or sequence length)";
+        case MQA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int mqa_device_sm_count(void) { return sm_count_current(); }
+
+int mqa_last_cuda_error(void) { return static_cast<int>(g_last_cuda_error); }
+
+const char* mqa_last_cuda_error_string(void) { return cudaGetErrorString(g_last_cuda_error); }
+
+int mqa_num_kv_splits(int max_seq_len, int sm_count, int batch_invariant) {
+    if (batch_invariant) return 1;
+    long long s = max_seq_len <= 0 ? 1 : (static_cast<long long>(max_seq_len) + 511) / 512;
+    const long long cap = 2LL * sm_count;
+    if (cap >= 1 && s > cap) s = cap;
+    if (s < 1) s = 1;
+    return static_cast<int>(s);
+}
+
+size_t mla_decode_workspace_bytes(int batch, int num_heads, int kv_lora_rank, int num_kv_splits) {
+    return partial_bytes(batch, num_heads, kv_lora_rank, num_kv_splits);
+}
+
+size_t gqa_paged_decode_workspace_bytes(int batch, int num_q_heads, int head_size, int num_kv_splits) {
+    return partial_bytes(batch, num_q_heads, head_size, num_kv_splits);
+}
+
+mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                      const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                      int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
+                      int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
+                      void* workspace, size_t workspace_bytes, int* device_status, void* stream) {
+    return mla_decode_rows(q, kv_cache, block_table, seq_lens, scale, k_scale, out, lse, batch, num_heads,
+                           head_size, kv_lora_rank, num_blocks, page_size, max_blocks, kv_dtype, num_kv_splits,
+                           workspace, workspace_bytes, device_status, stream, 1);
+}
+
+mqa_status mla_decode_multi(const void* q, const void* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                            int batch, int q_len, int num_heads, int head_size, int kv_lora_rank,
+                            int num_blocks, int page_size, int max_blocks, mqa_kv_dtype kv_dtype,
+                            int num_kv_splits, void* workspace, size_t workspace_bytes, int* device_status,
+                            void* stream) {
+    if (q_len < 1 || num_heads < 1) return MQA_ERR_INVALID_ARG;
+    if (static_cast<long long>(q_len) * num_heads > 128) return MQA_ERR_UNSUPPORTED;
+    return mla_decode_rows(q, kv_cache, block_table, seq_lens, scale, k_scale, out, lse, batch,
+                           q_len * num_heads, head_size, kv_lora_rank, num_blocks, page_size, max_blocks,
+                           kv_dtype, num_kv_splits, workspace, workspace_bytes, device_status, stream, q_len);
 }
 
 mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* block_table,

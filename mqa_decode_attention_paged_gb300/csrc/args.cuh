@@ -33,6 +33,10 @@ struct MlaArgs {
     float sl2;        // scale * k_scale(fp8) * log2(e)
     float out_scale;  // k_scale for fp8, 1 for bf16
     int H, num_blocks;
+    // multi-token decode: the H rows are q_len query tokens x heads
+    // (token-major); row r (token i = r / heads) sees the first
+    // len - q_len + i + 1 tokens of its request.  q_len = 1: plain decode.
+    int q_len, heads;
     Plan plan;
 };
 
@@ -60,6 +64,7 @@ struct MlaTcArgs {
     float sl2;
     float out_scale;
     int H, num_blocks;
+    int q_len, heads;  // multi-token decode rows, as in MlaArgs
     Plan plan;
 };
 

@@ -82,7 +82,9 @@ struct MlaMmaCfg {
     static_assert(1024 + kOffCum + 4 * (2 * kMaxBatchSmem + 1) <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, int R, bool FP8, int TILE>
+// MULTI: multi-token decode (per-row key limits); the plain-decode kernels
+// are compiled without that code
+template <int D, int R, bool FP8, int TILE, bool MULTI>
 __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
     mla_decode_mma_kernel(const __grid_constant__ MlaArgs a) {
     using C = MlaMmaCfg<D, R, FP8, TILE>;
@@ -248,6 +250,9 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
 
     while (!aborted && have) {
         const int len = lens[pc.b];
+        // multi-token decode: the softmax row sh (token i = row / heads) sees
+        // tokens below len - q_len + i + 1 (tutorial page §10); len otherwise
+        const int row_lim = MULTI ? len - (a.q_len - 1 - (h0 + sh) / a.heads) : len;
         const int tok0 = pc.j0 * P;
         const int tok_end = min(pc.j1 * P, len);
         Piece nxt;
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
                 float mx = -INFINITY;
 #pragma unroll
                 for (int i = 0; i < kTPT; ++i) {
-                    const bool valid = (vmask >> (kTPT * sk + i)) & 1ull;
+                    const bool valid = ((vmask >> (kTPT * sk + i)) & 1ull) && (!MULTI || t0 + kTPT * sk + i < row_lim);
                     x[i] = valid ? x[i] * a.sl2 : -INFINITY;
                     mx = fmaxf(mx, x[i]);
                 }
@@ -510,7 +515,7 @@ static cudaError_t launch_mla_mma(const MlaArgs& a, int grid, cudaStream_t strea
     constexpr int kTile = MlaTile<D, FP8>::value;
     using C = MlaMmaCfg<D, R, FP8, kTile>;
     const size_t smem = C::smem_bytes(a.plan.batch);
-    auto kern = mla_decode_mma_kernel<D, R, FP8, kTile>;
+    auto kern = a.q_len > 1 ? mla_decode_mma_kernel<D, R, FP8, kTile, true> : mla_decode_mma_kernel<D, R, FP8, kTile, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -144,7 +144,9 @@ __device__ __forceinline__ void issue_qk(uint32_t d, uint32_t q_tmem, uint64_t k
                   idesc, 1u);
 }
 
-template <int D, int R, bool FP8>
+// MULTI: multi-token decode (per-row key limits); the plain-decode kernels
+// are compiled without that code
+template <int D, int R, bool FP8, bool MULTI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThreads, 1)
     mla_decode_tc_kernel(const __grid_constant__ MlaTcArgs a) {
     using C = MlaTcCfg<D, R>;
@@ -656,6 +658,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                     break;
                 }
                 const uint64_t vm = mask_s[p % C::kStages];
+                // tokens of the pair this row sees: multi-token decode limits
+                // row h (token i = h / heads) to tokens below len - q_len + i + 1
+                // (tutorial page §10); the V rows past the sequence end are
+                // still cleared by vm
+                uint64_t vmr = vm;
+                if constexpr (MULTI) {
+                    const int lim = lens[pc.b] - (a.q_len - 1 - h / a.heads) - (tok0 + j * C::kPair);
+                    vmr &= lim >= C::kPair ? ~0ull : lim <= 0 ? 0ull : ((1ull << lim) - 1);
+                }
                 if (!wait_all(&bars[kXFull + g], (p >> 1) & 1, true)) {
                     ok = false;
                     break;
@@ -677,9 +688,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 // the e4m3 kernel, whose registers are at their limit) the
                 // sums are masked and scaled here and k2 = 1.
                 float k2 = FP8 ? 1.f : a.sl2;
-                if (FP8 || vm != ~0ull || !(a.sl2 > 0.f)) {
+                if (FP8 || vmr != ~0ull || !(a.sl2 > 0.f)) {
 #pragma unroll
-                    for (int i = 0; i < C::kPair; ++i) s[i] = ((vm >> i) & 1ull) ? s[i] * a.sl2 : -INFINITY;
+                    for (int i = 0; i < C::kPair; ++i) s[i] = ((vmr >> i) & 1ull) ? s[i] * a.sl2 : -INFINITY;
                     k2 = 1.f;
                 }
                 float mx[8];
@@ -856,7 +867,7 @@ template <int D, int R, bool FP8>
 static cudaError_t launch_mla_tc(const MlaTcArgs& a, int clusters, cudaStream_t stream) {
     using C = MlaTcCfg<D, R>;
     const size_t smem = C::smem_bytes(a.plan.batch);
-    auto kern = mla_decode_tc_kernel<D, R, FP8>;
+    auto kern = a.q_len > 1 ? mla_decode_tc_kernel<D, R, FP8, true> : mla_decode_tc_kernel<D, R, FP8, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -197,6 +197,11 @@ WORKLOADS = {
                         page=64, kv_dtype="bf16", seed=1004),
     "gqa": dict(kind="gqa", B=256, seq_lens=("lognormal", 2048, 1.0, 16384), Hq=32, Hkv=8, D=128,
                 page=16, kv_dtype="bf16", seed=1005),
+    # multi-token decode (speculative verification): the V2-Lite-like batch
+    # with 8 new positions per request, 16 heads -> 128 query rows (q is
+    # [B, q_len, H, D], stored here as its [B, q_len * H, D] view)
+    "mla_mtp": dict(kind="mla", B=64, seq_lens=("uniform", 1024, 8192), H=128, D=576, page=64,
+                    kv_dtype="bf16", pool_factor=1.5, seed=1006, q_len=8),
 }
 
 
@@ -205,9 +210,12 @@ def workload(name: str, **overrides) -> PagedCase:
     spec = dict(WORKLOADS[name])
     spec.update(overrides)
     kind = spec.pop("kind")
+    q_len = spec.pop("q_len", 1)
     spec.setdefault("name", name)
     if kind == "mla":
-        return make_mla_case(**spec)
+        case = make_mla_case(**spec)
+        case.meta["q_len"] = q_len  # query rows are q_len x heads, token-major
+        return case
     return make_gqa_case(**spec)
 
 

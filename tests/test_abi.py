@@ -30,7 +30,7 @@ def _declared_functions():
 
 def test_header_symbols_are_exported():
     names = _declared_functions()
-    assert {"mla_decode", "gqa_paged_decode", "mqa_num_kv_splits", "mla_decode_workspace_bytes",
+    assert {"mla_decode", "mla_decode_multi", "gqa_paged_decode", "mqa_num_kv_splits", "mla_decode_workspace_bytes",
             "gqa_paged_decode_workspace_bytes", "mqa_status_string", "mqa_abi_version",
             "mqa_device_sm_count"} <= set(names)
     lib = ctypes.CDLL(mqa.LIB_PATH)
@@ -70,6 +70,29 @@ def _mla(**kw):
                               P(a["out"]), P(a["lse"]), a["B"], a["H"], a["D"], a["R"], a["nb"],
                               a["P"], a["maxb"], a["kvd"], a["S"], P(a["ws"]), a["wsb"],
                               P(a["status"]), P(a["stream"]))
+
+
+def _mla_multi(**kw):
+    a = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, scale=0.07, k_scale=1.0, out=FAKE, lse=None,
+             B=2, L=4, H=16, D=576, R=512, nb=10, P=16, maxb=8, kvd=0, S=1, ws=None, wsb=0)
+    a.update(kw)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)  # noqa: E731
+    return mqa.lib.mla_decode_multi(P(a["q"]), P(a["kv"]), P(a["bt"]), P(a["sl"]), a["scale"], a["k_scale"],
+                                    P(a["out"]), P(a["lse"]), a["B"], a["L"], a["H"], a["D"], a["R"], a["nb"],
+                                    a["P"], a["maxb"], a["kvd"], a["S"], P(a["ws"]), a["wsb"], None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(L=0), mqa.ERR_INVALID_ARG),
+    (dict(H=0), mqa.ERR_INVALID_ARG),
+    (dict(L=9, H=16), mqa.ERR_UNSUPPORTED),            # q_len x heads rows at most 128
+    (dict(L=129, H=1), mqa.ERR_UNSUPPORTED),
+    (dict(q=None), mqa.ERR_INVALID_ARG),               # then the checks of mla_decode on the rows
+    (dict(D=512, R=448), mqa.ERR_UNSUPPORTED),
+    (dict(S=4, ws=FAKE, wsb=mqa.mla_decode_workspace_bytes(2, 64, 512, 4) - 1), mqa.ERR_WORKSPACE_TOO_SMALL),
+])
+def test_mla_multi_validation(kw, code):
+    assert _mla_multi(**kw) == code
 
 
 def _gqa(**kw):
