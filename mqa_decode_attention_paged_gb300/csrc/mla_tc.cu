@@ -1,4 +1,5 @@
-// MLA decode, stage 1, fifth-generation tensor-core path for 65..128 heads.
+// MLA decode, stage 1, fifth-generation tensor-core path for 33..128 heads
+// (rows past the head count are padding of the M = 128 MMA).
 //
 // A thread-block cluster of two CTAs owns one work unit (plan.cuh) and splits
 // the 576 (or 320) latent columns so that both ranks contract over the same

@@ -46,7 +46,7 @@ def test_ragged_shapes(D, page, kv_dtype, splits):
 @pytest.mark.parametrize("page", [16, 64])
 @pytest.mark.parametrize("splits", [1, 4])
 def test_tensor_core_path_ragged(D, page, splits):
-    # 65..128 heads over a bf16 cache run on the 2-CTA tcgen05 clusters.
+    # 33..128 heads over a bf16 cache run on the 2-CTA tcgen05 clusters.
     case = synth.poison(synth.make_mla_case(RAGGED, H=128, D=D, page=page, pool_factor=1.2, seed=8,
                                             extra_cols=1))
     out, lse = run_gpu(case, splits)
@@ -95,13 +95,24 @@ def test_tensor_core_path_multi_tile_and_rescale():
         assert_close(out, lse, ref_out, ref_lse, what=f"tc rescale S={splits}")
 
 
-@pytest.mark.parametrize("H", [1, 5, 16, 40, 80, 100, 128])
+@pytest.mark.parametrize("H", [1, 5, 16, 32, 33, 40, 64, 80, 100, 128])
 def test_head_counts(H):
     case = synth.make_mla_case([77, 300, 1], H=H, page=64, seed=11)
     for splits in (1, 3):
         out, lse = run_gpu(case, splits)
         ref_out, ref_lse = run_oracle(case)
         assert_close(out, lse, ref_out, ref_lse, what=f"H={H} S={splits}")
+
+
+@pytest.mark.parametrize("H", [33, 64])
+def test_mid_head_counts_fp8(H):
+    # 33..64 heads of an e4m3 cache on the tcgen05 clusters (M = 128 padded)
+    case = synth.poison(synth.make_mla_case(RAGGED, H=H, page=64, kv_dtype="fp8_e4m3", k_scale=0.05,
+                                            pool_factor=1.2, seed=44, extra_cols=1))
+    for splits in (1, 3):
+        out, lse = run_gpu(case, splits)
+        ref_out, ref_lse = run_oracle(case)
+        assert_close(out, lse, ref_out, ref_lse, fp8=True, what=f"fp8 H={H} S={splits}")
 
 
 def test_many_units_and_tiles():
