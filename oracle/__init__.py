@@ -79,6 +79,8 @@ def _load():
         lib.oracle_mla_decode_split.argtypes = mla + [I]
         lib.oracle_mla_decode_multi.restype = I
         lib.oracle_mla_decode_multi.argtypes = [P, P, I, P, P, D, D, P, P, I, I, I, I, I, I, I, I]
+        lib.oracle_mla_decode_sparse.restype = I
+        lib.oracle_mla_decode_sparse.argtypes = [P, P, I, P, P, P, I, D, D, P, P, I, I, I, I, I, I, I]
         lib.oracle_gqa_paged_decode.restype = I
         lib.oracle_gqa_paged_decode.argtypes = [P, P, I, P, P, D, D, D, P, P, I, I, I, I, I, I, I]
         _lib = lib
@@ -182,6 +184,24 @@ def mla_decode_split(q, kv, kv_dtype, block_table, seq_lens, scale, k_scale=1.0,
     R = D - 64 if kv_lora_rank is None else kv_lora_rank
     return _run_mla("oracle_mla_decode_split", q, kv, kv_dtype, block_table, seq_lens, scale,
                     k_scale, R, [int(num_splits)])
+
+
+def mla_decode_sparse(q, kv, kv_dtype, block_table, seq_lens, indices, scale, k_scale=1.0, kv_lora_rank=None):
+    """Sparse decode: each query of request b attends the positions indices[b, :]
+    (entries outside [0, seq_lens[b]) select nothing).  Returns (out [B, H, R], lse [B, H])."""
+    q, kv, bt, sl, code, B, H, D, nb, P = _mla_args(q, kv, kv_dtype, block_table, seq_lens)
+    idx = np.ascontiguousarray(indices, dtype=np.int32)
+    if idx.ndim != 2 or idx.shape[0] != B:
+        raise ValueError("indices must be [batch, topk]")
+    R = D - 64 if kv_lora_rank is None else int(kv_lora_rank)
+    out = np.zeros((B, H, R), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    rc = _load().oracle_mla_decode_sparse(_ptr(q), _ptr(kv), code, _ptr(bt), _ptr(sl), _ptr(idx), idx.shape[1],
+                                          float(scale), float(k_scale), _ptr(out), _ptr(lse), B, H, D, R, nb,
+                                          P, bt.shape[1])
+    if rc != 0:
+        raise ValueError("oracle: block table entry out of range for a selected position")
+    return out, lse
 
 
 def mla_decode_multi(q, kv, kv_dtype, block_table, seq_lens, scale, k_scale=1.0, kv_lora_rank=None):

@@ -43,6 +43,13 @@
  *   context_length + query_local_position, mask = key_position <=
  *   query_abs_position).
  *
+ *   Sparse (top-k) decode: each query attends only the key positions its
+ *   request's index list selects (e.g. the top 2048), each translated to a
+ *   physical slot through the request's block table.  Source: tutorial page
+ *   §13 (Dense / Sparse Attention: "每个 Query 只与选中的 2048 个 Key 计算相关性",
+ *   and the request's top-k logical positions converted to physical KV
+ *   slots through its block table).
+ *
  *   GQA paged decode over a [num_blocks, 2, page, num_kv_heads, head_size]
  *   cache.  Source: "AttentionBackend" page (vllm-arch-zh, fr/attention/backend),
  *   section "Motivation de conception" (FlashAttention cache layout).
@@ -52,6 +59,10 @@
  *   - bf16 caches ignore k_scale (the page's "is_fp8 check is a no-op").
  *   - fp8 caches are OCP e4m3fn; value = k_scale * e4m3(code) for K and V.
  *   - a sequence of length 0 gives out = 0 and lse = -inf.
+ *   - sparse decode: index entries outside [0, seq_lens[b]) (e.g. -1 padding)
+ *     select nothing; the others are used as listed (an index listed twice
+ *     counts twice: callers pass distinct positions); none selected gives
+ *     out = 0 and lse = -inf.
  *   - multi-token decode: seq_lens[b] is kv_length (history plus the q_len
  *     new tokens, whose keys are already in the cache); a query that sees no
  *     key (kv_length < q_len - i) gives out = 0 and lse = -inf.
@@ -400,6 +411,57 @@ int oracle_mla_decode_split(const uint16_t* q, const void* kv, int kv_dtype,
                             int num_blocks, int P, int max_blocks, int num_splits) {
     token_view tv = mla_view(kv, kv_dtype, block_table, k_scale, D, R, num_blocks, P, max_blocks);
     return run_heads(&tv, q, seq_lens, scale, B, H, H, D, out, lse, FORM_SPLIT, num_splits);
+}
+
+/* Sparse MLA decode.  q: bf16 bits [B, H, D]; indices: [B, topk] token
+ * positions; out: [B, H, R]; lse: [B, H].  softmax(s) V over the selected
+ * tokens, written out directly (lse = m + log sum exp(s - m)). */
+int oracle_mla_decode_sparse(const uint16_t* q, const void* kv, int kv_dtype, const int32_t* block_table,
+                             const int32_t* seq_lens, const int32_t* indices, int topk, double scale,
+                             double k_scale, double* out, double* lse, int B, int H, int D, int R,
+                             int num_blocks, int P, int max_blocks) {
+    token_view tv = mla_view(kv, kv_dtype, block_table, k_scale, D, R, num_blocks, P, max_blocks);
+    int failed = 0;
+    int64_t pairs = (int64_t)B * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int64_t bh = 0; bh < pairs; ++bh) {
+        int b = (int)(bh / H);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+        double* s = (double*)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1));
+        int64_t* base = (int64_t*)malloc(sizeof(int64_t) * (size_t)(topk > 0 ? topk : 1));
+        for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_value(q[bh * D + d]);
+        double* o = out + bh * R;
+        for (int r = 0; r < R; ++r) o[r] = 0.0;
+        int n = 0;
+        double m = -INFINITY;
+        for (int e = 0; e < topk; ++e) {
+            int pos = indices[(int64_t)b * topk + e];
+            if (pos < 0 || pos >= seq_lens[b]) continue;
+            if (pos / P >= max_blocks) { failed = 1; continue; }
+            int64_t bs = token_base(&tv, b, pos);
+            if (bs < 0) { failed = 1; continue; }
+            base[n] = bs;
+            s[n] = logit(&tv, qd, bs, scale);
+            if (s[n] > m) m = s[n];
+            ++n;
+        }
+        if (n == 0) {
+            lse[bh] = -INFINITY;
+        } else {
+            double sum = 0.0;
+            for (int t = 0; t < n; ++t) sum += exp(s[t] - m);
+            double L = m + log(sum);
+            for (int t = 0; t < n; ++t) {
+                double w = exp(s[t] - L);
+                for (int r = 0; r < R; ++r) o[r] += w * (tv.v_mult * elem(&tv, base[t] + tv.v_offset + r));
+            }
+            lse[bh] = L;
+        }
+        free(qd);
+        free(s);
+        free(base);
+    }
+    return failed ? -1 : 0;
 }
 
 /* Multi-token MLA decode.  q: bf16 bits [B, q_len, H, D]; out: [B, q_len, H, R];
