@@ -78,8 +78,15 @@ def load_peaks():
 
 
 def workload_stats(case, splits):
-    """Algorithmic bytes and flops of one decode call."""
-    tokens = int(case.seq_lens.astype(np.int64).sum())
+    """Algorithmic bytes and flops of one decode call.  Sparse decode reads
+    the selected rows only (plus the index lists and one block-table entry per
+    selected row)."""
+    idx = case.meta.get("indices")
+    if idx is not None:
+        sel = (idx >= 0) & (idx < case.seq_lens[:, None])
+        tokens = int(sel.sum())
+    else:
+        tokens = int(case.seq_lens.astype(np.int64).sum())
     elt = 2 if case.kv_dtype == "bf16" else 1
     B, H, D = case.q.shape
     if case.kind == "mla":
@@ -93,6 +100,8 @@ def workload_stats(case, splits):
         flops = 2.0 * H * tokens * 2 * D
         out_w = D
     io_bytes = B * H * D * 2 + B * H * out_w * 2 + B * H * 4
+    if idx is not None:
+        io_bytes += idx.size * 4 + tokens * 4
     return dict(tokens=tokens, kv_bytes=kv_bytes, alg_bytes=kv_bytes + io_bytes, flops=flops,
                 q_bytes=B * H * D * 2, out_bytes=B * H * out_w * 2, lse_bytes=B * H * 4)
 
@@ -112,6 +121,9 @@ def workload_config(case, name, splits):
             cfg["q_len"] = case.meta["q_len"]
             cfg["num_heads"] = case.num_heads // case.meta["q_len"]
             cfg["query_rows"] = case.num_heads
+        if case.meta.get("indices") is not None:
+            cfg["topk"] = int(case.meta["indices"].shape[1])
+            cfg["selected_tokens"] = workload_stats(case, splits)["tokens"]
     else:
         cfg["num_kv_heads"] = case.num_kv_heads
     return cfg
@@ -184,9 +196,14 @@ def time_oracle(case, budget_s=12.0, min_reps=1):
         rows = order[rows_used:rows_used + n]
         sub = synth.replace(case, q=case.q[rows], block_table=case.block_table[rows],
                             seq_lens=case.seq_lens[rows])
+        idx = case.meta.get("indices")
         t0 = time.perf_counter()
         q_len = case.meta.get("q_len", 1)
-        if case.kind == "mla" and q_len > 1:
+        if idx is not None:
+            oracle.mla_decode_sparse(sub.q, sub.kv, sub.kv_dtype, sub.block_table, sub.seq_lens,
+                                     np.ascontiguousarray(idx[rows]), sub.scale, k_scale=sub.k_scale,
+                                     kv_lora_rank=sub.kv_lora_rank)
+        elif case.kind == "mla" and q_len > 1:
             nb_, rows_, d_ = sub.q.shape
             oracle.mla_decode_multi(sub.q.reshape(nb_, q_len, rows_ // q_len, d_), sub.kv, sub.kv_dtype,
                                     sub.block_table, sub.seq_lens, sub.scale, k_scale=sub.k_scale,
@@ -199,7 +216,11 @@ def time_oracle(case, budget_s=12.0, min_reps=1):
                                     sub.scale, k_scale=sub.k_scale, v_scale=sub.v_scale)
         dt = time.perf_counter() - t0
         elapsed += dt
-        done_tokens += int(sub.seq_lens.astype(np.int64).sum())
+        if idx is not None:
+            sel = idx[rows]
+            done_tokens += int(((sel >= 0) & (sel < sub.seq_lens[:, None])).sum())
+        else:
+            done_tokens += int(sub.seq_lens.astype(np.int64).sum())
         rows_used += len(rows)
         reps += 1
         n = min(case.batch - rows_used, max(1, len(rows) * 2))
@@ -286,7 +307,10 @@ def run_ours(args):
     case = synth.workload(args.workload)
     st = workload_stats(case, 1)
     sms = mqa.device_sm_count()
-    splits = args.splits or mqa.num_kv_splits(int(case.seq_lens.max()), sms, False)
+    idx_np = case.meta.get("indices")
+    # sparse decode splits the topk entries, dense decode the context
+    split_len = idx_np.shape[1] if idx_np is not None else int(case.seq_lens.max())
+    splits = args.splits or mqa.num_kv_splits(split_len, sms, False)
 
     # inputs resident in HBM
     q = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -296,6 +320,7 @@ def run_ours(args):
         kv = torch.from_numpy(case.kv).view(torch.float8_e4m3fn).to(dev)
     bt = torch.from_numpy(case.block_table).to(dev)
     sl = torch.from_numpy(case.seq_lens).to(dev)
+    idx = torch.from_numpy(idx_np).to(dev) if idx_np is not None else None
     B, H, D = q.shape
     R = case.kv_lora_rank if case.kind == "mla" else D
     out = torch.empty((B, H, R), dtype=torch.bfloat16, device=dev)
@@ -317,8 +342,11 @@ def run_ours(args):
 
     q_len = case.meta.get("q_len", 1)
 
-    def call(qq=q, btt=bt, sll=sl, oo=out, ll=lse):
-        if case.kind == "mla" and q_len > 1:  # rows are q_len x heads, token-major
+    def call(qq=q, btt=bt, sll=sl, oo=out, ll=lse, ii=idx):
+        if ii is not None:
+            mqa.mla_decode_sparse(qq, kv, btt, sll, ii, case.scale, case.k_scale, out=oo, lse=ll,
+                                  num_kv_splits=splits, workspace=ws, kv_lora_rank=R, stream=stream)
+        elif case.kind == "mla" and q_len > 1:  # rows are q_len x heads, token-major
             hh = H // q_len
             mqa.mla_decode_multi(qq.view(B, q_len, hh, D), kv, btt, sll, case.scale, case.k_scale,
                                  out=oo.view(B, q_len, hh, R), lse=ll.view(B, q_len, hh),
@@ -361,6 +389,8 @@ def run_ours(args):
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     q_d, bt_d, sl_d = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(sl)
+    idx_h = torch.from_numpy(idx_np).pin_memory() if idx_np is not None else None
+    idx_d = torch.empty_like(idx) if idx is not None else None
     e2e_steps = max(3, min(args.steps, 200))
     es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
     ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
@@ -372,14 +402,16 @@ def run_ours(args):
         q_d.copy_(q_h, non_blocking=True)
         bt_d.copy_(bt_h, non_blocking=True)
         sl_d.copy_(sl_h, non_blocking=True)
-        call(q_d, bt_d, sl_d, out, lse)
+        if idx_d is not None:
+            idx_d.copy_(idx_h, non_blocking=True)
+        call(q_d, bt_d, sl_d, out, lse, idx_d)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
         if j >= 0:
             ee[j].record(stream)
         stream.synchronize()
     e2e_ms = sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e2e_steps
-    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4
+    h2d = q_h.numel() * 2 + bt_h.numel() * 4 + sl_h.numel() * 4 + (idx_h.numel() * 4 if idx_h is not None else 0)
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
     # ---- max over ranks
@@ -431,7 +463,8 @@ def run_ours(args):
         "roofline": roof, "cpu_baseline": cpu,
         "e2e": {"value": round(job_throughput_gbs(world, st["kv_bytes"], e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "per step: q, block_table, seq_lens host->device and out, lse device->host "
+                "note": "per step: q, block_table, seq_lens (and sparse indices) host->device and out, "
+                        "lse device->host "
                         "(pinned host buffers); the KV cache is decode state resident in HBM"},
         "gpu_launches": args.steps * launches_per_call,
         "clocks": sampler.summary(),

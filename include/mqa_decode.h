@@ -166,6 +166,39 @@ mqa_status mla_decode_multi(const void* q, const void* kv_cache, const int32_t* 
                             int num_kv_splits, void* workspace, size_t workspace_bytes, int* device_status,
                             void* stream);
 
+/* Sparse (top-k) MLA decode.  The tutorial page (lshu.cn/news/265860) §13
+ * describes it: an indexer picks, per request, topk key positions (2048 in
+ * its example, at head size 576), and the query attends those positions
+ * only, each found in the paged cache through the block table, so one query
+ * row's logits are [1, 576] x [576, topk] instead of a walk over the whole
+ * context.
+ *
+ *   indices  int32 [batch, topk] (row-major, 4-byte aligned): logical token
+ *            positions of request b.  An entry selects position p when
+ *            0 <= p < seq_lens[b]; anything else (the usual -1 padding, or a
+ *            position at or past the end) selects nothing.  The order of
+ *            entries does not matter; a position listed twice counts twice.
+ *            A request that selects nothing gets out = 0, lse = -inf.
+ *   topk     entries per request, 1 .. 2^24.
+ *   seq_lens int32 [batch]: cached tokens per request (bounds the valid
+ *            positions; the work done is topk entries per request whatever
+ *            the length).
+ *   num_heads 1 .. 128 (query heads of the request, all sharing the cache).
+ *   workspace: mla_decode_workspace_bytes(batch, num_heads, kv_lora_rank,
+ *   num_kv_splits) bytes; splits divide the topk entries (mqa_num_kv_splits
+ *   with max_seq_len = topk is a good choice).
+ *   A selected position whose page has no valid block id (outside
+ *   [0, num_blocks)), or that lies at or past max_blocks * page_size while
+ *   below seq_lens[b], is skipped and MQA_ERR_DEVICE_CHECK is written to
+ *   *device_status.  Other arguments, results and errors are those of
+ *   mla_decode (q, out, lse, dtypes, scale, k_scale, head sizes). */
+mqa_status mla_decode_sparse(const void* q, const void* kv_cache, const int32_t* block_table,
+                             const int32_t* seq_lens, const int32_t* indices, float scale, float k_scale,
+                             void* out, float* lse, int batch, int num_heads, int head_size,
+                             int kv_lora_rank, int num_blocks, int page_size, int max_blocks, int topk,
+                             mqa_kv_dtype kv_dtype, int num_kv_splits, void* workspace,
+                             size_t workspace_bytes, int* device_status, void* stream);
+
 /* Size of the library-owned scratch array used by mla_decode_noalloc. */
 #define MQA_NOALLOC_SCRATCH_BYTES (64u << 20)
 

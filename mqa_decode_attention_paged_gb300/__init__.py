@@ -16,8 +16,8 @@ def _load_binding():
 
 def __getattr__(name):
     exported = {
-        "mla_decode", "mla_decode_multi", "gqa_paged_decode", "num_kv_splits", "mla_decode_workspace_bytes",
-        "gqa_paged_decode_workspace_bytes", "status_string", "abi_version", "device_sm_count",
+        "mla_decode", "mla_decode_multi", "mla_decode_sparse", "gqa_paged_decode", "num_kv_splits",
+        "mla_decode_workspace_bytes", "gqa_paged_decode_workspace_bytes", "status_string", "abi_version", "device_sm_count",
         "MqaError",
     }
     if name in exported:

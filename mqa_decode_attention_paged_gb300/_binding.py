@@ -62,6 +62,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_decode.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
     lib.mla_decode_multi.restype = I
     lib.mla_decode_multi.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
+    lib.mla_decode_sparse.restype = I
+    lib.mla_decode_sparse.argtypes = [P, P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
     lib.mla_decode_noalloc.restype = I
     lib.mla_decode_noalloc.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, P]
     lib.gqa_paged_decode.restype = I
@@ -175,6 +177,39 @@ def mla_decode_multi(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *, 
                               _ptr(device_status), _stream(stream))
     if rc != OK:
         raise MqaError(rc, "mla_decode_multi")
+    return out, lse
+
+
+def mla_decode_sparse(q, kv_cache, block_table, seq_lens, indices, scale, k_scale=1.0, *, out=None,
+                      lse=None, num_kv_splits=1, workspace=None, kv_lora_rank=None, kv_dtype=None,
+                      device_status=None, stream=None, return_lse=True):
+    """Sparse (top-k) MLA decode through the C ABI.  q [B, H, D] bf16, indices [B, topk]
+    int32 logical positions (entries outside [0, seq_lens[b]) select nothing); returns
+    out [B, H, R] bf16 and lse [B, H] fp32."""
+    import torch
+    B, H, D = q.shape
+    nb, page, D2 = kv_cache.shape
+    if D2 != D:
+        raise ValueError("q and kv_cache head sizes differ")
+    if indices.dim() != 2 or indices.shape[0] != B or indices.dtype != torch.int32:
+        raise ValueError("indices must be int32 [batch, topk]")
+    topk = indices.shape[1]
+    R = (D - 64) if kv_lora_rank is None else int(kv_lora_rank)
+    code = _kv_code(kv_cache, kv_dtype)
+    if out is None:
+        out = torch.empty((B, H, R), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    need = mla_decode_workspace_bytes(B, H, R, num_kv_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.mla_decode_sparse(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), _ptr(indices),
+                               float(scale), float(k_scale), _ptr(out), _ptr(lse), B, H, D, R, nb, page,
+                               block_table.shape[1], topk, code, int(num_kv_splits), _ptr(workspace),
+                               ws_bytes, _ptr(device_status), _stream(stream))
+    if rc != OK:
+        raise MqaError(rc, "mla_decode_sparse")
     return out, lse
 
 

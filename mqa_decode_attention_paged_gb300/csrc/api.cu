@@ -471,6 +471,92 @@ mqa_status mla_decode_multi(const void* q, const void* kv_cache, const int32_t* 
                            kv_dtype, num_kv_splits, workspace, workspace_bytes, device_status, stream, q_len);
 }
 
+mqa_status mla_decode_sparse(const void* q, const void* kv_cache, const int32_t* block_table,
+                             const int32_t* seq_lens, const int32_t* indices, float scale, float k_scale,
+                             void* out, float* lse, int batch, int num_heads, int head_size,
+                             int kv_lora_rank, int num_blocks, int page_size, int max_blocks, int topk,
+                             mqa_kv_dtype kv_dtype, int num_kv_splits, void* workspace,
+                             size_t workspace_bytes, int* device_status, void* stream) {
+    if (!q || !kv_cache || !block_table || !seq_lens || !indices || !out) return MQA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4) || !aligned(indices, 4) || (lse && !aligned(lse, 4)) ||
+        (device_status && !aligned(device_status, 4)))
+        return MQA_ERR_INVALID_ARG;
+    if (batch < 1 || num_heads < 1 || num_blocks < 1 || max_blocks < 1 || page_size < 1 || num_kv_splits < 1 ||
+        topk < 1)
+        return MQA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !std::isfinite(k_scale)) return MQA_ERR_INVALID_ARG;
+    if (!((head_size == 576 && kv_lora_rank == 512) || (head_size == 320 && kv_lora_rank == 256)))
+        return MQA_ERR_UNSUPPORTED;
+    // rows are gathered one by one: any page size works
+    if (kv_dtype != MQA_KV_BF16 && kv_dtype != MQA_KV_FP8_E4M3) return MQA_ERR_UNSUPPORTED;
+    if (num_heads > 128 || batch > kMaxBatch || topk > (1 << 24)) return MQA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(max_blocks) * page_size > INT32_MAX ||
+        static_cast<long long>(num_blocks) * page_size > INT32_MAX)
+        return MQA_ERR_UNSUPPORTED;
+
+    const size_t need = mla_decode_workspace_bytes(batch, num_heads, kv_lora_rank, num_kv_splits);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return MQA_ERR_WORKSPACE_TOO_SMALL;
+    if (need > 0 && !aligned(workspace, 16)) return MQA_ERR_INVALID_ARG;
+
+    const int sms = sm_count_current();
+    if (sms < 1) return MQA_ERR_CUDA;
+    const bool fp8 = kv_dtype == MQA_KV_FP8_E4M3;
+    const int groups = (num_heads + 15) / 16;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    // The warp-MMA kernel with an index-driven gather: its plan walks the
+    // topk entries of every request in "pages" of one pipeline tile (every
+    // request has length topk); each 16-head group gathers the rows itself.
+    mqa::MlaArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.kv = static_cast<const uint8_t*>(kv_cache);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.indices = indices;
+    a.topk = topk;
+    a.cache_page = page_size;
+    a.bt_stride = max_blocks;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    const size_t slots = static_cast<size_t>(batch) * num_kv_splits;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = need > 0 ? a.ws_o + slots * num_heads * kv_lora_rank : nullptr;
+    a.status = device_status;
+    const float ks = fp8 ? k_scale : 1.0f;
+    a.sl2 = scale * ks * mqa::kLog2e;
+    a.out_scale = ks;
+    a.H = num_heads;
+    a.q_len = 1;
+    a.heads = num_heads;
+    a.num_blocks = num_blocks;
+    const int tile = mqa::mla_mma_sparse_tile(fp8);
+    a.plan.batch = batch;
+    a.plan.page = tile;
+    a.plan.max_blocks = (topk + tile - 1) / tile;
+    a.plan.fixed_len = topk;
+    a.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
+    a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms / groups);
+
+    if (cudaError_t e = mqa::mla_mma_stage1(a, head_size, fp8, a.plan.units * groups, st); e != cudaSuccess)
+        return cuda_fail(e);
+    if (!a.plan.per_seq) {
+        mqa::MergeArgs m{};
+        m.ws_o = a.ws_o;
+        m.ws_lse = a.ws_lse;
+        m.seq_lens = seq_lens;
+        m.out = a.out;
+        m.lse = lse;
+        m.status = device_status;
+        m.out_scale = 1.0f;  // stage-1 partials already carry k_scale
+        m.H = num_heads;
+        m.R = kv_lora_rank;
+        m.plan = a.plan;
+        if (cudaError_t e = mqa::lse_merge(m, st); e != cudaSuccess) return cuda_fail(e);
+    }
+    return MQA_OK;
+}
+
 mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* block_table,
                             const int32_t* seq_lens, float scale, float k_scale, float v_scale,
                             void* out, float* lse, int batch, int num_q_heads, int num_kv_heads,

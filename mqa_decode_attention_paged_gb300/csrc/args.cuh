@@ -37,6 +37,13 @@ struct MlaArgs {
     // (token-major); row r (token i = r / heads) sees the first
     // len - q_len + i + 1 tokens of its request.  q_len = 1: plain decode.
     int q_len, heads;
+    // sparse decode (indices != null): request b attends the positions
+    // indices[b * topk + e]; the plan runs over the topk entries in "pages"
+    // of one pipeline tile (plan.fixed_len = topk) and a selected position's
+    // row is found through block_table (row stride bt_stride) with pages of
+    // cache_page tokens
+    const int32_t* indices;
+    int topk, cache_page, bt_stride;
     Plan plan;
 };
 
@@ -98,6 +105,8 @@ struct MergeArgs {
 cudaError_t mla_mma_stage1(const MlaArgs& a, int D, bool fp8, int grid, cudaStream_t stream);
 size_t mla_mma_smem_bytes(int D, bool fp8, int batch);
 int mla_mma_tile();
+// entries per pipeline tile of the sparse (index-gather) kernel
+int mla_mma_sparse_tile(bool fp8);
 cudaError_t gqa_mma_stage1(const GqaArgs& a, int D, int grid, cudaStream_t stream);
 cudaError_t mla_tc_stage1(const MlaTcArgs& a, int D, bool fp8, int clusters, cudaStream_t stream);
 int mla_tc_tile();

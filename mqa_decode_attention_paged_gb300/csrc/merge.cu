@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps, G == 4 ? 6 : 1) lse_merge_ke
     // stage-1 kernel's prefix (same clamping).
     int before = 0, total = 0;
     for (int i = lane; i < a.plan.batch; i += 32) {
-        const int n = clamp_len(a.seq_lens[i], a.plan.max_blocks, P, nullptr);
+        const int n = plan_len(a.plan, a.seq_lens, i, nullptr);
         const int pages = (n + P - 1) / P;
         total += pages;
         if (i < b) before += pages;
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps, G == 4 ? 6 : 1) lse_merge_ke
         before += __shfl_xor_sync(0xffffffffu, before, o);
         total += __shfl_xor_sync(0xffffffffu, total, o);
     }
-    const int n_b = (clamp_len(a.seq_lens[b], a.plan.max_blocks, P, nullptr) + P - 1) / P;
+    const int n_b = (plan_len(a.plan, a.seq_lens, b, nullptr) + P - 1) / P;
     const int R = a.R;
     const long long orow = (static_cast<long long>(b) * a.H + h) * R;
     const int col = q * kMergeCols + 4 * lane;  // first column of the lane's group k: col + 128 k

@@ -29,8 +29,11 @@ namespace mqa {
 // Shared-memory budget: everything but the staging ring is fixed, the ring
 // gets as many stages as fit (at most 8).
 
-template <int D, int R, bool FP8, int TILE>
+// SPARSE: the stage is filled by per-row bulk copies (unswizzled rows) and
+// turned into the swizzled operand tile by the consumers, as for e4m3
+template <int D, int R, bool FP8, int TILE, bool SPARSE = false>
 struct MlaMmaCfg {
+    static constexpr bool kStaged = FP8 || SPARSE;                 // operand tile built from the stage
     static constexpr int kHeads = 16;
     static constexpr int kTile = TILE;                         // tokens per stage
     static constexpr int kHalf = kTile / 2;                    // tokens per QK warp
@@ -53,7 +56,7 @@ struct MlaMmaCfg {
     static constexpr int kRedBytes = 4 * kHeads * kRedStride * 4;
     static constexpr int kPBytes = kHeads * kPStride * 2;
     static constexpr int kMiscBytes = kHeads * 4 + kHeads * 8 + 8 * 8 + 16 * 8 + 16;
-    static constexpr int kFixed = 1024 + (FP8 ? kOpBytes : 0) + kQBytes + kRedBytes + kPBytes + kMiscBytes +
+    static constexpr int kFixed = 1024 + (kStaged ? kOpBytes : 0) + kQBytes + kRedBytes + kPBytes + kMiscBytes +
                                   4 * (2 * kMaxBatchSmem + 1) + 1024;
     static constexpr int kStagesFit = (227 * 1024 - kFixed) / kStageBytes;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
@@ -61,7 +64,7 @@ struct MlaMmaCfg {
     static constexpr int align1k(int x) { return (x + 1023) & ~1023; }
     static constexpr int kOffStages = 0;
     static constexpr int kOffOp = align1k(kStages * kStageBytes);
-    static constexpr int kOffQ = kOffOp + (FP8 ? kOpBytes : 0);
+    static constexpr int kOffQ = kOffOp + (kStaged ? kOpBytes : 0);
     static constexpr int kOffRed = kOffQ + kQBytes;
     static constexpr int kOffP = kOffRed + kRedBytes;
     static constexpr int kOffAlpha = kOffP + kPBytes;
@@ -84,10 +87,10 @@ struct MlaMmaCfg {
 
 // MULTI: multi-token decode (per-row key limits); the plain-decode kernels
 // are compiled without that code
-template <int D, int R, bool FP8, int TILE, bool MULTI>
-__global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
+template <int D, int R, bool FP8, int TILE, bool MULTI, bool SPARSE>
+__global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 1)
     mla_decode_mma_kernel(const __grid_constant__ MlaArgs a) {
-    using C = MlaMmaCfg<D, R, FP8, TILE>;
+    using C = MlaMmaCfg<D, R, FP8, TILE, SPARSE>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned window: the 128-byte swizzle pattern is a function of
     // address bits 7..9.
@@ -116,7 +119,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
         }
         *abort_s = 0;
         fence_mbar_init();
-        prefetch_tmap(&a.tmap);
+        if constexpr (!SPARSE) prefetch_tmap(&a.tmap);
     }
     // Zero the staging ring (and the widened operand tile) once so that rows
     // never written by a copy hold finite values.
@@ -133,6 +136,104 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
     if (warp == C::kConsumerWarps) {
         // ------------------------------------------------------------ producer
         const uint64_t pol = l2_policy_evict_first();
+        if constexpr (SPARSE) {
+            // Sparse decode: a tile is kTile entries of the request's index
+            // list; lane l gathers rows l, l + 32, each whole cache row by one
+            // bulk copy (rows are D * elt bytes: 16-byte aligned) into the
+            // unswizzled stage.  The rows of the next tile are looked up
+            // (index, then block table) one tile ahead.  Entries outside
+            // [0, seq_len) select nothing; bad block ids are reported.
+            static_assert(C::kTile % 32 == 0, "whole warps of rows");
+            constexpr int kPer = C::kTile / 32;
+            constexpr int kRowBytes = D * (FP8 ? 1 : 2);
+            TileCursor cur;
+            cur.init(a.plan, cum, T, unit, C::kTile);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued[C::kStages];
+            for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
+            auto lookup = [&](const TileCursor& tc, const uint8_t* (&src)[kPer], bool (&val)[kPer]) {
+                const int b = tc.pc.b;
+                const long long cap = static_cast<long long>(a.bt_stride) * a.cache_page;
+                const int n = __ldg(a.seq_lens + b);
+                if (n < 0 && lane == 0) report(a.status, MQA_ERR_DEVICE_CHECK);
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const int e = tc.t0 + lane + 32 * k;
+                    bool v = e < tc.tok_end;
+                    const int pos = v ? __ldg(a.indices + static_cast<long long>(b) * a.topk + e) : -1;
+                    v = v && pos >= 0 && pos < n;
+                    if (v && pos >= cap) {
+                        // below the length but beyond what the block table maps
+                        report(a.status, MQA_ERR_DEVICE_CHECK);
+                        v = false;
+                    }
+                    int blk = 0;
+                    if (v) {
+                        blk = __ldg(a.block_table + static_cast<long long>(b) * a.bt_stride + pos / a.cache_page);
+                        if (blk < 0 || blk >= a.num_blocks) {
+                            report(a.status, MQA_ERR_DEVICE_CHECK);
+                            v = false;
+                        }
+                    }
+                    val[k] = v;
+                    src[k] = a.kv + (static_cast<long long>(v ? blk : 0) * a.cache_page + (v ? pos % a.cache_page : 0)) *
+                                        kRowBytes;
+                }
+            };
+            bool have = cur.next(a.plan, cum, lens, a.block_table);
+            const uint8_t* src[kPer];
+            bool val[kPer];
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                src[k] = a.kv;
+                val[k] = false;
+            }
+            if (have) lookup(cur, src, val);
+            while (have) {
+                const bool have_next = cur.next(a.plan, cum, lens, a.block_table);
+                const uint8_t* nsrc[kPer];
+                bool nval[kPer];
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    nsrc[k] = a.kv;
+                    nval[k] = false;
+                }
+                if (have_next) lookup(cur, nsrc, nval);
+                if (!mbar_wait(&empty[stage], phase ^ 1)) {
+                    report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+                    break;
+                }
+                uint8_t* dst = stages + stage * C::kStageBytes;
+                uint64_t vmask = 0;
+#pragma unroll
+                for (int k = 0; k < kPer; ++k)
+                    vmask |= static_cast<uint64_t>(__ballot_sync(0xffffffffu, val[k])) << (32 * k);
+                if (lane == 0) {
+                    mask_s[stage] = vmask;
+                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(__popcll(vmask)) * kRowBytes);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < kPer; ++k)
+                    if (val[k]) bulk_g2s(dst + (lane + 32 * k) * kRowBytes, src[k], kRowBytes, &full[stage], pol);
+                issued[stage] = static_cast<int>(phase);
+                if (++stage == C::kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+                have = have_next;
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    src[k] = nsrc[k];
+                    val[k] = nval[k];
+                }
+            }
+            for (int s = 0; s < C::kStages; ++s)
+                if (issued[s] >= 0 && !mbar_wait(&full[s], static_cast<uint32_t>(issued[s])))
+                    report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+            return;
+        }
         TileCursor cur;
         cur.init(a.plan, cum, T, unit, C::kTile);
         int stage = 0;
@@ -279,11 +380,19 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
             uint8_t* op = stage_buf;
             const uint64_t vmask = mask_s[stage];
             bool zeroed = false;
-            if constexpr (FP8) {
-                // Widen the e4m3 tile to bf16 (exact) into the swizzled operand tile.
+            if constexpr (C::kStaged) {
+                // Widen the e4m3 tile to bf16 (exact), or copy the gathered
+                // bf16 rows, into the swizzled operand tile.
                 op = smem + C::kOffOp;
                 named_bar_sync(3, C::kConsumers);  // previous tile's P.V is done
-                if (ok) {
+                if (ok && !FP8) {
+                    constexpr int kChunks = C::kTile * (D / 8);  // 8 bf16 (16 bytes) each
+                    for (int i = t; i < kChunks; i += C::kConsumers) {
+                        const int r = i / (D / 8), cc = i % (D / 8);
+                        *reinterpret_cast<uint4*>(op + swz_rows(r, 8 * cc, C::kPanels)) =
+                            *reinterpret_cast<const uint4*>(stage_buf + r * D * 2 + cc * 16);
+                    }
+                } else if (ok) {
                     constexpr int kChunks = C::kTile * (D / 16);
                     for (int i = t; i < kChunks; i += C::kConsumers) {
                         const int r = i / (D / 16), cc = i % (D / 16);
@@ -438,7 +547,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
                     }
                 }
             }
-            if constexpr (!FP8) {
+            if constexpr (!C::kStaged) {
                 // the stage goes back to the tensor copies (async proxy)
                 if (zeroed) fence_proxy_async_smem();
                 __syncwarp();
@@ -505,23 +614,32 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE>::kThreads, 1)
 #ifndef MQA_MLA_TILE
 #define MQA_MLA_TILE 64
 #endif
-template <int D, bool FP8>
+template <int D, bool FP8, bool SPARSE = false>
 struct MlaTile {
-    static constexpr int value = MQA_MLA_TILE;
+    // a gathered bf16 tile also needs its swizzled copy: 32-row tiles keep
+    // three stages in shared memory
+    static constexpr int value = (SPARSE && !FP8) ? 32 : MQA_MLA_TILE;
 };
 
-template <int D, int R, bool FP8>
-static cudaError_t launch_mla_mma(const MlaArgs& a, int grid, cudaStream_t stream) {
-    constexpr int kTile = MlaTile<D, FP8>::value;
-    using C = MlaMmaCfg<D, R, FP8, kTile>;
+template <int D, int R, bool FP8, bool MULTI, bool SPARSE>
+static cudaError_t launch_form(const MlaArgs& a, int grid, cudaStream_t stream) {
+    constexpr int kTile = MlaTile<D, FP8, SPARSE>::value;
+    using C = MlaMmaCfg<D, R, FP8, kTile, SPARSE>;
     const size_t smem = C::smem_bytes(a.plan.batch);
-    auto kern = a.q_len > 1 ? mla_decode_mma_kernel<D, R, FP8, kTile, true> : mla_decode_mma_kernel<D, R, FP8, kTile, false>;
+    auto kern = mla_decode_mma_kernel<D, R, FP8, kTile, MULTI, SPARSE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     e = launch_with_pdl(kern, dim3(grid), dim3(C::kThreads), smem, stream, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int D, int R, bool FP8>
+static cudaError_t launch_mla_mma(const MlaArgs& a, int grid, cudaStream_t stream) {
+    if (a.indices) return launch_form<D, R, FP8, false, true>(a, grid, stream);
+    if (a.q_len > 1) return launch_form<D, R, FP8, true, false>(a, grid, stream);
+    return launch_form<D, R, FP8, false, false>(a, grid, stream);
 }
 
 cudaError_t mla_mma_stage1(const MlaArgs& a, int D, bool fp8, int grid, cudaStream_t stream) {
@@ -532,6 +650,10 @@ cudaError_t mla_mma_stage1(const MlaArgs& a, int D, bool fp8, int grid, cudaStre
 }
 
 int mla_mma_tile() { return MQA_MLA_TILE; }
+
+int mla_mma_sparse_tile(bool fp8) {
+    return fp8 ? MlaTile<576, true, true>::value : MlaTile<576, false, true>::value;
+}
 
 size_t mla_mma_smem_bytes(int D, bool fp8, int batch) {
     if (D == 576) return fp8 ? MlaMmaCfg<576, 512, true, MQA_MLA_TILE>::smem_bytes(batch)

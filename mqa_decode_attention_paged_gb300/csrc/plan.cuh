@@ -29,7 +29,14 @@ struct Plan {
     int max_blocks;
     int units;
     int per_seq;
+    int fixed_len;  // > 0: every request has this length (sparse decode: its index list)
 };
+
+// The length the plan gives request b: fixed_len, or its clamped seq_len.
+__device__ __forceinline__ int clamp_len(int n, int max_blocks, int page, int* status);
+__device__ __forceinline__ int plan_len(const Plan& p, const int32_t* seq_lens, int b, int* status) {
+    return p.fixed_len > 0 ? p.fixed_len : clamp_len(seq_lens[b], p.max_blocks, p.page, status);
+}
 
 // Clamp a request length to [0, max_blocks * page]; report out-of-range values.
 __device__ __forceinline__ int clamp_len(int n, int max_blocks, int page, int* status) {
@@ -51,7 +58,7 @@ __device__ __forceinline__ int clamp_len(int n, int max_blocks, int page, int* s
 __device__ __forceinline__ int build_cum(const Plan& p, const int32_t* __restrict__ seq_lens,
                                          int* cum, int* lens, int* status) {
     for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
-        const int n = clamp_len(seq_lens[i], p.max_blocks, p.page, status);
+        const int n = plan_len(p, seq_lens, i, status);
         lens[i] = n;
         cum[i + 1] = (n + p.page - 1) / p.page;
     }

@@ -26,6 +26,10 @@ library is measured on):
                seq_lens [131072, 98304, 65536, 120000].
   gqa          B=256, Hq=32, Hkv=8, D=128, page 16, bf16, seq_lens
                ceil(exp(N(ln 2048, 1))) clipped to [1, 16384].
+  mla_mtp      the mla_v2lite batch with 8 query tokens x 16 heads per request.
+  mla_sparse   B=64, H=16, D=576, page 64, bf16, seq_lens uniform in
+               [16384, 40960], 2048 distinct random positions per request
+               (meta["indices"], drawn with seed + 7919).
 All q and KV values are N(0, 1) (before the fp8 division), from
 numpy.random.default_rng(seed); MLA scale is 1/sqrt(192), GQA 1/sqrt(128).
 """
@@ -149,6 +153,21 @@ def _fill_blocks(rng, kv: np.ndarray, ids: np.ndarray, kv_dtype: str, k_scale: f
             kv[sel] = to_e4m3_codes(x)
 
 
+def draw_topk_indices(rng: np.random.Generator, seq_lens: np.ndarray, topk: int,
+                      pad: float = 0.0) -> np.ndarray:
+    """Sparse-decode index lists, int32 [B, topk]: min(topk, seq_len) distinct
+    positions of each request in random order, -1 in the remaining entries,
+    and a share `pad` of all entries replaced by -1."""
+    out = np.full((len(seq_lens), topk), -1, dtype=np.int32)
+    for b, n in enumerate(seq_lens):
+        k = min(topk, int(n))
+        if k > 0:
+            out[b, :k] = rng.choice(int(n), size=k, replace=False)
+        if pad > 0:
+            out[b, rng.random(topk) < pad] = -1
+    return out
+
+
 def make_mla_case(seq_lens, B=None, H=16, D=576, R=None, page=16, kv_dtype="bf16",
                   k_scale=1.0, pool_factor=1.0, seed=0, scale=None, name="",
                   extra_cols=0) -> PagedCase:
@@ -202,6 +221,11 @@ WORKLOADS = {
     # [B, q_len, H, D], stored here as its [B, q_len * H, D] view)
     "mla_mtp": dict(kind="mla", B=64, seq_lens=("uniform", 1024, 8192), H=128, D=576, page=64,
                     kv_dtype="bf16", pool_factor=1.5, seed=1006, q_len=8),
+    # sparse (top-k) decode: 2048 selected positions per request out of
+    # 16k..40k-token contexts, 16 heads (128 heads split 8 ways); the index
+    # lists are in case.meta["indices"]
+    "mla_sparse": dict(kind="mla", B=64, seq_lens=("uniform", 16384, 40960), H=16, D=576, page=64,
+                       kv_dtype="bf16", seed=1007, topk=2048),
 }
 
 
@@ -211,10 +235,14 @@ def workload(name: str, **overrides) -> PagedCase:
     spec.update(overrides)
     kind = spec.pop("kind")
     q_len = spec.pop("q_len", 1)
+    topk = spec.pop("topk", 0)
     spec.setdefault("name", name)
     if kind == "mla":
         case = make_mla_case(**spec)
         case.meta["q_len"] = q_len  # query rows are q_len x heads, token-major
+        if topk:
+            rng = np.random.default_rng(int(spec["seed"]) + 7919)
+            case.meta["indices"] = draw_topk_indices(rng, case.seq_lens, topk)
         return case
     return make_gqa_case(**spec)
 

@@ -30,7 +30,7 @@ def _declared_functions():
 
 def test_header_symbols_are_exported():
     names = _declared_functions()
-    assert {"mla_decode", "mla_decode_multi", "gqa_paged_decode", "mqa_num_kv_splits", "mla_decode_workspace_bytes",
+    assert {"mla_decode", "mla_decode_multi", "mla_decode_sparse", "gqa_paged_decode", "mqa_num_kv_splits", "mla_decode_workspace_bytes",
             "gqa_paged_decode_workspace_bytes", "mqa_status_string", "mqa_abi_version",
             "mqa_device_sm_count"} <= set(names)
     lib = ctypes.CDLL(mqa.LIB_PATH)
@@ -93,6 +93,37 @@ def _mla_multi(**kw):
 ])
 def test_mla_multi_validation(kw, code):
     assert _mla_multi(**kw) == code
+
+
+def _mla_sparse(**kw):
+    a = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, idx=FAKE, scale=0.07, k_scale=1.0, out=FAKE, lse=None,
+             B=2, H=16, D=576, R=512, nb=10, P=16, maxb=8, topk=2048, kvd=0, S=1, ws=None, wsb=0)
+    a.update(kw)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)  # noqa: E731
+    return mqa.lib.mla_decode_sparse(P(a["q"]), P(a["kv"]), P(a["bt"]), P(a["sl"]), P(a["idx"]), a["scale"],
+                                     a["k_scale"], P(a["out"]), P(a["lse"]), a["B"], a["H"], a["D"], a["R"],
+                                     a["nb"], a["P"], a["maxb"], a["topk"], a["kvd"], a["S"], P(a["ws"]),
+                                     a["wsb"], None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(idx=None), mqa.ERR_INVALID_ARG),
+    (dict(idx=FAKE + 2), mqa.ERR_INVALID_ARG),         # indices are int32
+    (dict(topk=0), mqa.ERR_INVALID_ARG),
+    (dict(topk=(1 << 24) + 1), mqa.ERR_UNSUPPORTED),
+    (dict(q=None), mqa.ERR_INVALID_ARG),
+    (dict(bt=None), mqa.ERR_INVALID_ARG),
+    (dict(H=0), mqa.ERR_INVALID_ARG),
+    (dict(H=129), mqa.ERR_UNSUPPORTED),
+    (dict(B=4097), mqa.ERR_UNSUPPORTED),
+    (dict(D=512, R=448), mqa.ERR_UNSUPPORTED),
+    (dict(kvd=7), mqa.ERR_UNSUPPORTED),
+    (dict(scale=float("inf")), mqa.ERR_INVALID_ARG),
+    (dict(S=4, ws=None), mqa.ERR_WORKSPACE_TOO_SMALL),
+    (dict(S=4, ws=FAKE, wsb=mqa.mla_decode_workspace_bytes(2, 16, 512, 4) - 1), mqa.ERR_WORKSPACE_TOO_SMALL),
+])
+def test_mla_sparse_validation(kw, code):
+    assert _mla_sparse(**kw) == code
 
 
 def _gqa(**kw):
