@@ -50,11 +50,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 MMA_FILES = ("mla_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
 TC_FILES = ("mla_tc.cu", "tc_ptx.cuh", "common.cuh", "plan.cuh", "args.cuh")
 NCU_TRAFFIC = {
-    "mla_v2lite": {"files": MMA_FILES, "src_sha": "b12888e065c4399c", "splits": 16, "bytes": 329834496 + 3723520,
+    "mla_v2lite": {"files": MMA_FILES, "src_sha": "8b3793aae17c641a", "splits": 16, "bytes": 329795584 + 3738368,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64>"},
-    "mla_longctx": {"files": TC_FILES, "src_sha": "3a3417efce472d21", "splits": 256, "bytes": 485191168 + 4390144,
+    "mla_longctx": {"files": TC_FILES, "src_sha": "db7d88cc3b68ce52", "splits": 256, "bytes": 485207808 + 4084992,
                     "kernel": "mla_decode_tc_kernel<576,512,0>"},
-    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "3a3417efce472d21", "splits": 64, "bytes": 1423319040 + 25654784,
+    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "db7d88cc3b68ce52", "splits": 64, "bytes": 1423465728 + 25308416,
                    "kernel": "mla_decode_tc_kernel<576,512,1>"},
 }
 
