@@ -9,7 +9,11 @@ CPU oracle consume its arrays unchanged.
 Encodings (the same bytes the C-ABI takes):
   * q            uint16 bf16 bit patterns, [B, H, D]
   * MLA cache    [num_blocks, page, D], uint16 (bf16) or uint8 (e4m3 codes)
-  * GQA cache    [num_blocks, 2, page, Hkv, D], same element encodings
+  * GQA cache    [num_blocks, 2, page, Hkv, D], same element encodings; or,
+                 per-token-head quantised ("fp8_e4m3_pth", "int8_pth"), uint8
+                 [num_blocks, 2, page, Hkv, D + 4]: each (token, KV head) row
+                 holds D codes then its scale (little-endian float32),
+                 scale = max|row| / 448 (e4m3) or / 127 (int8)
   * block_table  int32 [B, max_blocks]; entries past a sequence's last page = -1
   * seq_lens     int32 [B]
 
@@ -26,6 +30,8 @@ library is measured on):
                seq_lens [131072, 98304, 65536, 120000].
   gqa          B=256, Hq=32, Hkv=8, D=128, page 16, bf16, seq_lens
                ceil(exp(N(ln 2048, 1))) clipped to [1, 16384].
+  gqa_fp8_pth  the gqa batch with a per-token-head e4m3 cache.
+  gqa_int8_pth the gqa batch with a per-token-head int8 cache.
   mla_mtp      the mla_v2lite batch with 8 query tokens x 16 heads per request.
   mla_sparse   B=64, H=16, D=576, page 64, bf16, seq_lens uniform in
                [16384, 40960], 2048 distinct random positions per request
@@ -153,6 +159,41 @@ def _fill_blocks(rng, kv: np.ndarray, ids: np.ndarray, kv_dtype: str, k_scale: f
             kv[sel] = to_e4m3_codes(x)
 
 
+# Per-token-head quantised GQA caches: code range each row is scaled into.
+PTH_DTYPES = {"fp8_e4m3_pth": E4M3_MAX, "int8_pth": 127.0}
+
+
+def encode_pth_rows(x: np.ndarray, kv_dtype: str) -> np.ndarray:
+    """Quantise rows x[..., D] (float32) per row: scale = max|x| / code range
+    (1 for an all-zero row), codes = x / scale encoded as e4m3 (torch's cast)
+    or as int8 (round half to even, clipped to +-127); returns uint8
+    [..., D + 4]: the D codes followed by the scale as little-endian binary32."""
+    top = PTH_DTYPES[kv_dtype]
+    amax = np.abs(x).max(axis=-1, keepdims=True)
+    sc = np.where(amax > 0, amax / np.float32(top), np.float32(1.0)).astype(np.float32)
+    y = x / sc
+    if kv_dtype == "fp8_e4m3_pth":
+        codes = to_e4m3_codes(y)
+    else:
+        codes = np.clip(np.rint(y), -127, 127).astype(np.int8).view(np.uint8)
+    out = np.empty(x.shape[:-1] + (x.shape[-1] + 4,), dtype=np.uint8)
+    out[..., :-4] = codes
+    out[..., -4:] = sc.astype("<f4").view(np.uint8).reshape(x.shape[:-1] + (4,))
+    return out
+
+
+def _fill_blocks_pth(rng, kv: np.ndarray, ids: np.ndarray, kv_dtype: str, chunk_elems: int = 1 << 26):
+    """Draw N(0,1) rows for the used blocks `ids` and quantise each (token, KV
+    head) row of each plane with its own scale."""
+    shape = kv.shape[1:-1] + (kv.shape[-1] - 4,)
+    per_block = int(np.prod(shape))
+    step = max(1, chunk_elems // max(per_block, 1))
+    for i in range(0, len(ids), step):
+        sel = ids[i:i + step]
+        x = rng.standard_normal(size=(len(sel),) + shape, dtype=np.float32)
+        kv[sel] = encode_pth_rows(x, kv_dtype)
+
+
 def draw_topk_indices(rng: np.random.Generator, seq_lens: np.ndarray, topk: int,
                       pad: float = 0.0) -> np.ndarray:
     """Sparse-decode index lists, int32 [B, topk]: min(topk, seq_len) distinct
@@ -197,6 +238,11 @@ def make_gqa_case(seq_lens, B=None, Hq=32, Hkv=8, D=128, page=16, kv_dtype="bf16
     scale = 1.0 / math.sqrt(float(D)) if scale is None else scale
     table, nb, ids = build_block_table(rng, sl, page, pool_factor, extra_cols)
     q = to_bf16_bits(rng.standard_normal(size=(B, Hq, D), dtype=np.float32))
+    if kv_dtype in PTH_DTYPES:
+        kv = np.zeros((nb, 2, page, Hkv, D + 4), dtype=np.uint8)
+        _fill_blocks_pth(rng, kv, ids, kv_dtype)
+        return PagedCase("gqa", q, kv, table, sl, kv_dtype, float(scale), page=page, num_kv_heads=Hkv,
+                         kv_lora_rank=0, name=name)
     kv = np.zeros((nb, 2, page, Hkv, D), dtype=np.uint16 if kv_dtype == "bf16" else np.uint8)
     _fill_blocks(rng, kv, ids, kv_dtype, k_scale)
     return PagedCase("gqa", q, kv, table, sl, kv_dtype, float(scale),
@@ -216,6 +262,11 @@ WORKLOADS = {
                         page=64, kv_dtype="bf16", seed=1004),
     "gqa": dict(kind="gqa", B=256, seq_lens=("lognormal", 2048, 1.0, 16384), Hq=32, Hkv=8, D=128,
                 page=16, kv_dtype="bf16", seed=1005),
+    # per-token-head quantised GQA caches (same batch as "gqa", own seeds)
+    "gqa_fp8_pth": dict(kind="gqa", B=256, seq_lens=("lognormal", 2048, 1.0, 16384), Hq=32, Hkv=8, D=128,
+                        page=16, kv_dtype="fp8_e4m3_pth", seed=1008),
+    "gqa_int8_pth": dict(kind="gqa", B=256, seq_lens=("lognormal", 2048, 1.0, 16384), Hq=32, Hkv=8, D=128,
+                         page=16, kv_dtype="int8_pth", seed=1009),
     # multi-token decode (speculative verification): the V2-Lite-like batch
     # with 8 new positions per request, 16 heads -> 128 query rows (q is
     # [B, q_len, H, D], stored here as its [B, q_len * H, D] view)
@@ -253,6 +304,9 @@ def poison(case: PagedCase, table_fill: int = -1) -> PagedCase:
     block-table entry past a sequence's last page."""
     kv = case.kv.copy()
     nan = BF16_NAN if kv.dtype == np.uint16 else E4M3_NAN
+    if case.kv_dtype in PTH_DTYPES:
+        # codes 0x7F (NaN for e4m3, 127 for int8) and a NaN scale
+        nan = np.array([0x7F] * (kv.shape[-1] - 4) + [0x00, 0x00, 0xC0, 0x7F], dtype=np.uint8)
     used = np.zeros(case.num_blocks, dtype=bool)
     table = case.block_table.copy()
     P = case.page

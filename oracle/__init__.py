@@ -83,6 +83,9 @@ def _load():
         lib.oracle_mla_decode_sparse.argtypes = [P, P, I, P, P, P, I, D, D, P, P, I, I, I, I, I, I, I]
         lib.oracle_gqa_paged_decode.restype = I
         lib.oracle_gqa_paged_decode.argtypes = [P, P, I, P, P, D, D, D, P, P, I, I, I, I, I, I, I]
+        lib.oracle_gqa_paged_decode_pth.restype = I
+        lib.oracle_gqa_paged_decode_pth.argtypes = [P, P, I, P, P, D, P, P, I, I, I, I, I, I, I]
+        lib.oracle_int8_values.argtypes = [P, P, I64]
         _lib = lib
         return lib
 
@@ -225,8 +228,25 @@ def mla_decode_multi(q, kv, kv_dtype, block_table, seq_lens, scale, k_scale=1.0,
     return out, lse
 
 
+PTH_KINDS = {"fp8_e4m3_pth": 0, "int8_pth": 1}
+
+
+def int8_values(codes: np.ndarray) -> np.ndarray:
+    """Two's-complement values of int8 codes given as uint8."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_int8_values(_ptr(c), _ptr(out), c.size)
+    return out
+
+
 def gqa_paged_decode(q, kv, kv_dtype, block_table, seq_lens, scale, k_scale=1.0, v_scale=1.0):
-    """q [B,Hq,D] bf16 bits; kv [num_blocks, 2, P, Hkv, D]; returns (out [B,Hq,D], lse [B,Hq])."""
+    """q [B,Hq,D] bf16 bits; kv [num_blocks, 2, P, Hkv, D] (bf16 bits or e4m3
+    codes with per-tensor k_scale / v_scale), or, for kv_dtype "fp8_e4m3_pth"
+    / "int8_pth", uint8 [num_blocks, 2, P, Hkv, D + 4] rows of D codes plus
+    their inline fp32 scale (k_scale / v_scale unused); returns
+    (out [B,Hq,D], lse [B,Hq])."""
+    if kv_dtype in PTH_KINDS:
+        return _gqa_pth(q, kv, kv_dtype, block_table, seq_lens, scale)
     q = np.ascontiguousarray(q, dtype=np.uint16)
     kv = np.ascontiguousarray(kv)
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
@@ -241,6 +261,27 @@ def gqa_paged_decode(q, kv, kv_dtype, block_table, seq_lens, scale, k_scale=1.0,
     rc = _load().oracle_gqa_paged_decode(_ptr(q), _ptr(kv), code, _ptr(bt), _ptr(sl), float(scale),
                                          float(k_scale), float(v_scale), _ptr(out), _ptr(lse),
                                          B, Hq, Hkv, D, nb, P, bt.shape[1])
+    if rc != 0:
+        raise ValueError("oracle: bad block table or head counts")
+    return out, lse
+
+
+def _gqa_pth(q, kv, kv_dtype, block_table, seq_lens, scale):
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    kv = np.ascontiguousarray(kv)
+    if kv.dtype != np.uint8:
+        raise TypeError("per-token-head cache must be given as uint8 bytes")
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, D = q.shape
+    nb, two, P, Hkv, Dp = kv.shape
+    if two != 2 or Dp != D + 4:
+        raise ValueError("per-token-head cache must be [num_blocks, 2, page, num_kv_heads, head_size + 4]")
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.zeros((B, Hq), dtype=np.float64)
+    rc = _load().oracle_gqa_paged_decode_pth(_ptr(q), _ptr(kv), PTH_KINDS[kv_dtype], _ptr(bt), _ptr(sl),
+                                             float(scale), _ptr(out), _ptr(lse), B, Hq, Hkv, D, nb, P,
+                                             bt.shape[1])
     if rc != 0:
         raise ValueError("oracle: bad block table or head counts")
     return out, lse

@@ -54,6 +54,13 @@
  *   cache.  Source: "AttentionBackend" page (vllm-arch-zh, fr/attention/backend),
  *   section "Motivation de conception" (FlashAttention cache layout).
  *
+ *   Per-token-head quantised GQA cache (fp8_per_token_head /
+ *   int8_per_token_head): every (token, KV head) vector is stored as 8-bit
+ *   codes with its own scale kept inline, the head dimension padded to make
+ *   room for it.  Source: "Triton と MLA" page, 役割 and 設計動機
+ *   (supported_kv_cache_dtypes) and 主要ファイル (get_kv_cache_shape pads
+ *   head_dim for the inline scale in per_token_head modes).
+ *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - lse is the natural log of sum_t exp(s_t) of the SCALED logits s_t.
  *   - bf16 caches ignore k_scale (the page's "is_fp8 check is a no-op").
@@ -67,6 +74,10 @@
  *     new tokens, whose keys are already in the cache); a query that sees no
  *     key (kv_length < q_len - i) gives out = 0 and lse = -inf.
  *   - GQA query head h reads KV head h / (Hq / Hkv).
+ *   - per-token-head caches: a (token, KV head) row is D + 4 bytes, the D
+ *     codes followed by the row's scale as a little-endian IEEE binary32;
+ *     element value = scale * code, with the code read as OCP e4m3fn or as a
+ *     two's-complement int8.  K and V rows carry separate scales.
  *   - split s of a sequence with n tokens covers the page-aligned token range
  *     [s*L, min((s+1)*L, n)), L = ceil(ceil(n/page)/S) * page.
  *
@@ -513,4 +524,101 @@ int oracle_gqa_paged_decode(const uint16_t* q, const void* kv, int kv_dtype,
     tv.k_mult = kv_dtype == ORACLE_KV_FP8_E4M3 ? k_scale : 1.0;
     tv.v_mult = kv_dtype == ORACLE_KV_FP8_E4M3 ? v_scale : 1.0;
     return run_heads(&tv, q, seq_lens, scale, B, Hq, Hq / Hkv, D, out, lse, FORM_DIRECT, 0);
+}
+
+/* ---- per-token-head quantised GQA --------------------------------------- */
+
+enum { ORACLE_PTH_E4M3 = 0, ORACLE_PTH_INT8 = 1 };
+
+/* Two's-complement byte, without relying on the signedness of char. */
+static double int8_code_value(uint8_t c) { return c < 128 ? (double)c : (double)c - 256.0; }
+
+/* The inline scale of a row: the 4 bytes after its D codes, little-endian
+ * binary32. */
+static double pth_row_scale(const uint8_t* row, int D) {
+    uint32_t u = (uint32_t)row[D] | ((uint32_t)row[D + 1] << 8) | ((uint32_t)row[D + 2] << 16) |
+                 ((uint32_t)row[D + 3] << 24);
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Dequantised row: out[d] = scale * value(code[d]). */
+static void pth_row_values(const uint8_t* row, int D, int kind, double* out) {
+    double sc = pth_row_scale(row, D);
+    for (int d = 0; d < D; ++d)
+        out[d] = sc * (kind == ORACLE_PTH_INT8 ? int8_code_value(row[d]) : oracle_e4m3_value(row[d]));
+}
+
+void oracle_int8_values(const uint8_t* codes, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = int8_code_value(codes[i]);
+}
+
+/* q: bf16 bits [B, Hq, D]; kv: bytes [num_blocks, 2, P, Hkv, D + 4] (plane 0 =
+ * K, plane 1 = V, each row D codes + its scale); out: [B, Hq, D]; lse:
+ * [B, Hq].  The direct definition: K_t, V_t dequantised row by row,
+ * s_t = scale * <q, K_t>, lse = m + log sum exp(s_t - m),
+ * out = sum_t exp(s_t - lse) V_t. */
+int oracle_gqa_paged_decode_pth(const uint16_t* q, const uint8_t* kv, int kind,
+                                const int32_t* block_table, const int32_t* seq_lens, double scale,
+                                double* out, double* lse, int B, int Hq, int Hkv, int D,
+                                int num_blocks, int P, int max_blocks) {
+    if (Hkv <= 0 || Hq % Hkv != 0 || (kind != ORACLE_PTH_E4M3 && kind != ORACLE_PTH_INT8)) return -1;
+    const int group = Hq / Hkv;
+    const int64_t Dp = (int64_t)D + 4;
+    int failed = 0;
+    int64_t pairs = (int64_t)B * Hq;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int64_t bh = 0; bh < pairs; ++bh) {
+        int b = (int)(bh / Hq), h = (int)(bh % Hq), g = h / group;
+        int n = seq_lens[b];
+        double* o = out + bh * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (n <= 0) {
+            lse[bh] = -INFINITY;
+            continue;
+        }
+        if (((int64_t)n + P - 1) / P > max_blocks) {
+            failed = 1;
+            continue;
+        }
+        int bad = 0;
+        for (int64_t t = 0; t < n; t += P) {
+            int32_t blk = block_table[(int64_t)b * max_blocks + t / P];
+            if (blk < 0 || blk >= num_blocks) bad = 1;
+        }
+        if (bad) {
+            failed = 1;
+            continue;
+        }
+        double* qd = (double*)malloc(sizeof(double) * (size_t)D);
+        double* kd = (double*)malloc(sizeof(double) * (size_t)D);
+        double* s = (double*)malloc(sizeof(double) * (size_t)n);
+        for (int d = 0; d < D; ++d) qd[d] = oracle_bf16_value(q[bh * D + d]);
+        double m = -INFINITY;
+        for (int t = 0; t < n; ++t) {
+            int64_t blk = block_table[(int64_t)b * max_blocks + t / P];
+            const uint8_t* krow = kv + (((blk * 2 + 0) * P + t % P) * Hkv + g) * Dp;
+            pth_row_values(krow, D, kind, kd);
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d) acc += qd[d] * kd[d];
+            s[t] = scale * acc;
+            if (s[t] > m) m = s[t];
+        }
+        double sum = 0.0;
+        for (int t = 0; t < n; ++t) sum += exp(s[t] - m);
+        double L = m + log(sum);
+        for (int t = 0; t < n; ++t) {
+            int64_t blk = block_table[(int64_t)b * max_blocks + t / P];
+            const uint8_t* vrow = kv + (((blk * 2 + 1) * P + t % P) * Hkv + g) * Dp;
+            pth_row_values(vrow, D, kind, kd);
+            double w = exp(s[t] - L);
+            for (int d = 0; d < D; ++d) o[d] += w * kd[d];
+        }
+        lse[bh] = L;
+        free(qd);
+        free(kd);
+        free(s);
+    }
+    return failed ? -1 : 0;
 }
