@@ -49,6 +49,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # valid only while the sources that kernel is built from hash to `src_sha`.
 MMA_FILES = ("mla_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
 TC_FILES = ("mla_tc.cu", "tc_ptx.cuh", "common.cuh", "plan.cuh", "args.cuh")
+Q8_FILES = ("gqa_q8.cu", "gqa_q8.cuh", "common.cuh", "plan.cuh", "args.cuh")
 NCU_TRAFFIC = {
     "mla_v2lite": {"files": MMA_FILES, "src_sha": "8b3793aae17c641a", "splits": 16, "bytes": 329795584 + 3738368,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64>"},
@@ -56,6 +57,10 @@ NCU_TRAFFIC = {
                     "kernel": "mla_decode_tc_kernel<576,512,0>"},
     "mla_v3_fp8": {"files": TC_FILES, "src_sha": "db7d88cc3b68ce52", "splits": 64, "bytes": 1423465728 + 25308416,
                    "kernel": "mla_decode_tc_kernel<576,512,1>"},
+    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "e82ed99867428332", "splits": 32, "bytes": 1538930176 + 4318720,
+                    "kernel": "gqa_decode_q8_kernel<128,2>"},
+    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "e82ed99867428332", "splits": 32, "bytes": 1693782016 + 4549376,
+                     "kernel": "gqa_decode_q8_kernel<128,3>"},
 }
 
 
@@ -96,7 +101,9 @@ def workload_stats(case, splits):
         out_w = R
     else:
         Hkv = case.num_kv_heads
-        kv_bytes = tokens * 2 * Hkv * D * elt
+        # per-token-head rows carry their 4-byte scale after the codes
+        row = D + 4 if case.kv_dtype in ("fp8_e4m3_pth", "int8_pth") else D
+        kv_bytes = tokens * 2 * Hkv * row * elt
         flops = 2.0 * H * tokens * 2 * D
         out_w = D
     io_bytes = B * H * D * 2 + B * H * out_w * 2 + B * H * 4
@@ -314,8 +321,11 @@ def run_ours(args):
 
     # inputs resident in HBM
     q = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    pth = case.kv_dtype in synth.PTH_DTYPES
     if case.kv_dtype == "bf16":
         kv = torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).to(dev)
+    elif pth:
+        kv = torch.from_numpy(case.kv).to(dev)  # uint8 rows: codes + inline scale
     else:
         kv = torch.from_numpy(case.kv).view(torch.float8_e4m3fn).to(dev)
     bt = torch.from_numpy(case.block_table).to(dev)
@@ -356,7 +366,8 @@ def run_ours(args):
                            num_kv_splits=splits, workspace=ws, kv_lora_rank=R, stream=stream)
         else:
             mqa.gqa_paged_decode(qq, kv, btt, sll, case.scale, case.k_scale, case.v_scale, out=oo,
-                                 lse=ll, num_kv_splits=splits, workspace=ws, stream=stream)
+                                 lse=ll, num_kv_splits=splits, workspace=ws, stream=stream,
+                                 kv_dtype=case.kv_dtype if pth else None)
 
     for i in range(args.warmup):
         flush_l2(i)
@@ -457,7 +468,9 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
         "us_per_call": round(mean_ms * 1e3, 2), "tflops": round(tflops, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if case.kv_dtype == "bf16" else "bf16 (fp8-e4m3 KV)",
+        "dtype": {"bf16": "bf16", "fp8_e4m3": "bf16 (fp8-e4m3 KV)",
+                  "fp8_e4m3_pth": "bf16 (fp8-e4m3 KV, per-token-head scales)",
+                  "int8_pth": "bf16 (int8 KV, per-token-head scales)"}[case.kv_dtype],
         "data": "synthetic (seeded N(0,1) q/KV, random block permutation)",
         "config": workload_config(case, args.workload, splits),
         "roofline": roof, "cpu_baseline": cpu,

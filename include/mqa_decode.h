@@ -74,7 +74,12 @@ typedef enum mqa_status {
 
 typedef enum mqa_kv_dtype {
     MQA_KV_BF16 = 0,     /* bfloat16 cache; k_scale / v_scale are ignored */
-    MQA_KV_FP8_E4M3 = 1  /* OCP e4m3fn cache; element value = scale * e4m3(code) */
+    MQA_KV_FP8_E4M3 = 1, /* OCP e4m3fn cache; element value = scale * e4m3(code) */
+    /* Per-token-head quantised GQA caches (gqa_paged_decode only): each
+     * (token, KV head) row of the K and V planes carries its own scale
+     * inline, after its codes; see gqa_paged_decode. */
+    MQA_KV_FP8_E4M3_PER_TOKEN_HEAD = 2,
+    MQA_KV_INT8_PER_TOKEN_HEAD = 3
 } mqa_kv_dtype;
 
 /* ABI version of the loaded library (MQA_ABI_VERSION at build time). */
@@ -241,14 +246,35 @@ mqa_status mla_decode_noalloc(const void* q, const void* kv_cache, const int32_t
  * page, "Motivation de conception").
  *
  *   q            bf16 [batch, num_q_heads, head_size]
- *   kv_cache     [num_blocks, 2, page_size, num_kv_heads, head_size]; plane 0
- *                holds K, plane 1 holds V.  bf16 only in this version.
+ *   kv_cache     [num_blocks, 2, page_size, num_kv_heads, row]; plane 0
+ *                holds K, plane 1 holds V.  By kv_dtype:
+ *                  MQA_KV_BF16      row = head_size bf16 values;
+ *                  MQA_KV_FP8_E4M3  row = head_size e4m3 codes, K value =
+ *                                   k_scale * code, V value = v_scale * code;
+ *                  MQA_KV_FP8_E4M3_PER_TOKEN_HEAD / MQA_KV_INT8_PER_TOKEN_HEAD
+ *                                   row = head_size + 4 bytes: head_size e4m3
+ *                                   or int8 (two's complement) codes, then
+ *                                   the row's scale as a little-endian IEEE
+ *                                   binary32; value = that scale * code
+ *                                   (k_scale / v_scale are ignored).  The
+ *                                   Triton backend's fp8_per_token_head /
+ *                                   int8_per_token_head caches ("Triton と
+ *                                   MLA" page, 設計動機 and 主要ファイル: the
+ *                                   head dimension is padded to hold the
+ *                                   inline scale; the 4-byte padding and the
+ *                                   scale's position are this library's
+ *                                   reading of that).
+ *   k_scale, v_scale  finite; used by MQA_KV_FP8_E4M3 only.
+ *   With an 8-bit cache the tensor cores take the query as f16 (the codes
+ *   widen to f16 exactly): q entries must lie within +-65504.
  *   out          bf16 [batch, num_q_heads, head_size]; lse fp32 [batch,
  *                num_q_heads] or NULL.
  *   Query head h reads KV head h / (num_q_heads / num_kv_heads).
  *   head_size in {64, 128}; num_kv_heads in [1, 8]; num_q_heads a multiple of
  *   num_kv_heads with at most 16 query heads per KV head; page_size a multiple
- *   of 16.  Other arguments as for mla_decode.
+ *   of 16.  Tokens past seq_lens[b] in a request's last page are never used,
+ *   whatever their bytes (NaN codes or scales included).  Other arguments as
+ *   for mla_decode.
  */
 mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* block_table,
                             const int32_t* seq_lens, float scale, float k_scale, float v_scale,

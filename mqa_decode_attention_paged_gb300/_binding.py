@@ -22,6 +22,10 @@ ERR_DEVICE_TIMEOUT = 6
 
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
+KV_FP8_E4M3_PER_TOKEN_HEAD = 2
+KV_INT8_PER_TOKEN_HEAD = 3
+_KV_NAMES = {"bf16": KV_BF16, "fp8_e4m3": KV_FP8_E4M3, "fp8_e4m3_pth": KV_FP8_E4M3_PER_TOKEN_HEAD,
+             "int8_pth": KV_INT8_PER_TOKEN_HEAD}
 
 LIB_PATH = _build.LIB_PATH
 
@@ -112,7 +116,7 @@ def _stream(stream):
 def _kv_code(kv_cache, kv_dtype):
     import torch
     if kv_dtype is not None:
-        return {"bf16": KV_BF16, "fp8_e4m3": KV_FP8_E4M3}[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
+        return _KV_NAMES[kv_dtype] if isinstance(kv_dtype, str) else int(kv_dtype)
     if kv_cache.dtype == torch.bfloat16:
         return KV_BF16
     if kv_cache.dtype == torch.float8_e4m3fn:
@@ -216,14 +220,17 @@ def mla_decode_sparse(q, kv_cache, block_table, seq_lens, indices, scale, k_scal
 def gqa_paged_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, v_scale=1.0, *,
                      out=None, lse=None, num_kv_splits=1, workspace=None, kv_dtype=None,
                      device_status=None, stream=None, return_lse=True):
-    """GQA paged decode through the C ABI.  q [B,Hq,D] bf16, kv_cache
-    [num_blocks, 2, page, Hkv, D] bf16."""
+    """GQA paged decode through the C ABI.  q [B,Hq,D] bf16; kv_cache
+    [num_blocks, 2, page, Hkv, D] bf16 or e4m3 (k_scale / v_scale), or, with
+    kv_dtype "fp8_e4m3_pth" / "int8_pth", uint8 [num_blocks, 2, page, Hkv,
+    D + 4] rows of D codes followed by their fp32 scale."""
     import torch
     B, Hq, D = q.shape
     nb, two, page, Hkv, D2 = kv_cache.shape
-    if two != 2 or D2 != D:
-        raise ValueError("kv_cache must be [num_blocks, 2, page, num_kv_heads, head_size]")
     code = _kv_code(kv_cache, kv_dtype)
+    row = D + 4 if code in (KV_FP8_E4M3_PER_TOKEN_HEAD, KV_INT8_PER_TOKEN_HEAD) else D
+    if two != 2 or D2 != row:
+        raise ValueError(f"kv_cache must be [num_blocks, 2, page, num_kv_heads, {row}]")
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=q.device)
     if lse is None and return_lse:

@@ -11,6 +11,7 @@
 #include "plan.cuh"
 
 #include "args.cuh"
+#include "gqa_q8.cuh"
 
 namespace {
 
@@ -563,8 +564,6 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
                             int head_size, int num_blocks, int page_size, int max_blocks,
                             mqa_kv_dtype kv_dtype, int num_kv_splits, void* workspace,
                             size_t workspace_bytes, int* device_status, void* stream) {
-    (void)k_scale;
-    (void)v_scale;
     if (!q || !kv_cache || !block_table || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
         !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (device_status && !aligned(device_status, 4)))
@@ -577,7 +576,11 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
     if (head_size != 64 && head_size != 128) return MQA_ERR_UNSUPPORTED;
     if (num_kv_heads > 8 || num_q_heads / num_kv_heads > 16) return MQA_ERR_UNSUPPORTED;
     if (page_size % 16 != 0) return MQA_ERR_UNSUPPORTED;
-    if (kv_dtype != MQA_KV_BF16) return MQA_ERR_UNSUPPORTED;
+    if (kv_dtype != MQA_KV_BF16 && kv_dtype != MQA_KV_FP8_E4M3 && kv_dtype != MQA_KV_FP8_E4M3_PER_TOKEN_HEAD &&
+        kv_dtype != MQA_KV_INT8_PER_TOKEN_HEAD)
+        return MQA_ERR_UNSUPPORTED;
+    if (kv_dtype == MQA_KV_FP8_E4M3 && (!std::isfinite(k_scale) || !std::isfinite(v_scale)))
+        return MQA_ERR_INVALID_ARG;
     if (batch > kMaxBatch) return MQA_ERR_UNSUPPORTED;
     if (static_cast<long long>(max_blocks) * page_size > INT32_MAX ||
         static_cast<long long>(num_blocks) * page_size > INT32_MAX)
@@ -601,7 +604,8 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
     a.ws_o = static_cast<float*>(workspace);
     a.ws_lse = need > 0 ? a.ws_o + slots * num_q_heads * head_size : nullptr;
     a.status = device_status;
-    a.sl2 = scale * mqa::kLog2e;
+    const bool per_tensor_fp8 = kv_dtype == MQA_KV_FP8_E4M3;
+    a.sl2 = scale * (per_tensor_fp8 ? k_scale : 1.0f) * mqa::kLog2e;
     a.Hq = num_q_heads;
     a.Hkv = num_kv_heads;
     a.num_blocks = num_blocks;
@@ -612,7 +616,17 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
     a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaError_t e = mqa::gqa_mma_stage1(a, head_size, a.plan.units, st); e != cudaSuccess) return cuda_fail(e);
+    if (kv_dtype == MQA_KV_BF16) {
+        if (cudaError_t e = mqa::gqa_mma_stage1(a, head_size, a.plan.units, st); e != cudaSuccess)
+            return cuda_fail(e);
+    } else {
+        // 8-bit codes: widened per KV head in shared memory; per-tensor fp8
+        // folds k_scale into the softmax scale and v_scale into the output
+        const float out_scale = per_tensor_fp8 ? v_scale : 1.0f;
+        if (cudaError_t e = mqa::gqa_q8_stage1(a, out_scale, head_size, static_cast<int>(kv_dtype), a.plan.units, st);
+            e != cudaSuccess)
+            return cuda_fail(e);
+    }
     if (!a.plan.per_seq) {
         mqa::MergeArgs m{};
         m.ws_o = a.ws_o;

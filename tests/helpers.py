@@ -23,6 +23,8 @@ def to_device(case: synth.PagedCase, device="cuda"):
     q = torch.from_numpy(case.q.view(np.int16)).view(torch.bfloat16).to(device)
     if case.kv_dtype == "bf16":
         kv = torch.from_numpy(case.kv.view(np.int16)).view(torch.bfloat16).to(device)
+    elif case.kv_dtype in synth.PTH_DTYPES:
+        kv = torch.from_numpy(case.kv).to(device)  # uint8 rows: codes + inline scale
     else:
         kv = torch.from_numpy(case.kv).view(torch.float8_e4m3fn).to(device)
     bt = torch.from_numpy(case.block_table).to(device)
@@ -52,7 +54,8 @@ def run_gpu(case, num_kv_splits=1, dev=None, status=None):
     else:
         out, lse = mqa.gqa_paged_decode(q, kv, bt, sl, case.scale, case.k_scale, case.v_scale,
                                         out=out, lse=lse, num_kv_splits=num_kv_splits,
-                                        workspace=ws, device_status=status)
+                                        workspace=ws, device_status=status,
+                                        kv_dtype=case.kv_dtype if case.kv_dtype in synth.PTH_DTYPES else None)
     torch.cuda.synchronize()
     return out.double().cpu().numpy(), lse.double().cpu().numpy()
 

@@ -127,12 +127,12 @@ def test_mla_sparse_validation(kw, code):
 
 
 def _gqa(**kw):
-    a = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, scale=0.09, out=FAKE, lse=None, B=2, Hq=32, Hkv=8,
-             D=128, nb=10, P=16, maxb=8, kvd=0, S=1, ws=None, wsb=0)
+    a = dict(q=FAKE, kv=FAKE, bt=FAKE, sl=FAKE, scale=0.09, ks=1.0, vs=1.0, out=FAKE, lse=None, B=2, Hq=32,
+             Hkv=8, D=128, nb=10, P=16, maxb=8, kvd=0, S=1, ws=None, wsb=0)
     a.update(kw)
     P = lambda v: None if v is None else ctypes.c_void_p(v)  # noqa: E731
-    return mqa.lib.gqa_paged_decode(P(a["q"]), P(a["kv"]), P(a["bt"]), P(a["sl"]), a["scale"], 1.0,
-                                    1.0, P(a["out"]), P(a["lse"]), a["B"], a["Hq"], a["Hkv"], a["D"],
+    return mqa.lib.gqa_paged_decode(P(a["q"]), P(a["kv"]), P(a["bt"]), P(a["sl"]), a["scale"], a["ks"],
+                                    a["vs"], P(a["out"]), P(a["lse"]), a["B"], a["Hq"], a["Hkv"], a["D"],
                                     a["nb"], a["P"], a["maxb"], a["kvd"], a["S"], P(a["ws"]), a["wsb"],
                                     None, None)
 
@@ -154,6 +154,8 @@ def _gqa(**kw):
     (dict(P=24), mqa.ERR_UNSUPPORTED),                 # page must be a multiple of 16
     (dict(P=8), mqa.ERR_UNSUPPORTED),
     (dict(kvd=7), mqa.ERR_UNSUPPORTED),
+    (dict(kvd=2), mqa.ERR_UNSUPPORTED),                # per-token-head formats are GQA-only
+    (dict(kvd=3), mqa.ERR_UNSUPPORTED),
     (dict(H=129), mqa.ERR_UNSUPPORTED),
     (dict(B=4097), mqa.ERR_UNSUPPORTED),
     (dict(S=4, ws=None, wsb=0), mqa.ERR_WORKSPACE_TOO_SMALL),
@@ -169,7 +171,13 @@ def test_mla_validation(kw, code):
     (dict(D=96), mqa.ERR_UNSUPPORTED),
     (dict(Hkv=16, Hq=32), mqa.ERR_UNSUPPORTED),
     (dict(Hkv=1, Hq=32), mqa.ERR_UNSUPPORTED),         # at most 16 query heads per KV head
-    (dict(kvd=1), mqa.ERR_UNSUPPORTED),                # GQA serves bf16 caches only
+    (dict(kvd=4), mqa.ERR_UNSUPPORTED),                # bf16, e4m3 and the per-token-head formats only
+    (dict(kvd=-1), mqa.ERR_UNSUPPORTED),
+    (dict(kvd=1, ks=float("nan")), mqa.ERR_INVALID_ARG),  # per-tensor fp8 needs finite scales
+    (dict(kvd=1, vs=float("inf")), mqa.ERR_INVALID_ARG),
+    (dict(kvd=1, S=2), mqa.ERR_WORKSPACE_TOO_SMALL),   # each accepted format reaches the workspace check
+    (dict(kvd=2, S=2), mqa.ERR_WORKSPACE_TOO_SMALL),
+    (dict(kvd=3, S=2, ks=float("nan")), mqa.ERR_WORKSPACE_TOO_SMALL),  # scales unused by per-token-head
     (dict(P=40), mqa.ERR_UNSUPPORTED),
     (dict(S=2), mqa.ERR_WORKSPACE_TOO_SMALL),
 ])
