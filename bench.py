@@ -57,9 +57,9 @@ NCU_TRAFFIC = {
                     "kernel": "mla_decode_tc_kernel<576,512,0>"},
     "mla_v3_fp8": {"files": TC_FILES, "src_sha": "db7d88cc3b68ce52", "splits": 64, "bytes": 1423465728 + 25308416,
                    "kernel": "mla_decode_tc_kernel<576,512,1>"},
-    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "e82ed99867428332", "splits": 32, "bytes": 1538930176 + 4318720,
+    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "1406af8df51abd32", "splits": 32, "bytes": 1535293184 + 4885504,
                     "kernel": "gqa_decode_q8_kernel<128,2>"},
-    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "e82ed99867428332", "splits": 32, "bytes": 1693782016 + 4549376,
+    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "1406af8df51abd32", "splits": 32, "bytes": 1690158848 + 5242624,
                      "kernel": "gqa_decode_q8_kernel<128,3>"},
 }
 

@@ -11,24 +11,33 @@
 //
 // One thread block = Hkv consumer warps + 1 producer warp, persistent over a
 // work unit (plan.cuh), as in the bf16 kernel.  The producer stages 16-token
-// tiles with two bulk copies per tile: the 16 consecutive rows of the K plane
-// and of the V plane of one page (16 * Hkv * row bytes each; tiles start on a
-// multiple of 16 tokens and pages hold a multiple of 16, so every copy is
-// 16-byte aligned and stays inside its page).  Consumer warp g owns KV head
-// g: it widens its head's 16 K rows and 16 V rows to f16 codes (exact for
-// both code types) in a private shared-memory tile, reads the K and V scales
-// of its tokens, frees the stage, and then runs the register-resident tile of
-// the bf16 kernel with f16 operands (the query is rounded to f16 once per
-// piece): S = Q K^T by warp MMA, the K scale applied per token column to S in
-// fp32, online softmax in base 2 (tutorial page lshu.cn/news/265860, §7),
-// O += P V with P multiplied by the V scale of its token.  So that those
-// products stay normal f16 numbers whatever the scales' magnitude, P carries
-// a power-of-two factor 2^-e (e: exponent above the largest V scale seen so
-// far in the piece); O is rescaled by the same power of two when e grows,
-// together with the softmax rescale, and multiplied back at the end.  Tokens
-// past the sequence end (and whole tiles of a page with an invalid block id)
-// are widened as zeros, masked out of the softmax and get V scale 0, so
-// padding never reaches the output.
+// tiles of the K and V planes of one page (tiles start on a multiple of 16
+// tokens and pages hold a multiple of 16, so a tile stays inside its page):
+// one bulk copy per token row when a row (all KV heads) is a multiple of 16
+// bytes, into rows padded by 16 bytes so that the consumers' reads spread
+// over the banks (measured faster than dense tiles even where those would
+// collide only 2 ways), else one bulk copy of the 16 dense rows per plane.
+// The stage count is set per launch from the shared memory left by the batch.
+//
+// Consumer warp g owns KV head g and its query heads (an m16 tile).
+//   * S = Q K^T by warp MMA with f16 operands.  The reduction order inside
+//     each 16-wide step is permuted (lane c takes head dims 4c .. 4c + 3 in
+//     both Q and K), so a lane's K operand of one token is one 4-byte read of
+//     codes, widened to f16 in registers: no K tile is written back.
+//   * the K scale of each token multiplies its logits in fp32; online
+//     softmax in base 2 (tutorial page lshu.cn/news/265860, §7) with lazy
+//     rescaling: the reference max moves only when a logit exceeds it by more
+//     than 8 (P <= 2^8), so O is rescaled rarely.
+//   * V codes are widened to f16 into a private 16-row tile (ldmatrix.trans
+//     feeds P.V); P is multiplied by the V scale of its token and by 2^-e, e
+//     the exponent above the largest V scale of the piece so far, so the f16
+//     products stay normal numbers whatever the scales' magnitude; O follows
+//     e with exact power-of-two rescales and is multiplied back at the end.
+//   * the stage is released as soon as the K reads and the V widening are
+//     done, before the softmax.
+// Tokens past the sequence end (and whole tiles of a page with an invalid
+// block id) are masked out of the softmax, their V rows widened as zeros and
+// their V scale taken as 0, so padding never reaches the output.
 //
 // f16 operands: e4m3 -> f16 is one conversion per code pair and int8 -> f16
 // an exact integer trick (1024 + u - 1152), where bf16 needs three more
@@ -57,25 +66,33 @@ struct GqaQ8Cfg {
     static constexpr int kDp = kPth ? D + 4 : D;  // bytes of one (token, KV head) row
     static constexpr int kKSteps = D / 16;
     static constexpr int kNb = D / 8;
-    // widened f16 tile rows: 16 bytes of padding keep ldmatrix conflict-free
+    // widened f16 V tile rows: 16 bytes of padding keep ldmatrix conflict-free
     static constexpr int kWStride = 2 * D + 16;
-    static constexpr int kWBytes = 2 * kTile * kWStride;  // K and V tiles of one warp
+    static constexpr int kWBytes = kTile * kWStride;  // one warp's V tile
     static_assert(kWBytes % 128 == 0, "per-warp tiles stay 128-byte aligned");
+    static constexpr int kMaxStages = 8;
     __host__ __device__ static int row_bytes(int hkv) { return hkv * kDp; }  // one token, all heads
-    __host__ __device__ static int plane_bytes(int hkv) { return kTile * row_bytes(hkv); }
+    // Rows are copied one by one into rows padded by 16 bytes when a row is a
+    // multiple of 16 bytes (the consumers' reads of 8 rows then spread over
+    // the banks), else a tile is one copy of 16 dense rows per plane.
+    __host__ __device__ static bool per_row(int hkv) { return row_bytes(hkv) % 16 == 0; }
+    __host__ __device__ static int row_stride(int hkv) { return row_bytes(hkv) + (per_row(hkv) ? 16 : 0); }
+    __host__ __device__ static int plane_bytes(int hkv) { return kTile * row_stride(hkv); }
     __host__ __device__ static int stage_bytes(int hkv) { return 2 * plane_bytes(hkv); }
-    __host__ __device__ static int stages(int hkv) {
-        const int n = (200 * 1024 - hkv * kWBytes) / stage_bytes(hkv);
-        return n < 2 ? 2 : (n > 8 ? 8 : n);
-    }
-    // layout: widened tiles (per warp) | stages | masks | full bars | empty bars | cum
+    // layout: V tiles (per warp) | stages | masks | full bars | empty bars | cum
     __host__ __device__ static size_t off_stages(int hkv) { return static_cast<size_t>(hkv) * kWBytes; }
-    __host__ __device__ static size_t off_masks(int hkv) {
-        return off_stages(hkv) + static_cast<size_t>(stages(hkv)) * stage_bytes(hkv);
+    __host__ __device__ static size_t off_masks(int hkv, int ns) {
+        return off_stages(hkv) + static_cast<size_t>(ns) * stage_bytes(hkv);
     }
-    __host__ __device__ static size_t off_bars(int hkv) { return off_masks(hkv) + 8 * stages(hkv); }
-    __host__ __device__ static size_t off_cum(int hkv) { return off_bars(hkv) + 16 * stages(hkv); }
-    static size_t smem_bytes(int hkv, int batch) { return off_cum(hkv) + 4 * (2 * batch + 1); }
+    __host__ __device__ static size_t off_bars(int hkv, int ns) { return off_masks(hkv, ns) + 8 * ns; }
+    __host__ __device__ static size_t off_cum(int hkv, int ns) { return off_bars(hkv, ns) + 16 * ns; }
+    static size_t smem_bytes(int hkv, int ns, int batch) { return off_cum(hkv, ns) + 4 * (2 * batch + 1); }
+    // as many stages as fit in `limit` bytes of shared memory (2 .. kMaxStages)
+    static int stages_for(int hkv, int batch, size_t limit) {
+        int ns = kMaxStages;
+        while (ns > 2 && smem_bytes(hkv, ns, batch) > limit) --ns;
+        return ns;
+    }
 };
 
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -144,19 +161,19 @@ __device__ __forceinline__ int scale_exponent(float vmax) {
 
 template <int D, int KIND>
 __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
-    gqa_decode_q8_kernel(const GqaArgs a, const float out_scale) {
+    gqa_decode_q8_kernel(const GqaArgs a, const float out_scale, const int nstage) {
     using C = GqaQ8Cfg<D, KIND>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int Hkv = a.Hkv;
-    const int nstage = C::stages(Hkv);
     const int rbytes = C::row_bytes(Hkv);
+    const int rstride = C::row_stride(Hkv);
     const int pbytes = C::plane_bytes(Hkv);
     const int sbytes = C::stage_bytes(Hkv);
     uint8_t* stages = smem + C::off_stages(Hkv);
-    uint64_t* mask_s = reinterpret_cast<uint64_t*>(smem + C::off_masks(Hkv));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::off_bars(Hkv));
+    uint64_t* mask_s = reinterpret_cast<uint64_t*>(smem + C::off_masks(Hkv, nstage));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::off_bars(Hkv, nstage));
     uint64_t* empty = full + nstage;
-    int* cum = reinterpret_cast<int*>(smem + C::off_cum(Hkv));
+    int* cum = reinterpret_cast<int*>(smem + C::off_cum(Hkv, nstage));
     int* lens = cum + a.plan.batch + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -177,14 +194,16 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
 
     if (warp == Hkv) {
         // ------------------------------------------------------------ producer
-        if (lane != 0) return;
+        const bool rows = C::per_row(Hkv);
         const uint64_t pol = l2_policy_evict_first();
+        // per-row mode: lane -> (plane, row): lanes 0-15 copy K rows, 16-31 V rows
+        const int plane = lane >> 4, r = lane & 15;
         TileCursor cur;
         cur.init(a.plan, cum, T, unit, C::kTile);
         int stage = 0;
         uint32_t phase = 0;
-        int issued[8];
-        for (int s = 0; s < 8; ++s) issued[s] = -1;
+        int issued[C::kMaxStages];
+        for (int s = 0; s < C::kMaxStages; ++s) issued[s] = -1;
         // the tile's block id is read one tile ahead of its use
         bool have = cur.next(a.plan, cum, lens, a.block_table);
         int t0 = have ? cur.t0 : 0, tend = have ? cur.tok_end : 0;
@@ -198,16 +217,27 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
                 break;
             }
             const bool valid = blk >= 0 && blk < a.num_blocks;
-            if (!valid) report(a.status, MQA_ERR_DEVICE_CHECK);
             const int nv = min(C::kTile, tend - t0);  // >= 1: the cursor only yields non-empty tiles
-            mask_s[stage] = valid ? ((1ull << nv) - 1ull) : 0ull;
-            mbar_arrive_expect_tx(&full[stage], valid ? 2u * pbytes : 0u);
+            // slot t0 % P of page blk: plane 0 (K), plane 1 (V) P rows later
+            const uint8_t* src = a.kv + (static_cast<long long>(blk) * 2 * P + t0 % P) * rbytes;
+            uint8_t* dst = stages + stage * sbytes;
+            if (lane == 0) {
+                if (!valid) report(a.status, MQA_ERR_DEVICE_CHECK);
+                mask_s[stage] = valid ? ((1ull << nv) - 1ull) : 0ull;
+                // per-row mode copies the nv valid rows of each plane
+                const uint32_t bytes = !valid ? 0u : (rows ? 2u * nv * rbytes : 2u * pbytes);
+                mbar_arrive_expect_tx(&full[stage], bytes);
+            }
+            __syncwarp();
             if (valid) {
-                // slot t0 % P of page blk: plane 0 (K) then plane 1 (V), P rows later
-                const uint8_t* src = a.kv + (static_cast<long long>(blk) * 2 * P + t0 % P) * rbytes;
-                uint8_t* dst = stages + stage * sbytes;
-                bulk_g2s(dst, src, pbytes, &full[stage], pol);
-                bulk_g2s(dst + pbytes, src + static_cast<long long>(P) * rbytes, pbytes, &full[stage], pol);
+                if (rows) {
+                    if (r < nv)
+                        bulk_g2s(dst + plane * pbytes + r * rstride,
+                                 src + (static_cast<long long>(plane) * P + r) * rbytes, rbytes, &full[stage], pol);
+                } else if (lane == 0) {
+                    bulk_g2s(dst, src, pbytes, &full[stage], pol);
+                    bulk_g2s(dst + pbytes, src + static_cast<long long>(P) * rbytes, pbytes, &full[stage], pol);
+                }
             }
             issued[stage] = static_cast<int>(phase);
             if (++stage == nstage) {
@@ -230,8 +260,7 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
     const int g = lane >> 2, c = lane & 3;
     const bool row0 = g < grp, row1 = g + 8 < grp;
     const int hoff = gk * C::kDp;  // byte offset of this KV head inside a token row
-    uint8_t* wk = smem + gk * C::kWBytes;
-    uint8_t* wv = wk + C::kTile * C::kWStride;
+    uint8_t* wv = smem + gk * C::kWBytes;
 
     PieceIter it;
     it.init(a.plan, cum, T, unit);
@@ -246,18 +275,20 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
         const int tok_end = min(pc.j1 * P, len);
         const int hq0 = gk * grp;
 
+        // Q as f16, in the permuted reduction order: step ks, lane c holds
+        // head dims 16 ks + 4c .. 4c + 3 of rows g and g + 8 (a0/a2 and a1/a3)
         uint32_t qa[C::kKSteps][4];
         {
             const __nv_bfloat16* qb = a.q + (static_cast<long long>(pc.b) * a.Hq + hq0) * D;
 #pragma unroll
             for (int ks = 0; ks < C::kKSteps; ++ks) {
-                const int k0 = ks * 16 + 2 * c;
-                qa[ks][0] = row0 ? *reinterpret_cast<const uint32_t*>(qb + g * D + k0) : 0u;
-                qa[ks][1] = row1 ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + k0) : 0u;
-                qa[ks][2] = row0 ? *reinterpret_cast<const uint32_t*>(qb + g * D + k0 + 8) : 0u;
-                qa[ks][3] = row1 ? *reinterpret_cast<const uint32_t*>(qb + (g + 8) * D + k0 + 8) : 0u;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) qa[ks][i] = bf16x2_to_f16x2(qa[ks][i]);
+                const int k0 = ks * 16 + 4 * c;
+                const uint2 q0 = row0 ? *reinterpret_cast<const uint2*>(qb + g * D + k0) : make_uint2(0u, 0u);
+                const uint2 q1 = row1 ? *reinterpret_cast<const uint2*>(qb + (g + 8) * D + k0) : make_uint2(0u, 0u);
+                qa[ks][0] = bf16x2_to_f16x2(q0.x);
+                qa[ks][1] = bf16x2_to_f16x2(q1.x);
+                qa[ks][2] = bf16x2_to_f16x2(q0.y);
+                qa[ks][3] = bf16x2_to_f16x2(q1.y);
             }
         }
         float o[C::kNb][4];
@@ -282,17 +313,31 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
                 const int tok = (i >> 1) * 8 + 2 * c + (i & 1);
                 const bool v = (vmask >> tok) & 1ull;
                 if constexpr (C::kPth) {
-                    ksc[i] = v ? *reinterpret_cast<const float*>(kb + tok * rbytes + D) : 0.f;
-                    vsc[i] = v ? *reinterpret_cast<const float*>(vb + tok * rbytes + D) : 0.f;
+                    ksc[i] = v ? *reinterpret_cast<const float*>(kb + tok * rstride + D) : 0.f;
+                    vsc[i] = v ? *reinterpret_cast<const float*>(vb + tok * rstride + D) : 0.f;
                 } else {
                     ksc[i] = 1.f;
                     vsc[i] = 1.f;
                 }
             }
-            __syncwarp();  // the previous tile's ldmatrix reads of wk / wv are done
-            widen_rows<D, KIND>(kb, wk, vmask, rbytes, lane);
-            widen_rows<D, KIND>(vb, wv, vmask, rbytes, lane);
-            __syncwarp();
+            __syncwarp();  // the previous tile's ldmatrix reads of wv are done
+            widen_rows<D, KIND>(vb, wv, vmask, rstride, lane);
+
+            // S = Q K^T: token n = nb * 8 + g, one 4-byte read of its codes
+            // per step (masked tokens' columns are discarded below)
+            float s[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < C::kKSteps; ++ks) {
+#pragma unroll
+                for (int nb = 0; nb < 2; ++nb) {
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(kb + (nb * 8 + g) * rstride + ks * 16 + 4 * c);
+                    const uint2 kf = widen4<KIND>(w);
+                    mma_f16_16816(s[nb], qa[ks], kf.x, kf.y);
+                }
+            }
+            __syncwarp();  // every lane's K reads and V tile writes are done
             if (lane == 0) mbar_arrive(&empty[stage]);
             if (++stage == nstage) {
                 stage = 0;
@@ -316,18 +361,6 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
                 for (int i = 0; i < 4; ++i) vsc[i] *= p_fac;
             }
 
-            float s[2][4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < C::kKSteps; ++ks) {
-                const int row = (lane & 7) + ((lane >> 4) << 3);
-                const int col = ks * 16 + ((lane >> 3) & 1) * 8;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(b0, b1, b2, b3, wk + row * C::kWStride + col * 2);
-                mma_f16_16816(s[0], qa[ks], b0, b1);
-                mma_f16_16816(s[1], qa[ks], b2, b3);
-            }
             // online softmax; rows g (values 0,1) and g+8 (values 2,3)
             float x[2][4];
             float mx[2] = {-INFINITY, -INFINITY};
@@ -340,36 +373,43 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
                     x[nb][j] = valid ? s[nb][j] * ksc[nb * 2 + (j & 1)] * a.sl2 : -INFINITY;
                     mx[j >> 1] = fmaxf(mx[j >> 1], x[nb][j]);
                 }
-            float alpha[2], m_use[2];
+            float alpha[2] = {1.f, 1.f};
+            bool grow = false;
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
                 mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                const float m_new = fmaxf(m_run[r], mx[r]);
-                m_use[r] = m_new == -INFINITY ? 0.f : m_new;
-                alpha[r] = ex2(m_run[r] - m_use[r]);
-                m_run[r] = m_new;
-                l_part[r] *= alpha[r];
+                // lazy: move the reference only when P would exceed 2^8
+                if (mx[r] > m_run[r] + 8.f) {
+                    alpha[r] = ex2(m_run[r] - mx[r]);
+                    m_run[r] = mx[r];
+                    l_part[r] *= alpha[r];
+                    grow = true;
+                }
             }
+            const float m_use0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+            const float m_use1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
             uint32_t pa[4];
 #pragma unroll
             for (int nb = 0; nb < 2; ++nb) {
                 // l sums the fp32 probabilities; P.V takes them times the V
                 // scale of their token and 2^-e_run, rounded to f16
-                const float p0 = ex2(x[nb][0] - m_use[0]), p1 = ex2(x[nb][1] - m_use[0]);
-                const float p2 = ex2(x[nb][2] - m_use[1]), p3 = ex2(x[nb][3] - m_use[1]);
+                const float p0 = ex2(x[nb][0] - m_use0), p1 = ex2(x[nb][1] - m_use0);
+                const float p2 = ex2(x[nb][2] - m_use1), p3 = ex2(x[nb][3] - m_use1);
                 l_part[0] += p0 + p1;
                 l_part[1] += p2 + p3;
                 pa[2 * nb] = pack_f16x2(p0 * vsc[2 * nb], p1 * vsc[2 * nb + 1]);
                 pa[2 * nb + 1] = pack_f16x2(p2 * vsc[2 * nb], p3 * vsc[2 * nb + 1]);
             }
-            const float oa0 = alpha[0] * o_fix, oa1 = alpha[1] * o_fix;
+            if (__any_sync(0xffffffffu, grow) || o_fix != 1.f) {
+                const float oa0 = alpha[0] * o_fix, oa1 = alpha[1] * o_fix;
 #pragma unroll
-            for (int i = 0; i < C::kNb; ++i) {
-                o[i][0] *= oa0;
-                o[i][1] *= oa0;
-                o[i][2] *= oa1;
-                o[i][3] *= oa1;
+                for (int i = 0; i < C::kNb; ++i) {
+                    o[i][0] *= oa0;
+                    o[i][1] *= oa0;
+                    o[i][2] *= oa1;
+                    o[i][3] *= oa1;
+                }
             }
 #pragma unroll
             for (int nb2 = 0; nb2 < C::kNb / 2; ++nb2) {
@@ -434,15 +474,19 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
     }
 }
 
+// Dynamic shared memory a block may use on sm_103a (227 KB).
+constexpr size_t kSmemLimit = 227 * 1024;
+
 template <int D, int KIND>
 cudaError_t launch_q8(const GqaArgs& a, float out_scale, int grid, cudaStream_t stream) {
     using C = GqaQ8Cfg<D, KIND>;
-    const size_t smem = C::smem_bytes(a.Hkv, a.plan.batch);
+    const int ns = C::stages_for(a.Hkv, a.plan.batch, kSmemLimit);
+    const size_t smem = C::smem_bytes(a.Hkv, ns, a.plan.batch);
     auto kern = gqa_decode_q8_kernel<D, KIND>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = launch_with_pdl(kern, dim3(grid), dim3(32 * (a.Hkv + 1)), smem, stream, a, out_scale);
+    e = launch_with_pdl(kern, dim3(grid), dim3(32 * (a.Hkv + 1)), smem, stream, a, out_scale, ns);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -454,11 +498,17 @@ cudaError_t launch_q8_kind(const GqaArgs& a, float out_scale, int kind, int grid
     return launch_q8<D, kFmtE4m3>(a, out_scale, grid, stream);
 }
 
+template <int D, int KIND>
+size_t smem_of(int hkv, int batch) {
+    using C = GqaQ8Cfg<D, KIND>;
+    return C::smem_bytes(hkv, C::stages_for(hkv, batch, kSmemLimit), batch);
+}
+
 template <int D>
 size_t smem_kind(int kind, int hkv, int batch) {
-    if (kind == kFmtE4m3Pth) return GqaQ8Cfg<D, kFmtE4m3Pth>::smem_bytes(hkv, batch);
-    if (kind == kFmtInt8Pth) return GqaQ8Cfg<D, kFmtInt8Pth>::smem_bytes(hkv, batch);
-    return GqaQ8Cfg<D, kFmtE4m3>::smem_bytes(hkv, batch);
+    if (kind == kFmtE4m3Pth) return smem_of<D, kFmtE4m3Pth>(hkv, batch);
+    if (kind == kFmtInt8Pth) return smem_of<D, kFmtInt8Pth>(hkv, batch);
+    return smem_of<D, kFmtE4m3>(hkv, batch);
 }
 
 }  // namespace
