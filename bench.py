@@ -57,10 +57,12 @@ NCU_TRAFFIC = {
                     "kernel": "mla_decode_tc_kernel<576,512,0>"},
     "mla_v3_fp8": {"files": TC_FILES, "src_sha": "db7d88cc3b68ce52", "splits": 64, "bytes": 1423465728 + 25308416,
                    "kernel": "mla_decode_tc_kernel<576,512,1>"},
-    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "1406af8df51abd32", "splits": 32, "bytes": 1535293184 + 4885504,
-                    "kernel": "gqa_decode_q8_kernel<128,2>"},
-    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "1406af8df51abd32", "splits": 32, "bytes": 1690158848 + 5242624,
-                     "kernel": "gqa_decode_q8_kernel<128,3>"},
+    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "8566ab172970c1e5", "splits": 32, "bytes": 1535300864 + 5419264,
+                    "kernel": "gqa_decode_q8_kernel<128,2,1>"},
+    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "8566ab172970c1e5", "splits": 32, "bytes": 1689826560 + 5800192,
+                     "kernel": "gqa_decode_q8_kernel<128,3,1>"},
+    "mla_sparse": {"files": MMA_FILES, "src_sha": "8b3793aae17c641a", "splits": 4, "bytes": 152913664 + 3286528,
+                   "kernel": "mla_decode_mma_kernel<576,512,0,32,0,1>"},
 }
 
 

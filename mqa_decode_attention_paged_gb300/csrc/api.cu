@@ -613,7 +613,9 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
     a.plan.page = page_size;
     a.plan.max_blocks = max_blocks;
     a.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
-    a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms);
+    const int resident =
+        kv_dtype == MQA_KV_BF16 ? sms : sms * mqa::gqa_q8_ctas_per_sm(num_q_heads / num_kv_heads);
+    a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, resident);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (kv_dtype == MQA_KV_BF16) {

@@ -103,6 +103,14 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8x8 matrix of 16-bit values held in the MMA fragment
+// layout (lane i: row i / 4, columns 2 (i % 4) and + 1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -159,8 +167,13 @@ __device__ __forceinline__ int scale_exponent(float vmax) {
     return e;
 }
 
-template <int D, int KIND>
-__global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
+// Resident blocks per SM: two when a KV head serves up to 8 query heads (one
+// head block: 96 registers a thread suffice), one for up to 16.
+__host__ __device__ constexpr int q8_ctas(int nhb) { return nhb == 1 ? 2 : 1; }
+
+// NHB: head blocks of 8 query heads per KV head (1 for up to 8, 2 for up to 16).
+template <int D, int KIND, int NHB>
+__global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), q8_ctas(NHB))
     gqa_decode_q8_kernel(const GqaArgs a, const float out_scale, const int nstage) {
     using C = GqaQ8Cfg<D, KIND>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -204,22 +217,38 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
         uint32_t phase = 0;
         int issued[C::kMaxStages];
         for (int s = 0; s < C::kMaxStages; ++s) issued[s] = -1;
-        // the tile's block id is read one tile ahead of its use
-        bool have = cur.next(a.plan, cum, lens, a.block_table);
-        int t0 = have ? cur.t0 : 0, tend = have ? cur.tok_end : 0;
-        int blk = have ? __ldg(cur.bt + t0 / P) : 0;
-        while (have) {
-            const bool have_next = cur.next(a.plan, cum, lens, a.block_table);
-            const int nt0 = have_next ? cur.t0 : 0, ntend = have_next ? cur.tok_end : 0;
-            const int nblk = have_next ? __ldg(cur.bt + nt0 / P) : 0;
-            if (!mbar_wait(&empty[stage], phase ^ 1)) {
+        // Block ids 32 pages at a time: lane l holds the id of page base + l of
+        // the current piece, and the next 32 are loaded one chunk ahead, so
+        // a tile never waits for a block-table read (with 16-token pages every
+        // tile is a new page).
+        int cur_b = -1, base = 0, jend = 0, ids = 0, nids = 0;
+        auto load_chunk = [&](int j0) {
+            return j0 + lane < jend ? __ldg(cur.bt + j0 + lane) : -1;
+        };
+        while (cur.next(a.plan, cum, lens, a.block_table)) {
+            const int t0 = cur.t0, tend = cur.tok_end;
+            const int j = t0 / P;
+            if (cur.pc.b != cur_b || cur.pc.j1 != jend || j < base) {  // new piece
+                cur_b = cur.pc.b;
+                jend = cur.pc.j1;
+                base = j;
+                ids = load_chunk(base);
+                nids = load_chunk(base + 32);
+            } else if (j >= base + 32) {
+                base += 32;
+                ids = nids;
+                nids = load_chunk(base + 32);
+            }
+            const int blk = __shfl_sync(0xffffffffu, ids, j - base);
+            // warp-uniform decision: the lanes continue or leave together
+            if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1))) {
                 report(a.status, MQA_ERR_DEVICE_TIMEOUT);
                 break;
             }
             const bool valid = blk >= 0 && blk < a.num_blocks;
             const int nv = min(C::kTile, tend - t0);  // >= 1: the cursor only yields non-empty tiles
             // slot t0 % P of page blk: plane 0 (K), plane 1 (V) P rows later
-            const uint8_t* src = a.kv + (static_cast<long long>(blk) * 2 * P + t0 % P) * rbytes;
+            const uint8_t* src = a.kv + (static_cast<long long>(valid ? blk : 0) * 2 * P + t0 % P) * rbytes;
             uint8_t* dst = stages + stage * sbytes;
             if (lane == 0) {
                 if (!valid) report(a.status, MQA_ERR_DEVICE_CHECK);
@@ -244,10 +273,6 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
                 stage = 0;
                 phase ^= 1;
             }
-            have = have_next;
-            t0 = nt0;
-            tend = ntend;
-            blk = nblk;
         }
         for (int s = 0; s < nstage; ++s)
             if (issued[s] >= 0 && !mbar_wait(&full[s], static_cast<uint32_t>(issued[s])))
@@ -256,9 +281,13 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
     }
 
     // ------------------------------------------------------------- consumers
+    // Tokens are the MMA's M dimension: S^T = K Q^T (M = 16 tokens, N = 8
+    // query heads per head block, K = head dims) and O^T = V^T P^T (M = 16
+    // head dims per block, N = 8 heads, K = 16 tokens).  Lane (g, c) holds
+    // tokens g and g + 8 and heads 2c, 2c + 1 of S^T, and head dims
+    // 16 mb + g, + 8 of O^T.
     const int gk = warp;  // KV head
     const int g = lane >> 2, c = lane & 3;
-    const bool row0 = g < grp, row1 = g + 8 < grp;
     const int hoff = gk * C::kDp;  // byte offset of this KV head inside a token row
     uint8_t* wv = smem + gk * C::kWBytes;
 
@@ -275,26 +304,34 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
         const int tok_end = min(pc.j1 * P, len);
         const int hq0 = gk * grp;
 
-        // Q as f16, in the permuted reduction order: step ks, lane c holds
-        // head dims 16 ks + 4c .. 4c + 3 of rows g and g + 8 (a0/a2 and a1/a3)
-        uint32_t qa[C::kKSteps][4];
+        // Q^T operand, f16, in the permuted reduction order (step ks, lane c:
+        // head dims 16 ks + 4c .. + 3): query head hb * 8 + g
+        uint32_t qb[NHB][C::kKSteps][2];
         {
-            const __nv_bfloat16* qb = a.q + (static_cast<long long>(pc.b) * a.Hq + hq0) * D;
+            const __nv_bfloat16* qrow = a.q + (static_cast<long long>(pc.b) * a.Hq + hq0) * D;
 #pragma unroll
-            for (int ks = 0; ks < C::kKSteps; ++ks) {
-                const int k0 = ks * 16 + 4 * c;
-                const uint2 q0 = row0 ? *reinterpret_cast<const uint2*>(qb + g * D + k0) : make_uint2(0u, 0u);
-                const uint2 q1 = row1 ? *reinterpret_cast<const uint2*>(qb + (g + 8) * D + k0) : make_uint2(0u, 0u);
-                qa[ks][0] = bf16x2_to_f16x2(q0.x);
-                qa[ks][1] = bf16x2_to_f16x2(q1.x);
-                qa[ks][2] = bf16x2_to_f16x2(q0.y);
-                qa[ks][3] = bf16x2_to_f16x2(q1.y);
+            for (int hb = 0; hb < NHB; ++hb) {
+                const int h = hb * 8 + g;
+#pragma unroll
+                for (int ks = 0; ks < C::kKSteps; ++ks) {
+                    const uint2 v = h < grp ? *reinterpret_cast<const uint2*>(qrow + h * D + ks * 16 + 4 * c)
+                                            : make_uint2(0u, 0u);
+                    qb[hb][ks][0] = bf16x2_to_f16x2(v.x);
+                    qb[hb][ks][1] = bf16x2_to_f16x2(v.y);
+                }
             }
         }
-        float o[C::kNb][4];
+        float o[NHB][C::kKSteps][4];  // O^T: head dims 16 mb + g (0, 1) and + 8 (2, 3); heads 2c, 2c + 1
 #pragma unroll
-        for (int i = 0; i < C::kNb; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
+        for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+            for (int mb = 0; mb < C::kKSteps; ++mb) o[hb][mb][0] = o[hb][mb][1] = o[hb][mb][2] = o[hb][mb][3] = 0.f;
+        float m_run[NHB][2], l_part[NHB][2];  // per head 2c + j of each head block
+#pragma unroll
+        for (int hb = 0; hb < NHB; ++hb) {
+            m_run[hb][0] = m_run[hb][1] = -INFINITY;
+            l_part[hb][0] = l_part[hb][1] = 0.f;
+        }
         int e_run = -1000000;  // exponent of the P . V factor 2^-e (per-token-head scales)
         float p_fac = 1.f;     // 2^-e_run
 
@@ -304,38 +341,35 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
             const uint8_t* kb = stages + stage * sbytes + hoff;
             const uint8_t* vb = kb + pbytes;
             const uint64_t vmask = mask_s[stage];
+            const bool v0 = (vmask >> g) & 1ull, v1 = (vmask >> (g + 8)) & 1ull;
 
-            // K and V scales of this lane's four token columns (nb * 8 + 2c + e);
-            // 0 for masked tokens
-            float ksc[4], vsc[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tok = (i >> 1) * 8 + 2 * c + (i & 1);
-                const bool v = (vmask >> tok) & 1ull;
-                if constexpr (C::kPth) {
-                    ksc[i] = v ? *reinterpret_cast<const float*>(kb + tok * rstride + D) : 0.f;
-                    vsc[i] = v ? *reinterpret_cast<const float*>(vb + tok * rstride + D) : 0.f;
-                } else {
-                    ksc[i] = 1.f;
-                    vsc[i] = 1.f;
-                }
+            // K and V scales of this lane's tokens g, g + 8 (0 when masked)
+            float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
+            if constexpr (C::kPth) {
+                ks0 = v0 ? *reinterpret_cast<const float*>(kb + g * rstride + D) : 0.f;
+                ks1 = v1 ? *reinterpret_cast<const float*>(kb + (g + 8) * rstride + D) : 0.f;
+                vs0 = v0 ? *reinterpret_cast<const float*>(vb + g * rstride + D) : 0.f;
+                vs1 = v1 ? *reinterpret_cast<const float*>(vb + (g + 8) * rstride + D) : 0.f;
             }
             __syncwarp();  // the previous tile's ldmatrix reads of wv are done
             widen_rows<D, KIND>(vb, wv, vmask, rstride, lane);
 
-            // S = Q K^T: token n = nb * 8 + g, one 4-byte read of its codes
-            // per step (masked tokens' columns are discarded below)
-            float s[2][4];
+            // S^T = K Q^T; A = the codes of tokens g and g + 8, one 4-byte read
+            // each per step (masked tokens' rows are discarded below); two
+            // accumulators per head block halve the dependent MMA chain
+            float st[NHB][2][4];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+            for (int hb = 0; hb < NHB; ++hb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) st[hb][e][0] = st[hb][e][1] = st[hb][e][2] = st[hb][e][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < C::kKSteps; ++ks) {
+                const uint2 k0 = widen4<KIND>(*reinterpret_cast<const uint32_t*>(kb + g * rstride + ks * 16 + 4 * c));
+                const uint2 k1 =
+                    widen4<KIND>(*reinterpret_cast<const uint32_t*>(kb + (g + 8) * rstride + ks * 16 + 4 * c));
+                const uint32_t af[4] = {k0.x, k1.x, k0.y, k1.y};
 #pragma unroll
-                for (int nb = 0; nb < 2; ++nb) {
-                    const uint32_t w = *reinterpret_cast<const uint32_t*>(kb + (nb * 8 + g) * rstride + ks * 16 + 4 * c);
-                    const uint2 kf = widen4<KIND>(w);
-                    mma_f16_16816(s[nb], qa[ks], kf.x, kf.y);
-                }
+                for (int hb = 0; hb < NHB; ++hb) mma_f16_16816(st[hb][ks & 1], af, qb[hb][ks][0], qb[hb][ks][1]);
             }
             __syncwarp();  // every lane's K reads and V tile writes are done
             if (lane == 0) mbar_arrive(&empty[stage]);
@@ -346,9 +380,10 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
             // P . V factor: grows with the largest |V scale| of the piece
             float o_fix = 1.f;
             if constexpr (C::kPth) {
-                float vmax = fmaxf(fmaxf(fabsf(vsc[0]), fabsf(vsc[1])), fmaxf(fabsf(vsc[2]), fabsf(vsc[3])));
-                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
-                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+                float vmax = fmaxf(fabsf(vs0), fabsf(vs1));
+                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
+                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 8));
+                vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 16));
                 if (vmax > 0.f && vmax <= 3.0e38f) {
                     const int e = scale_exponent(vmax);
                     if (e > e_run) {
@@ -357,68 +392,74 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
                         p_fac = ldexpf(1.f, -e);
                     }
                 }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) vsc[i] *= p_fac;
+                vs0 *= p_fac;
+                vs1 *= p_fac;
             }
+            const float kx0 = ks0 * a.sl2, kx1 = ks1 * a.sl2;
 
-            // online softmax; rows g (values 0,1) and g+8 (values 2,3)
-            float x[2][4];
-            float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-            for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int tok = nb * 8 + 2 * c + (j & 1);
-                    const bool valid = (vmask >> tok) & 1ull;
-                    x[nb][j] = valid ? s[nb][j] * ksc[nb * 2 + (j & 1)] * a.sl2 : -INFINITY;
-                    mx[j >> 1] = fmaxf(mx[j >> 1], x[nb][j]);
-                }
-            float alpha[2] = {1.f, 1.f};
+            // online softmax per head (column of S^T), over the 16 tokens
+            uint32_t pb[NHB][2];
+            float alpha[NHB][2];
             bool grow = false;
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-                mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-                // lazy: move the reference only when P would exceed 2^8
-                if (mx[r] > m_run[r] + 8.f) {
-                    alpha[r] = ex2(m_run[r] - mx[r]);
-                    m_run[r] = mx[r];
-                    l_part[r] *= alpha[r];
-                    grow = true;
-                }
-            }
-            const float m_use0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
-            const float m_use1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
-            uint32_t pa[4];
+            for (int hb = 0; hb < NHB; ++hb) {
+                float x[4];
+                x[0] = v0 ? (st[hb][0][0] + st[hb][1][0]) * kx0 : -INFINITY;  // token g, head 2c
+                x[1] = v0 ? (st[hb][0][1] + st[hb][1][1]) * kx0 : -INFINITY;  // token g, head 2c + 1
+                x[2] = v1 ? (st[hb][0][2] + st[hb][1][2]) * kx1 : -INFINITY;  // token g + 8, head 2c
+                x[3] = v1 ? (st[hb][0][3] + st[hb][1][3]) * kx1 : -INFINITY;
+                float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
 #pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
+                for (int j = 0; j < 2; ++j) {
+                    mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
+                    mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
+                    mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
+                    alpha[hb][j] = 1.f;
+                    // lazy: move the reference only when P would exceed 2^8
+                    if (mx[j] > m_run[hb][j] + 8.f) {
+                        alpha[hb][j] = ex2(m_run[hb][j] - mx[j]);
+                        m_run[hb][j] = mx[j];
+                        l_part[hb][j] *= alpha[hb][j];
+                        grow = true;
+                    }
+                }
+                const float mu0 = m_run[hb][0] == -INFINITY ? 0.f : m_run[hb][0];
+                const float mu1 = m_run[hb][1] == -INFINITY ? 0.f : m_run[hb][1];
+                const float p0 = ex2(x[0] - mu0), p1 = ex2(x[1] - mu1);
+                const float p2 = ex2(x[2] - mu0), p3 = ex2(x[3] - mu1);
                 // l sums the fp32 probabilities; P.V takes them times the V
                 // scale of their token and 2^-e_run, rounded to f16
-                const float p0 = ex2(x[nb][0] - m_use0), p1 = ex2(x[nb][1] - m_use0);
-                const float p2 = ex2(x[nb][2] - m_use1), p3 = ex2(x[nb][3] - m_use1);
-                l_part[0] += p0 + p1;
-                l_part[1] += p2 + p3;
-                pa[2 * nb] = pack_f16x2(p0 * vsc[2 * nb], p1 * vsc[2 * nb + 1]);
-                pa[2 * nb + 1] = pack_f16x2(p2 * vsc[2 * nb], p3 * vsc[2 * nb + 1]);
+                l_part[hb][0] += p0 + p2;
+                l_part[hb][1] += p1 + p3;
+                // P^T rows g and g + 8 -> the B operand (tokens 2c, 2c + 1 and
+                // 2c + 8, 2c + 9 of head g) by an 8x8 transpose each
+                pb[hb][0] = movmatrix_t(pack_f16x2(p0 * vs0, p1 * vs0));
+                pb[hb][1] = movmatrix_t(pack_f16x2(p2 * vs1, p3 * vs1));
             }
             if (__any_sync(0xffffffffu, grow) || o_fix != 1.f) {
-                const float oa0 = alpha[0] * o_fix, oa1 = alpha[1] * o_fix;
 #pragma unroll
-                for (int i = 0; i < C::kNb; ++i) {
-                    o[i][0] *= oa0;
-                    o[i][1] *= oa0;
-                    o[i][2] *= oa1;
-                    o[i][3] *= oa1;
+                for (int hb = 0; hb < NHB; ++hb) {
+                    const float f0 = alpha[hb][0] * o_fix, f1 = alpha[hb][1] * o_fix;
+#pragma unroll
+                    for (int mb = 0; mb < C::kKSteps; ++mb) {
+                        o[hb][mb][0] *= f0;
+                        o[hb][mb][1] *= f1;
+                        o[hb][mb][2] *= f0;
+                        o[hb][mb][3] *= f1;
+                    }
                 }
             }
+            // O^T += V^T P^T: A = V^T from the widened tile (16 head dims x 16
+            // tokens per ldmatrix.x4.trans), B = P^T
 #pragma unroll
-            for (int nb2 = 0; nb2 < C::kNb / 2; ++nb2) {
-                const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int col = nb2 * 16 + (lane >> 4) * 8;
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(b0, b1, b2, b3, wv + tok * C::kWStride + col * 2);
-                mma_f16_16816(o[2 * nb2], pa, b0, b1);
-                mma_f16_16816(o[2 * nb2 + 1], pa, b2, b3);
+            for (int mb = 0; mb < C::kKSteps; ++mb) {
+                const int q = lane >> 3;
+                const int tok = (lane & 7) + (q >> 1) * 8;
+                const int col = mb * 16 + (q & 1) * 8;
+                uint32_t av[4];
+                ldsm_x4_t(av[0], av[1], av[2], av[3], wv + tok * C::kWStride + col * 2);
+#pragma unroll
+                for (int hb = 0; hb < NHB; ++hb) mma_f16_16816(o[hb][mb], av, pb[hb][0], pb[hb][1]);
             }
             if (!ok) {
                 aborted = true;
@@ -427,62 +468,63 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), 1)
         }
         if (aborted) break;
 
-        float l[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            l[r] = l_part[r];
-            l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-            l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-        }
-        // undo the P . V factor 2^-e_run (per-token-head scales)
+        // epilogue: head hb * 8 + 2c + j, head dims 16 mb + g (+ 8)
         const float osc = (C::kPth && e_run != -1000000) ? ldexpf(out_scale, e_run) : out_scale;
-        const float i0 = l[0] > 0.f ? osc / l[0] : 0.f, i1 = l[1] > 0.f ? osc / l[1] : 0.f;
-        const int hr0 = hq0 + g, hr1 = hq0 + g + 8;
 #pragma unroll
-        for (int i = 0; i < C::kNb; ++i) {
-            const int col = i * 8 + 2 * c;
-            if (pc.whole) {
-                if (row0)
-                    *reinterpret_cast<uint32_t*>(a.out + (static_cast<long long>(pc.b) * a.Hq + hr0) * D + col) =
-                        pack_bf16x2(o[i][0] * i0, o[i][1] * i0);
-                if (row1)
-                    *reinterpret_cast<uint32_t*>(a.out + (static_cast<long long>(pc.b) * a.Hq + hr1) * D + col) =
-                        pack_bf16x2(o[i][2] * i1, o[i][3] * i1);
-            } else {
-                if (row0)
-                    *reinterpret_cast<float2*>(a.ws_o + (static_cast<long long>(pc.slot) * a.Hq + hr0) * D + col) =
-                        make_float2(o[i][0] * i0, o[i][1] * i0);
-                if (row1)
-                    *reinterpret_cast<float2*>(a.ws_o + (static_cast<long long>(pc.slot) * a.Hq + hr1) * D + col) =
-                        make_float2(o[i][2] * i1, o[i][3] * i1);
+        for (int hb = 0; hb < NHB; ++hb) {
+            float inv[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float l = l_part[hb][j];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                inv[j] = l > 0.f ? osc / l : 0.f;
+                const int h = hb * 8 + 2 * c + j;
+                if (g == 0 && h < grp) {
+                    const float lse = l > 0.f ? (m_run[hb][j] + log2f(l)) * kLn2 : -INFINITY;
+                    if (pc.whole) {
+                        if (a.lse) a.lse[static_cast<long long>(pc.b) * a.Hq + hq0 + h] = lse;
+                    } else {
+                        a.ws_lse[static_cast<long long>(pc.slot) * a.Hq + hq0 + h] = lse;
+                    }
+                }
             }
-        }
-        if (c == 0) {
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const bool have = r == 0 ? row0 : row1;
-                if (!have) continue;
-                const int hr = r == 0 ? hr0 : hr1;
-                const float lse = l[r] > 0.f ? (m_run[r] + log2f(l[r])) * kLn2 : -INFINITY;
+            for (int j = 0; j < 2; ++j) {
+                const int h = hb * 8 + 2 * c + j;
+                if (h >= grp) continue;
                 if (pc.whole) {
-                    if (a.lse) a.lse[static_cast<long long>(pc.b) * a.Hq + hr] = lse;
+                    __nv_bfloat16* orow = a.out + (static_cast<long long>(pc.b) * a.Hq + hq0 + h) * D;
+#pragma unroll
+                    for (int mb = 0; mb < C::kKSteps; ++mb) {
+                        orow[mb * 16 + g] = __float2bfloat16_rn(o[hb][mb][j] * inv[j]);
+                        orow[mb * 16 + g + 8] = __float2bfloat16_rn(o[hb][mb][2 + j] * inv[j]);
+                    }
                 } else {
-                    a.ws_lse[static_cast<long long>(pc.slot) * a.Hq + hr] = lse;
+                    float* wrow = a.ws_o + (static_cast<long long>(pc.slot) * a.Hq + hq0 + h) * D;
+#pragma unroll
+                    for (int mb = 0; mb < C::kKSteps; ++mb) {
+                        wrow[mb * 16 + g] = o[hb][mb][j] * inv[j];
+                        wrow[mb * 16 + g + 8] = o[hb][mb][2 + j] * inv[j];
+                    }
                 }
             }
         }
     }
 }
 
-// Dynamic shared memory a block may use on sm_103a (227 KB).
-constexpr size_t kSmemLimit = 227 * 1024;
+// Dynamic shared memory a block may use: 227 KB on sm_103a, or its share of
+// the SM's 228 KB (less 1 KB reserved per block) with several blocks per SM.
+constexpr size_t smem_limit(int ctas) { return ctas == 1 ? 227 * 1024 : (228 * 1024) / ctas - 1024; }
 
 template <int D, int KIND>
 cudaError_t launch_q8(const GqaArgs& a, float out_scale, int grid, cudaStream_t stream) {
     using C = GqaQ8Cfg<D, KIND>;
-    const int ns = C::stages_for(a.Hkv, a.plan.batch, kSmemLimit);
+    const int nhb = (a.Hq / a.Hkv) <= 8 ? 1 : 2;
+    const int ns = C::stages_for(a.Hkv, a.plan.batch, smem_limit(q8_ctas(nhb)));
     const size_t smem = C::smem_bytes(a.Hkv, ns, a.plan.batch);
-    auto kern = gqa_decode_q8_kernel<D, KIND>;
+    auto kern = nhb == 1 ? gqa_decode_q8_kernel<D, KIND, 1> : gqa_decode_q8_kernel<D, KIND, 2>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -499,16 +541,17 @@ cudaError_t launch_q8_kind(const GqaArgs& a, float out_scale, int kind, int grid
 }
 
 template <int D, int KIND>
-size_t smem_of(int hkv, int batch) {
+size_t smem_of(int hkv, int q_per_kv, int batch) {
     using C = GqaQ8Cfg<D, KIND>;
-    return C::smem_bytes(hkv, C::stages_for(hkv, batch, kSmemLimit), batch);
+    const int ctas = q8_ctas(q_per_kv <= 8 ? 1 : 2);
+    return C::smem_bytes(hkv, C::stages_for(hkv, batch, smem_limit(ctas)), batch);
 }
 
 template <int D>
-size_t smem_kind(int kind, int hkv, int batch) {
-    if (kind == kFmtE4m3Pth) return smem_of<D, kFmtE4m3Pth>(hkv, batch);
-    if (kind == kFmtInt8Pth) return smem_of<D, kFmtInt8Pth>(hkv, batch);
-    return smem_of<D, kFmtE4m3>(hkv, batch);
+size_t smem_kind(int kind, int hkv, int q_per_kv, int batch) {
+    if (kind == kFmtE4m3Pth) return smem_of<D, kFmtE4m3Pth>(hkv, q_per_kv, batch);
+    if (kind == kFmtInt8Pth) return smem_of<D, kFmtInt8Pth>(hkv, q_per_kv, batch);
+    return smem_of<D, kFmtE4m3>(hkv, q_per_kv, batch);
 }
 
 }  // namespace
@@ -518,8 +561,10 @@ cudaError_t gqa_q8_stage1(const GqaArgs& a, float out_scale, int D, int kind, in
     return launch_q8_kind<64>(a, out_scale, kind, grid, stream);
 }
 
-size_t gqa_q8_smem_bytes(int D, int kind, int hkv, int batch) {
-    return D == 128 ? smem_kind<128>(kind, hkv, batch) : smem_kind<64>(kind, hkv, batch);
+int gqa_q8_ctas_per_sm(int q_per_kv) { return q8_ctas(q_per_kv <= 8 ? 1 : 2); }
+
+size_t gqa_q8_smem_bytes(int D, int kind, int hkv, int q_per_kv, int batch) {
+    return D == 128 ? smem_kind<128>(kind, hkv, q_per_kv, batch) : smem_kind<64>(kind, hkv, q_per_kv, batch);
 }
 
 }  // namespace mqa

@@ -12,6 +12,9 @@ namespace mqa {
 // out_scale multiplies the output (v_scale for format 1, 1 otherwise); the
 // softmax scale in a.sl2 already holds k_scale for format 1.
 cudaError_t gqa_q8_stage1(const GqaArgs& a, float out_scale, int D, int kind, int grid, cudaStream_t stream);
-size_t gqa_q8_smem_bytes(int D, int kind, int hkv, int batch);
+size_t gqa_q8_smem_bytes(int D, int kind, int hkv, int q_per_kv, int batch);
+// Blocks of the kernel resident per SM (2 for up to 8 query heads per KV
+// head, else 1): the balanced plan should make that many units per SM.
+int gqa_q8_ctas_per_sm(int q_per_kv);
 
 }  // namespace mqa
