@@ -51,7 +51,7 @@ MMA_FILES = ("mla_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
 TC_FILES = ("mla_tc.cu", "tc_ptx.cuh", "common.cuh", "plan.cuh", "args.cuh")
 Q8_FILES = ("gqa_q8.cu", "gqa_q8.cuh", "common.cuh", "plan.cuh", "args.cuh")
 NCU_TRAFFIC = {
-    "mla_v2lite": {"files": MMA_FILES, "src_sha": "8b3793aae17c641a", "splits": 16, "bytes": 329795584 + 3738368,
+    "mla_v2lite": {"files": MMA_FILES, "src_sha": "fd8f4fa37c70f883", "splits": 16, "bytes": 329830656 + 3700992,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64>"},
     "mla_longctx": {"files": TC_FILES, "src_sha": "db7d88cc3b68ce52", "splits": 256, "bytes": 485207808 + 4084992,
                     "kernel": "mla_decode_tc_kernel<576,512,0>"},
@@ -61,7 +61,7 @@ NCU_TRAFFIC = {
                     "kernel": "gqa_decode_q8_kernel<128,2,1>"},
     "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "8566ab172970c1e5", "splits": 32, "bytes": 1689826560 + 5800192,
                      "kernel": "gqa_decode_q8_kernel<128,3,1>"},
-    "mla_sparse": {"files": MMA_FILES, "src_sha": "8b3793aae17c641a", "splits": 4, "bytes": 152913664 + 3286528,
+    "mla_sparse": {"files": MMA_FILES, "src_sha": "fd8f4fa37c70f883", "splits": 4, "bytes": 152898560 + 3114496,
                    "kernel": "mla_decode_mma_kernel<576,512,0,32,0,1>"},
 }
 

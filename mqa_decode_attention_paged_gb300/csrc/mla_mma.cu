@@ -140,75 +140,86 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
             // Sparse decode: a tile is kTile entries of the request's index
             // list; lane l gathers rows l, l + 32, each whole cache row by one
             // bulk copy (rows are D * elt bytes: 16-byte aligned) into the
-            // unswizzled stage.  The rows of the next tile are looked up
-            // (index, then block table) one tile ahead.  Entries outside
-            // [0, seq_len) select nothing; bad block ids are reported.
+            // unswizzled stage.  The two dependent lookups of a row (its
+            // index entry, then its block id) are spread over the two tiles
+            // before its own: in the turn of tile i the producer reads the
+            // entries of tile i + 2, the block ids of tile i + 1 and copies
+            // tile i, so no read waits on another within one turn.  Entries
+            // outside [0, seq_len) select nothing; bad block ids are reported.
             static_assert(C::kTile % 32 == 0, "whole warps of rows");
             constexpr int kPer = C::kTile / 32;
             constexpr int kRowBytes = D * (FP8 ? 1 : 2);
+            const long long cap = static_cast<long long>(a.bt_stride) * a.cache_page;
+            struct Look {
+                int b, n;        // request and its length (seq_lens[b])
+                int pos[kPer];   // selected position, -1 for none
+                int blk[kPer];   // block id of the position's page
+                bool val[kPer];  // position selects a row of a mapped page
+            };
+            // first lookup: the tile's entries and its request's length
+            auto read_entries = [&](const TileCursor& tc, Look& L) {
+                L.b = tc.pc.b;
+                L.n = __ldg(a.seq_lens + L.b);
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const int e = tc.t0 + lane + 32 * k;
+                    L.pos[k] = e < tc.tok_end ? __ldg(a.indices + static_cast<long long>(L.b) * a.topk + e) : -1;
+                }
+            };
+            // second lookup: the block ids of the selected positions
+            auto read_blocks = [&](Look& L) {
+                if (L.n < 0 && lane == 0) report(a.status, MQA_ERR_DEVICE_CHECK);
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const int pos = L.pos[k];
+                    bool v = pos >= 0 && pos < L.n;
+                    if (v && pos >= cap) {
+                        // below the length but beyond what the block table maps
+                        report(a.status, MQA_ERR_DEVICE_CHECK);
+                        v = false;
+                    }
+                    L.val[k] = v;
+                    L.blk[k] = v ? __ldg(a.block_table + static_cast<long long>(L.b) * a.bt_stride + pos / a.cache_page)
+                                 : 0;
+                }
+            };
             TileCursor cur;
             cur.init(a.plan, cum, T, unit, C::kTile);
             int stage = 0;
             uint32_t phase = 0;
             int issued[C::kStages];
             for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
-            auto lookup = [&](const TileCursor& tc, const uint8_t* (&src)[kPer], bool (&val)[kPer]) {
-                const int b = tc.pc.b;
-                const long long cap = static_cast<long long>(a.bt_stride) * a.cache_page;
-                const int n = __ldg(a.seq_lens + b);
-                if (n < 0 && lane == 0) report(a.status, MQA_ERR_DEVICE_CHECK);
-#pragma unroll
-                for (int k = 0; k < kPer; ++k) {
-                    const int e = tc.t0 + lane + 32 * k;
-                    bool v = e < tc.tok_end;
-                    const int pos = v ? __ldg(a.indices + static_cast<long long>(b) * a.topk + e) : -1;
-                    v = v && pos >= 0 && pos < n;
-                    if (v && pos >= cap) {
-                        // below the length but beyond what the block table maps
-                        report(a.status, MQA_ERR_DEVICE_CHECK);
-                        v = false;
-                    }
-                    int blk = 0;
-                    if (v) {
-                        blk = __ldg(a.block_table + static_cast<long long>(b) * a.bt_stride + pos / a.cache_page);
-                        if (blk < 0 || blk >= a.num_blocks) {
-                            report(a.status, MQA_ERR_DEVICE_CHECK);
-                            v = false;
-                        }
-                    }
-                    val[k] = v;
-                    src[k] = a.kv + (static_cast<long long>(v ? blk : 0) * a.cache_page + (v ? pos % a.cache_page : 0)) *
-                                        kRowBytes;
-                }
-            };
-            bool have = cur.next(a.plan, cum, lens, a.block_table);
-            const uint8_t* src[kPer];
-            bool val[kPer];
-#pragma unroll
-            for (int k = 0; k < kPer; ++k) {
-                src[k] = a.kv;
-                val[k] = false;
-            }
-            if (have) lookup(cur, src, val);
-            while (have) {
-                const bool have_next = cur.next(a.plan, cum, lens, a.block_table);
-                const uint8_t* nsrc[kPer];
-                bool nval[kPer];
-#pragma unroll
-                for (int k = 0; k < kPer; ++k) {
-                    nsrc[k] = a.kv;
-                    nval[k] = false;
-                }
-                if (have_next) lookup(cur, nsrc, nval);
+            Look L0, L1, L2;
+            bool h0 = cur.next(a.plan, cum, lens, a.block_table);
+            if (h0) read_entries(cur, L0);
+            bool h1 = h0 && cur.next(a.plan, cum, lens, a.block_table);
+            if (h1) read_entries(cur, L1);
+            if (h0) read_blocks(L0);
+            bool h2 = h1 && cur.next(a.plan, cum, lens, a.block_table);
+            if (h2) read_entries(cur, L2);
+            while (h0) {
+                if (h1) read_blocks(L1);
                 if (!mbar_wait(&empty[stage], phase ^ 1)) {
                     report(a.status, MQA_ERR_DEVICE_TIMEOUT);
                     break;
                 }
                 uint8_t* dst = stages + stage * C::kStageBytes;
+                const uint8_t* src[kPer];
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    bool v = L0.val[k];
+                    if (v && (L0.blk[k] < 0 || L0.blk[k] >= a.num_blocks)) {
+                        report(a.status, MQA_ERR_DEVICE_CHECK);
+                        v = false;
+                    }
+                    L0.val[k] = v;
+                    src[k] = a.kv + (static_cast<long long>(v ? L0.blk[k] : 0) * a.cache_page +
+                                     (v ? L0.pos[k] % a.cache_page : 0)) * kRowBytes;
+                }
                 uint64_t vmask = 0;
 #pragma unroll
                 for (int k = 0; k < kPer; ++k)
-                    vmask |= static_cast<uint64_t>(__ballot_sync(0xffffffffu, val[k])) << (32 * k);
+                    vmask |= static_cast<uint64_t>(__ballot_sync(0xffffffffu, L0.val[k])) << (32 * k);
                 if (lane == 0) {
                     mask_s[stage] = vmask;
                     mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(__popcll(vmask)) * kRowBytes);
@@ -216,18 +227,18 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
                 __syncwarp();
 #pragma unroll
                 for (int k = 0; k < kPer; ++k)
-                    if (val[k]) bulk_g2s(dst + (lane + 32 * k) * kRowBytes, src[k], kRowBytes, &full[stage], pol);
+                    if (L0.val[k]) bulk_g2s(dst + (lane + 32 * k) * kRowBytes, src[k], kRowBytes, &full[stage], pol);
                 issued[stage] = static_cast<int>(phase);
                 if (++stage == C::kStages) {
                     stage = 0;
                     phase ^= 1;
                 }
-                have = have_next;
-#pragma unroll
-                for (int k = 0; k < kPer; ++k) {
-                    src[k] = nsrc[k];
-                    val[k] = nval[k];
-                }
+                L0 = L1;
+                L1 = L2;
+                h0 = h1;
+                h1 = h2;
+                h2 = h1 && cur.next(a.plan, cum, lens, a.block_table);
+                if (h2) read_entries(cur, L2);
             }
             for (int s = 0; s < C::kStages; ++s)
                 if (issued[s] >= 0 && !mbar_wait(&full[s], static_cast<uint32_t>(issued[s])))
