@@ -268,9 +268,21 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
+    import oracle
     from mqa_decode_attention_paged_gb300 import synth
     case = synth.workload(args.workload)
-    splits = args.splits or 1
+    # The oracle computes the direct definition whatever the split count; the
+    # line names the split count the GPU arm uses on this machine (the heuristic
+    # with the device's SM count, 152 on a GB300 when no device is visible)
+    # so that both arms describe the same workload.
+    idx = case.meta.get("indices")
+    split_len = idx.shape[1] if idx is not None else int(case.seq_lens.max())
+    try:
+        import torch
+        sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+    except Exception:
+        sms = 152
+    splits = args.splits or oracle.num_kv_splits(split_len, sms, False)
     st = workload_stats(case, splits)
     times = []
     tokens = 0
