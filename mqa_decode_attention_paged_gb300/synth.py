@@ -298,6 +298,32 @@ def workload(name: str, **overrides) -> PagedCase:
     return make_gqa_case(**spec)
 
 
+def shard_case(case: PagedCase, num_shards: int) -> list:
+    """Cut every sequence of `case` into `num_shards` page-aligned shards, as
+    decode context parallelism places a request's KV pages on several ranks:
+    shard g of a sequence with n tokens (np pages) holds pages
+    [g L, min((g + 1) L, np)), L = ceil(np / num_shards).  Returns one case
+    per shard with the same q and cache, the shard's block-table columns and
+    its token count (0 for a shard past the end)."""
+    P = case.page
+    n = case.seq_lens.astype(np.int64)
+    npg = (n + P - 1) // P
+    L = np.maximum((npg + num_shards - 1) // num_shards, 1)
+    width = int(L.max()) if len(L) else 1
+    shards = []
+    for g in range(num_shards):
+        table = np.full((case.batch, width), -1, dtype=np.int32)
+        sl = np.zeros(case.batch, dtype=np.int32)
+        for b in range(case.batch):
+            j0 = int(g * L[b])
+            j1 = int(min((g + 1) * L[b], npg[b]))
+            if j1 > j0:
+                table[b, :j1 - j0] = case.block_table[b, j0:j1]
+                sl[b] = int(min(j1 * P, n[b]) - j0 * P)
+        shards.append(replace(case, block_table=table, seq_lens=sl))
+    return shards
+
+
 def poison(case: PagedCase, table_fill: int = -1) -> PagedCase:
     """Copy of `case` with NaN in every cache slot no valid token owns (tail
     slots of last pages and unreferenced blocks) and `table_fill` in every

@@ -86,6 +86,7 @@ def _load():
         lib.oracle_gqa_paged_decode_pth.restype = I
         lib.oracle_gqa_paged_decode_pth.argtypes = [P, P, I, P, P, D, P, P, I, I, I, I, I, I, I]
         lib.oracle_int8_values.argtypes = [P, P, I64]
+        lib.oracle_lse_merge.argtypes = [P, P, P, P, I, I, I, I]
         _lib = lib
         return lib
 
@@ -284,4 +285,18 @@ def _gqa_pth(q, kv, kv_dtype, block_table, seq_lens, scale):
                                              bt.shape[1])
     if rc != 0:
         raise ValueError("oracle: bad block table or head counts")
+    return out, lse
+
+
+def lse_merge(outs, lses):
+    """Merge shard results: outs [G, B, H, R] (normalised), lses [G, B, H]
+    (natural log, -inf for an empty shard); returns (out [B, H, R], lse [B, H])."""
+    o = np.ascontiguousarray(outs, dtype=np.float64)
+    l = np.ascontiguousarray(lses, dtype=np.float64)
+    G, B, H, R = o.shape
+    if l.shape != (G, B, H):
+        raise ValueError("lses must be [G, B, H]")
+    out = np.zeros((B, H, R), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    _load().oracle_lse_merge(_ptr(o), _ptr(l), _ptr(out), _ptr(lse), G, B, H, R)
     return out, lse

@@ -50,6 +50,14 @@
  *   and the request's top-k logical positions converted to physical KV
  *   slots through its block table).
  *
+ *   Merging the results of sequence shards (decode context parallelism): each
+ *   shard g of a request's KV cache gives its normalised output O_g and its
+ *   lse_g; with m = max_g lse_g the merged result is
+ *   O = sum_g e^{lse_g - m} O_g / sum_g e^{lse_g - m}, lse = m + ln sum_g
+ *   e^{lse_g - m}.  Source: tutorial page §12 (the split-KV merge written for
+ *   normalised partials) and the "Triton と MLA" page, 設計動機 (lse is
+ *   returned so that DCP shards can be merged by cp_lse_ag_out_rs).
+ *
  *   GQA paged decode over a [num_blocks, 2, page, num_kv_heads, head_size]
  *   cache.  Source: "AttentionBackend" page (vllm-arch-zh, fr/attention/backend),
  *   section "Motivation de conception" (FlashAttention cache layout).
@@ -621,4 +629,36 @@ int oracle_gqa_paged_decode_pth(const uint16_t* q, const uint8_t* kv, int kind,
         free(s);
     }
     return failed ? -1 : 0;
+}
+
+/* ---- merge of shard results ---------------------------------------------- */
+
+/* outs: [G, B, H, R] normalised shard outputs; lses: [G, B, H] natural-log
+ * LSEs (-inf for a shard with no token); out: [B, H, R]; lse: [B, H].  A shard
+ * whose lse is -inf has weight 0 and its output is not read. */
+void oracle_lse_merge(const double* outs, const double* lses, double* out, double* lse, int G, int B,
+                      int H, int R) {
+    int64_t rows = (int64_t)B * H;
+    for (int64_t row = 0; row < rows; ++row) {
+        double m = -INFINITY;
+        for (int g = 0; g < G; ++g)
+            if (lses[(int64_t)g * rows + row] > m) m = lses[(int64_t)g * rows + row];
+        double* o = out + row * R;
+        for (int r = 0; r < R; ++r) o[r] = 0.0;
+        if (m == -INFINITY) {
+            lse[row] = -INFINITY;
+            continue;
+        }
+        double wsum = 0.0;
+        for (int g = 0; g < G; ++g) {
+            double lg = lses[(int64_t)g * rows + row];
+            if (lg == -INFINITY) continue;
+            double w = exp(lg - m);
+            wsum += w;
+            const double* og = outs + ((int64_t)g * rows + row) * R;
+            for (int r = 0; r < R; ++r) o[r] += w * og[r];
+        }
+        for (int r = 0; r < R; ++r) o[r] /= wsum;
+        lse[row] = m + log(wsum);
+    }
 }
