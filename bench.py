@@ -50,6 +50,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 MMA_FILES = ("mla_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
 TC_FILES = ("mla_tc.cu", "tc_ptx.cuh", "common.cuh", "plan.cuh", "args.cuh")
 Q8_FILES = ("gqa_q8.cu", "gqa_q8.cuh", "common.cuh", "plan.cuh", "args.cuh")
+MERGE_FILES = ("shard_merge.cu", "shard_merge.cuh", "common.cuh")
 NCU_TRAFFIC = {
     "mla_v2lite": {"files": MMA_FILES, "src_sha": "fd8f4fa37c70f883", "splits": 16, "bytes": 329830656 + 3700992,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64>"},
@@ -61,6 +62,8 @@ NCU_TRAFFIC = {
                     "kernel": "gqa_decode_q8_kernel<128,2,1>"},
     "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "8566ab172970c1e5", "splits": 32, "bytes": 1689826560 + 5800192,
                      "kernel": "gqa_decode_q8_kernel<128,3,1>"},
+    "dcp_merge_v3": {"files": MERGE_FILES, "src_sha": "8c157f962d4da4f4", "bytes": 126340608 + 7121920,
+                     "kernel": "shard_merge_kernel"},
     "mla_sparse": {"files": MMA_FILES, "src_sha": "fd8f4fa37c70f883", "splits": 4, "bytes": 152898560 + 3114496,
                    "kernel": "mla_decode_mma_kernel<576,512,0,32,0,1>"},
 }
@@ -310,6 +313,181 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# Merge of sequence-shard results (decode context parallelism): the shards'
+# (output, lse) of the V3-like batch (B=128, H=128, R=512) spread over 8 ranks,
+# gathered on one GPU and merged.  Shard outputs ~ N(0,1) in bf16, lse ~
+# N(10, 3) with 1/16 of the (shard, row) pairs empty (lse = -inf).
+MERGE_WORKLOADS = {"dcp_merge_v3": dict(G=8, B=128, H=128, R=512, seed=1010)}
+
+
+def merge_inputs(spec):
+    rng = np.random.default_rng(spec["seed"])
+    G, rows, R = spec["G"], spec["B"] * spec["H"], spec["R"]
+    from mqa_decode_attention_paged_gb300 import synth
+    outs = synth.to_bf16_bits(rng.standard_normal((G, rows, R), dtype=np.float32))
+    lses = (10.0 + 3.0 * rng.standard_normal((G, rows))).astype(np.float32)
+    lses[rng.random((G, rows)) < 1.0 / 16] = -np.inf
+    return outs, lses
+
+
+def merge_stats(spec):
+    G, rows, R = spec["G"], spec["B"] * spec["H"], spec["R"]
+    alg = G * rows * R * 2 + G * rows * 4 + rows * R * 2 + rows * 4
+    return dict(alg_bytes=alg, in_bytes=G * rows * R * 2 + G * rows * 4, out_bytes=rows * R * 2 + rows * 4)
+
+
+def merge_config(name, spec):
+    return {"workload": name, "kind": "lse_merge", "num_shards": spec["G"], "batch": spec["B"],
+            "num_heads": spec["H"], "head_dim": spec["R"], "seed": spec["seed"],
+            "l2": "flushed before every timed step: 256 MiB written then read back (cold, clean L2), "
+                  "outside the timed events"}
+
+
+def run_merge(args):
+    """Time mqa_lse_merge (ours) or the oracle's merge (reference) on a
+    merge workload; same JSON contract as the decode workloads."""
+    spec = MERGE_WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    st = merge_stats(spec)
+    outs_np, lses_np = merge_inputs(spec)
+    G, rows, R = spec["G"], spec["B"] * spec["H"], spec["R"]
+
+    def time_cpu(budget_s):
+        import oracle
+        n, done, t = 64, 0, 0.0
+        while t < budget_s and done < rows:
+            sel = slice(done, min(rows, done + n))
+            o = oracle.bf16_values(outs_np[:, sel])[:, :, None, :]
+            t0 = time.perf_counter()
+            oracle.lse_merge(o, lses_np[:, sel, None].astype(np.float64))
+            t += time.perf_counter() - t0
+            done = sel.stop
+            n *= 2
+        gbs = st["alg_bytes"] * done / rows / t / 1e9
+        return gbs, oracle.max_threads(), f"{done} of {rows} rows (all {G} shards)"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        vals = [time_cpu(args.ref_budget / max(1, args.steps)) for _ in range(max(1, args.steps))]
+        gbs = statistics.median(v[0] for v in vals)
+        line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(st["alg_bytes"] / gbs / 1e6, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": merge_config(args.workload, spec),
+                "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": vals[0][1], "kind": "oracle",
+                                 "sample": vals[0][2] + " per step"},
+                "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from mqa_decode_attention_paged_gb300 import _binding as mqa
+    so = torch.from_numpy(outs_np.view(np.int16)).view(torch.bfloat16).to(dev)
+    sl = torch.from_numpy(lses_np).to(dev)
+    out = torch.empty((rows, R), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((rows,), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush32 = flush.view(torch.int32)
+    stream = torch.cuda.current_stream()
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+        flush32.max()
+
+    for i in range(args.warmup):
+        flush_l2(i)
+        mqa.lse_merge(so, sl, out=out, lse=lse, stream=stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    with sampler:
+        for i in range(args.steps):
+            flush_l2(i)
+            starts[i].record(stream)
+            mqa.lse_merge(so, sl, out=out, lse=lse, stream=stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    mean_ms = sum(s_.elapsed_time(e) for s_, e in zip(starts, ends)) / args.steps
+
+    # end to end: the gathered shard results copied in from pinned host
+    # memory, the merged output and lse copied back, every step
+    so_h = torch.from_numpy(outs_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    sl_h = torch.from_numpy(lses_np).pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    so_d, sl_d = torch.empty_like(so), torch.empty_like(sl)
+    e2e_steps = max(3, min(args.steps, 100))
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    for i in range(e2e_steps + 2):
+        flush_l2(i)
+        j = i - 2
+        if j >= 0:
+            es[j].record(stream)
+        so_d.copy_(so_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        mqa.lse_merge(so_d, sl_d, out=out, lse=lse, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        if j >= 0:
+            ee[j].record(stream)
+        stream.synchronize()
+    e2e_ms = sum(s_.elapsed_time(e) for s_, e in zip(es, ee)) / e2e_steps
+    mean_ms, e2e_ms = max_over_ranks([mean_ms, e2e_ms], dist, dev)
+
+    peaks, peak_src = load_peaks()
+    gbs = st["alg_bytes"] / (mean_ms * 1e-3) / 1e9
+    tr = NCU_TRAFFIC.get(args.workload)
+    traffic = tr["bytes"] if tr and tr.get("src_sha") == kernel_sources_sha(tr["files"]) else None
+    roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+            "traffic_kernel": "shard_merge_kernel" if traffic else None,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+            "kernel": "shard_merge_kernel (the whole call)", "alg_bytes_per_call": st["alg_bytes"],
+            "ideal_us": round(1e6 * st["alg_bytes"] / (peaks["hbm_gbs"] * 1e9), 2)}
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, cores, sample = time_cpu(args.ref_budget)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": METRIC, "value": round(job_throughput_gbs(world, st["alg_bytes"], mean_ms), 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_ms, 5),
+        "us_per_call": round(mean_ms * 1e3, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (fp32 sums)", "data": "synthetic (seeded N(0,1) shard outputs, N(10,3) lse, 1/16 empty)",
+        "config": merge_config(args.workload, spec), "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": round(job_throughput_gbs(world, st["alg_bytes"], e2e_ms), 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": st["in_bytes"],
+                "d2h_bytes_per_step": st["out_bytes"],
+                "note": "per step: the gathered shard outputs and lse host->device, the merged out and lse "
+                        "device->host (pinned host buffers)"},
+        "gpu_launches": args.steps, "clocks": sampler.summary(), "kernel_src_sha": kernel_sources_sha(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -515,7 +693,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.workload in MERGE_WORKLOADS:
+        run_merge(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

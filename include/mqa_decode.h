@@ -204,6 +204,28 @@ mqa_status mla_decode_sparse(const void* q, const void* kv_cache, const int32_t*
                              mqa_kv_dtype kv_dtype, int num_kv_splits, void* workspace,
                              size_t workspace_bytes, int* device_status, void* stream);
 
+/* Merge of sequence-shard results, the local step of decode context
+ * parallelism (DCP): a request's KV pages are spread over num_shards ranks,
+ * each rank decodes its shard (mla_decode / gqa_paged_decode on its pages,
+ * returning the shard's normalised output and natural-log lse), the caller
+ * gathers the shards' results (that exchange is the caller's), and this call
+ * merges them by LogSumExp: with m = max_g lse_g and w_g = e^{lse_g - m},
+ *   out = sum_g w_g out_g / sum_g w_g,   lse = m + ln sum_g w_g
+ * (tutorial page lshu.cn/news/265860, §12; the "Triton と MLA" page,
+ * 設計動機: lse is returned so that DCP shards can be merged,
+ * cp_lse_ag_out_rs).  A shard with lse_g = -inf (no token) has weight 0 and
+ * its output is not read; when every shard is empty, out = 0, lse = -inf.
+ *
+ *   shard_out  bf16 [num_shards, rows, head_dim], rows = batch * num_heads.
+ *   shard_lse  fp32 [num_shards, rows].
+ *   out        bf16 [rows, head_dim], fully written.
+ *   lse        fp32 [rows] or NULL.
+ *   num_shards >= 1, rows >= 1, head_dim a multiple of 8 in [8, 4096];
+ *   every pointer 16-byte aligned.  Fixed shard order: reproducible.
+ *   Allocates nothing; enqueues one kernel on `stream`. */
+mqa_status mqa_lse_merge(const void* shard_out, const float* shard_lse, void* out, float* lse, int num_shards,
+                         long long rows, int head_dim, void* stream);
+
 /* Size of the library-owned scratch array used by mla_decode_noalloc. */
 #define MQA_NOALLOC_SCRATCH_BYTES (64u << 20)
 

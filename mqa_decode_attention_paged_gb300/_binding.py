@@ -72,6 +72,8 @@ def _load() -> ctypes.CDLL:
     lib.mla_decode_noalloc.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, P]
     lib.gqa_paged_decode.restype = I
     lib.gqa_paged_decode.argtypes = [P, P, P, P, F, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
+    lib.mqa_lse_merge.restype = I
+    lib.mqa_lse_merge.argtypes = [P, P, P, P, I, ctypes.c_longlong, I, P]
     return lib
 
 
@@ -246,6 +248,31 @@ def gqa_paged_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, v_s
                               _stream(stream))
     if rc != OK:
         raise MqaError(rc, "gqa_paged_decode")
+    return out, lse
+
+
+def lse_merge(shard_out, shard_lse, *, out=None, lse=None, stream=None, return_lse=True):
+    """Merge sequence-shard results through the C ABI (decode context
+    parallelism, after the caller has gathered the shards): shard_out bf16
+    [G, ..., head_dim], shard_lse fp32 [G, ...]; returns (out [..., head_dim]
+    bf16, lse [...] fp32)."""
+    import torch
+    G = shard_out.shape[0]
+    D = shard_out.shape[-1]
+    lead = tuple(shard_out.shape[1:-1])
+    if tuple(shard_lse.shape) != (G,) + lead:
+        raise ValueError("shard_lse must be [num_shards, *shard_out.shape[1:-1]]")
+    rows = 1
+    for x in lead:
+        rows *= int(x)
+    if out is None:
+        out = torch.empty(lead + (D,), dtype=torch.bfloat16, device=shard_out.device)
+    if lse is None and return_lse:
+        lse = torch.empty(lead, dtype=torch.float32, device=shard_out.device)
+    rc = lib.mqa_lse_merge(_ptr(shard_out), _ptr(shard_lse), _ptr(out), _ptr(lse), int(G), rows, int(D),
+                           _stream(stream))
+    if rc != OK:
+        raise MqaError(rc, "mqa_lse_merge")
     return out, lse
 
 

@@ -12,6 +12,7 @@
 
 #include "args.cuh"
 #include "gqa_q8.cuh"
+#include "shard_merge.cuh"
 
 namespace {
 
@@ -555,6 +556,23 @@ mqa_status mla_decode_sparse(const void* q, const void* kv_cache, const int32_t*
         m.plan = a.plan;
         if (cudaError_t e = mqa::lse_merge(m, st); e != cudaSuccess) return cuda_fail(e);
     }
+    return MQA_OK;
+}
+
+mqa_status mqa_lse_merge(const void* shard_out, const float* shard_lse, void* out, float* lse, int num_shards,
+                         long long rows, int head_dim, void* stream) {
+    if (!shard_out || !shard_lse || !out) return MQA_ERR_INVALID_ARG;
+    if (!aligned(shard_out, 16) || !aligned(shard_lse, 16) || !aligned(out, 16) || (lse && !aligned(lse, 16)))
+        return MQA_ERR_INVALID_ARG;
+    if (num_shards < 1 || rows < 1 || head_dim < 8 || head_dim > 4096 || head_dim % 8 != 0)
+        return MQA_ERR_INVALID_ARG;
+    // grid of rows / 4 blocks
+    if (rows > 4LL * 0x7fffffffLL) return MQA_ERR_UNSUPPORTED;
+    if (cudaError_t e = mqa::shard_merge(static_cast<const __nv_bfloat16*>(shard_out), shard_lse,
+                                         static_cast<__nv_bfloat16*>(out), lse, num_shards, rows, head_dim,
+                                         static_cast<cudaStream_t>(stream));
+        e != cudaSuccess)
+        return cuda_fail(e);
     return MQA_OK;
 }
 

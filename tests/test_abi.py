@@ -30,7 +30,8 @@ def _declared_functions():
 
 def test_header_symbols_are_exported():
     names = _declared_functions()
-    assert {"mla_decode", "mla_decode_multi", "mla_decode_sparse", "gqa_paged_decode", "mqa_num_kv_splits", "mla_decode_workspace_bytes",
+    assert {"mla_decode", "mla_decode_multi", "mla_decode_sparse", "gqa_paged_decode", "mqa_lse_merge",
+            "mqa_num_kv_splits", "mla_decode_workspace_bytes",
             "gqa_paged_decode_workspace_bytes", "mqa_status_string", "mqa_abi_version",
             "mqa_device_sm_count"} <= set(names)
     lib = ctypes.CDLL(mqa.LIB_PATH)
@@ -183,3 +184,29 @@ def test_mla_validation(kw, code):
 ])
 def test_gqa_validation(kw, code):
     assert _gqa(**kw) == code
+
+
+def _merge(**kw):
+    a = dict(outs=FAKE, lses=FAKE, out=FAKE, lse=None, G=4, rows=64, D=512)
+    a.update(kw)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)  # noqa: E731
+    return mqa.lib.mqa_lse_merge(P(a["outs"]), P(a["lses"]), P(a["out"]), P(a["lse"]), a["G"], a["rows"], a["D"],
+                                 None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(outs=None), mqa.ERR_INVALID_ARG),
+    (dict(lses=None), mqa.ERR_INVALID_ARG),
+    (dict(out=None), mqa.ERR_INVALID_ARG),
+    (dict(outs=FAKE + 8), mqa.ERR_INVALID_ARG),         # 16-byte alignment
+    (dict(lses=FAKE + 4), mqa.ERR_INVALID_ARG),
+    (dict(lse=FAKE + 4), mqa.ERR_INVALID_ARG),
+    (dict(G=0), mqa.ERR_INVALID_ARG),
+    (dict(rows=0), mqa.ERR_INVALID_ARG),
+    (dict(D=4), mqa.ERR_INVALID_ARG),                   # head_dim a multiple of 8 in [8, 4096]
+    (dict(D=100), mqa.ERR_INVALID_ARG),
+    (dict(D=4104), mqa.ERR_INVALID_ARG),
+    (dict(rows=1 << 40), mqa.ERR_UNSUPPORTED),
+])
+def test_lse_merge_validation(kw, code):
+    assert _merge(**kw) == code
