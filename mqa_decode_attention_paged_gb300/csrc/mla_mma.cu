@@ -29,11 +29,15 @@ namespace mqa {
 // Shared-memory budget: everything but the staging ring is fixed, the ring
 // gets as many stages as fit (at most 8).
 
-// SPARSE: the stage is filled by per-row bulk copies (unswizzled rows) and
-// turned into the swizzled operand tile by the consumers, as for e4m3
+// SPARSE: the stage is filled by per-row bulk copies.  bf16 rows land in rows
+// padded by 16 bytes (eight consecutive rows then start on eight different
+// bank groups, so ldmatrix reads them without conflicts) and the consumers
+// use the stage directly; e4m3 rows land dense and are widened into the
+// swizzled operand tile as for the dense e4m3 path.
 template <int D, int R, bool FP8, int TILE, bool SPARSE = false>
 struct MlaMmaCfg {
-    static constexpr bool kStaged = FP8 || SPARSE;                 // operand tile built from the stage
+    static constexpr bool kStaged = FP8;                       // operand tile built from the stage
+    static constexpr bool kPadRows = SPARSE && !FP8;           // stage rows padded by 16 bytes
     static constexpr int kHeads = 16;
     static constexpr int kTile = TILE;                         // tokens per stage
     static constexpr int kHalf = kTile / 2;                    // tokens per QK warp
@@ -43,7 +47,8 @@ struct MlaMmaCfg {
     static constexpr int kThreads = kConsumers + 32;
     static constexpr int kPanels = D / 64;                     // 64-column bf16 panels
     static constexpr int kOpBytes = kPanels * kTile * 128;     // swizzled bf16 operand tile
-    static constexpr int kStageBytes = kTile * D * (FP8 ? 1 : 2);  // whole cache rows
+    static constexpr int kRowStride = kPadRows ? D * 2 + 16 : D * (FP8 ? 1 : 2);  // bytes per staged row
+    static constexpr int kStageBytes = kTile * kRowStride;     // whole cache rows
     static constexpr int kKSteps = D / 16;
     static constexpr int kKq = kKSteps / 4;                    // k-steps per head-dim quarter
     static constexpr int kColsPerWarp = R / kConsumerWarps;    // output columns per warp
@@ -60,6 +65,16 @@ struct MlaMmaCfg {
                                   4 * (2 * kMaxBatchSmem + 1) + 1024;
     static constexpr int kStagesFit = (227 * 1024 - kFixed) / kStageBytes;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+
+    // Byte offset of bf16 element (row, col) of the tile the consumers read:
+    // padded rows for the bf16 gather, else whole rows in the 128-byte
+    // swizzled layout of the tensor copies (or of the widened operand tile).
+    __device__ __forceinline__ static uint32_t op_addr(int row, int col) {
+        if constexpr (kPadRows)
+            return static_cast<uint32_t>(row * kRowStride + col * 2);
+        else
+            return swz_rows(row, col, kPanels);
+    }
 
     static constexpr int align1k(int x) { return (x + 1023) & ~1023; }
     static constexpr int kOffStages = 0;
@@ -80,7 +95,7 @@ struct MlaMmaCfg {
     static_assert(kStages >= 2, "at least two pipeline stages");
     static_assert(D % 64 == 0 && kKSteps % 4 == 0, "head size must split into 4 quarters");
     static_assert(kColsPerWarp % 16 == 0, "P.V columns per warp must be a multiple of 16");
-    static_assert(kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+    static_assert(kStageBytes % (kPadRows ? 16 : 1024) == 0, "stages stay aligned for their copies");
     static_assert(kPanels % 2 == 1, "odd panel count keeps ldmatrix conflict free");
     static_assert(1024 + kOffCum + 4 * (2 * kMaxBatchSmem + 1) <= 227 * 1024, "shared memory budget");
 };
@@ -140,7 +155,8 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
             // Sparse decode: a tile is kTile entries of the request's index
             // list; lane l gathers rows l, l + 32, each whole cache row by one
             // bulk copy (rows are D * elt bytes: 16-byte aligned) into the
-            // unswizzled stage.  The two dependent lookups of a row (its
+            // stage (bf16: rows padded by 16 bytes, read in place; e4m3:
+            // dense rows, widened by the consumers).  The two dependent lookups of a row (its
             // index entry, then its block id) are spread over the two tiles
             // before its own: in the turn of tile i the producer reads the
             // entries of tile i + 2, the block ids of tile i + 1 and copies
@@ -227,7 +243,8 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
                 __syncwarp();
 #pragma unroll
                 for (int k = 0; k < kPer; ++k)
-                    if (L0.val[k]) bulk_g2s(dst + (lane + 32 * k) * kRowBytes, src[k], kRowBytes, &full[stage], pol);
+                    if (L0.val[k])
+                        bulk_g2s(dst + (lane + 32 * k) * C::kRowStride, src[k], kRowBytes, &full[stage], pol);
                 issued[stage] = static_cast<int>(phase);
                 if (++stage == C::kStages) {
                     stage = 0;
@@ -392,18 +409,11 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
             const uint64_t vmask = mask_s[stage];
             bool zeroed = false;
             if constexpr (C::kStaged) {
-                // Widen the e4m3 tile to bf16 (exact), or copy the gathered
-                // bf16 rows, into the swizzled operand tile.
+                // Widen the e4m3 tile to bf16 (exact) into the swizzled
+                // operand tile.
                 op = smem + C::kOffOp;
                 named_bar_sync(3, C::kConsumers);  // previous tile's P.V is done
-                if (ok && !FP8) {
-                    constexpr int kChunks = C::kTile * (D / 8);  // 8 bf16 (16 bytes) each
-                    for (int i = t; i < kChunks; i += C::kConsumers) {
-                        const int r = i / (D / 8), cc = i % (D / 8);
-                        *reinterpret_cast<uint4*>(op + swz_rows(r, 8 * cc, C::kPanels)) =
-                            *reinterpret_cast<const uint4*>(stage_buf + r * D * 2 + cc * 16);
-                    }
-                } else if (ok) {
+                if (ok) {
                     constexpr int kChunks = C::kTile * (D / 16);
                     for (int i = t; i < kChunks; i += C::kConsumers) {
                         const int r = i / (D / 16), cc = i % (D / 16);
@@ -441,7 +451,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
                     const int r = i / kChunksPerWarp;
                     if (!((vmask >> r) & 1ull)) {
                         const int col = warp * C::kColsPerWarp + (i % kChunksPerWarp) * 8;
-                        *reinterpret_cast<uint4*>(op + swz_rows(r, col, C::kPanels)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(op + C::op_addr(r, col)) = make_uint4(0, 0, 0, 0);
                     }
                 }
                 zeroed = true;
@@ -461,7 +471,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
                         const int row = th * C::kHalf + nb2 * 16 + (lane & 7) + ((lane >> 4) << 3);
                         const int col = k0 + ((lane >> 3) & 1) * 8;
                         uint32_t b0, b1, b2, b3;
-                        ldsm_x4(b0, b1, b2, b3, op + swz_rows(row, col, C::kPanels));
+                        ldsm_x4(b0, b1, b2, b3, op + C::op_addr(row, col));
                         mma_bf16_16816(sacc[2 * nb2], qa[ks], b0, b1);
                         mma_bf16_16816(sacc[2 * nb2 + 1], qa[ks], b2, b3);
                     }
@@ -551,7 +561,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
                             const int tok = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
                             const int col = warp * C::kColsPerWarp + nb2 * 16 + (lane >> 4) * 8;
                             uint32_t b0, b1, b2, b3;
-                            ldsm_x4_t(b0, b1, b2, b3, op + swz_rows(tok, col, C::kPanels));
+                            ldsm_x4_t(b0, b1, b2, b3, op + C::op_addr(tok, col));
                             mma_bf16_16816(o[2 * nb2], pa, b0, b1);
                             mma_bf16_16816(o[2 * nb2 + 1], pa, b2, b3);
                         }
@@ -627,9 +637,9 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
 #endif
 template <int D, bool FP8, bool SPARSE = false>
 struct MlaTile {
-    // a gathered bf16 tile also needs its swizzled copy: 32-row tiles keep
-    // three stages in shared memory
-    static constexpr int value = (SPARSE && !FP8) ? 32 : MQA_MLA_TILE;
+    // dense, e4m3 and gathered tiles alike (a gathered bf16 tile is read in
+    // place from its padded rows, so two 64-row stages fit)
+    static constexpr int value = MQA_MLA_TILE;
 };
 
 template <int D, int R, bool FP8, bool MULTI, bool SPARSE>
