@@ -115,6 +115,56 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _check(t, name, dtypes=None, shape=None, optional=False, elt=None):
+    """Validate the layout of a tensor argument before its pointer is handed to
+    the C ABI: dtype (or element size), shape and contiguity.  The library
+    reads raw pointers, so a wrong layout would otherwise be read as garbage."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+    if elt is not None and t.element_size() != elt:
+        raise TypeError(f"{name} must have {elt}-byte elements, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _on_device(named):
+    """Every given tensor must live on the CUDA device of the first."""
+    dev = None
+    for name, t in named:
+        if t is None:
+            continue
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor, got one on {t.device}")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the call runs on {dev}")
+
+
+def _check_common(q, kv_cache, code, block_table, seq_lens, out, out_shape, lse, lse_shape, workspace,
+                  device_status, extra=()):
+    import torch
+    _check(q, "q", (torch.bfloat16,))
+    _check(kv_cache, "kv_cache", elt=2 if code == KV_BF16 else 1)
+    _check(block_table, "block_table", (torch.int32,))
+    if block_table.dim() != 2 or block_table.shape[0] != out_shape[0]:
+        raise ValueError("block_table must be int32 [batch, max_blocks]")
+    _check(seq_lens, "seq_lens", (torch.int32,), shape=(out_shape[0],))
+    _check(out, "out", (torch.bfloat16,), shape=out_shape)
+    _check(lse, "lse", (torch.float32,), shape=lse_shape, optional=True)
+    _check(workspace, "workspace", optional=True)
+    _check(device_status, "device_status", (torch.int32,), optional=True)
+    _on_device([("q", q), ("kv_cache", kv_cache), ("block_table", block_table), ("seq_lens", seq_lens),
+                ("out", out), ("lse", lse), ("workspace", workspace), ("device_status", device_status),
+                *extra])
+
+
 def _kv_code(kv_cache, kv_dtype):
     import torch
     if kv_dtype is not None:
@@ -146,6 +196,8 @@ def mla_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *, out=No
     need = mla_decode_workspace_bytes(B, H, R, num_kv_splits)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check_common(q, kv_cache, code, block_table, seq_lens, out, (B, H, R), lse, (B, H), workspace,
+                  device_status)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.mla_decode(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), float(scale),
                         float(k_scale), _ptr(out), _ptr(lse), B, H, D, R, nb, page,
@@ -176,6 +228,8 @@ def mla_decode_multi(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *, 
     need = mla_decode_workspace_bytes(B, Lq * H, R, num_kv_splits)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check_common(q, kv_cache, code, block_table, seq_lens, out, (B, Lq, H, R), lse, (B, Lq, H), workspace,
+                  device_status)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.mla_decode_multi(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), float(scale),
                               float(k_scale), _ptr(out), _ptr(lse), B, Lq, H, D, R, nb, page,
@@ -209,6 +263,9 @@ def mla_decode_sparse(q, kv_cache, block_table, seq_lens, indices, scale, k_scal
     need = mla_decode_workspace_bytes(B, H, R, num_kv_splits)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(indices, "indices", (torch.int32,))
+    _check_common(q, kv_cache, code, block_table, seq_lens, out, (B, H, R), lse, (B, H), workspace,
+                  device_status, extra=[("indices", indices)])
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.mla_decode_sparse(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), _ptr(indices),
                                float(scale), float(k_scale), _ptr(out), _ptr(lse), B, H, D, R, nb, page,
@@ -240,6 +297,8 @@ def gqa_paged_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, v_s
     need = gqa_paged_decode_workspace_bytes(B, Hq, D, num_kv_splits)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check_common(q, kv_cache, code, block_table, seq_lens, out, (B, Hq, D), lse, (B, Hq), workspace,
+                  device_status)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.gqa_paged_decode(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
                               float(scale), float(k_scale), float(v_scale), _ptr(out), _ptr(lse),
@@ -269,6 +328,11 @@ def lse_merge(shard_out, shard_lse, *, out=None, lse=None, stream=None, return_l
         out = torch.empty(lead + (D,), dtype=torch.bfloat16, device=shard_out.device)
     if lse is None and return_lse:
         lse = torch.empty(lead, dtype=torch.float32, device=shard_out.device)
+    _check(shard_out, "shard_out", (torch.bfloat16,))
+    _check(shard_lse, "shard_lse", (torch.float32,))
+    _check(out, "out", (torch.bfloat16,), shape=lead + (D,))
+    _check(lse, "lse", (torch.float32,), shape=lead, optional=True)
+    _on_device([("shard_out", shard_out), ("shard_lse", shard_lse), ("out", out), ("lse", lse)])
     rc = lib.mqa_lse_merge(_ptr(shard_out), _ptr(shard_lse), _ptr(out), _ptr(lse), int(G), rows, int(D),
                            _stream(stream))
     if rc != OK:
@@ -289,9 +353,11 @@ def mla_decode_noalloc(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *
     B, H, D = q.shape
     nb, page, _ = kv_cache.shape
     R = (D - 64) if kv_lora_rank is None else int(kv_lora_rank)
+    code = _kv_code(kv_cache, kv_dtype)
+    _check_common(q, kv_cache, code, block_table, seq_lens, out, (B, H, R), lse, (B, H), None, device_status)
     rc = lib.mla_decode_noalloc(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
                                 float(scale), float(k_scale), _ptr(out), _ptr(lse), B, H, D, R, nb,
-                                page, block_table.shape[1], _kv_code(kv_cache, kv_dtype),
+                                page, block_table.shape[1], code,
                                 int(num_kv_splits), _ptr(device_status), _stream(stream))
     if rc != OK:
         raise MqaError(rc, "mla_decode_noalloc")
