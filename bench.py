@@ -52,7 +52,7 @@ TC_FILES = ("mla_tc.cu", "tc_ptx.cuh", "common.cuh", "plan.cuh", "args.cuh")
 Q8_FILES = ("gqa_q8.cu", "gqa_q8.cuh", "common.cuh", "plan.cuh", "args.cuh")
 MERGE_FILES = ("shard_merge.cu", "shard_merge.cuh", "common.cuh")
 NCU_TRAFFIC = {
-    "mla_v2lite": {"files": MMA_FILES, "src_sha": "7f676f88f8cbea37", "splits": 16, "bytes": 329795584 + 3687424,
+    "mla_v2lite": {"files": MMA_FILES, "src_sha": "469c1abab8d15a69", "splits": 16, "bytes": 329795584 + 3687424,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64>"},
     "mla_longctx": {"files": TC_FILES, "src_sha": "db7d88cc3b68ce52", "splits": 256, "bytes": 485207808 + 4084992,
                     "kernel": "mla_decode_tc_kernel<576,512,0>"},
@@ -64,7 +64,7 @@ NCU_TRAFFIC = {
                      "kernel": "gqa_decode_q8_kernel<128,3,1>"},
     "dcp_merge_v3": {"files": MERGE_FILES, "src_sha": "8c157f962d4da4f4", "bytes": 126340608 + 7121920,
                      "kernel": "shard_merge_kernel"},
-    "mla_sparse": {"files": MMA_FILES, "src_sha": "7f676f88f8cbea37", "splits": 4, "bytes": 152899072 + 3118592,
+    "mla_sparse": {"files": MMA_FILES, "src_sha": "469c1abab8d15a69", "splits": 4, "bytes": 152899072 + 3118592,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64,0,1>"},
 }
 

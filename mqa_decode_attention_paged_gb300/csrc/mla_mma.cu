@@ -4,8 +4,10 @@
 // One thread block = 8 consumer warps + 1 producer warp, persistent over a
 // work unit (see plan.cuh).  The producer walks the block table (prefetching
 // the next tile's block ids while it waits for a free stage) and stages
-// kTile-token tiles of latent rows [kv_c | k_pe] into shared memory with
-// per-row bulk copies (TMA engine), zero-filling rows past the sequence end.
+// kTile-token tiles of latent rows [kv_c | k_pe] into shared memory: one 3D
+// tensor copy per box of whole rows of a page (128-byte swizzle), or, for
+// sparse decode, one bulk copy per selected row.  Rows past the sequence end
+// (or unselected) are masked and their V columns zeroed by the consumers.
 // The same staged tile serves as K (all D columns) and V (first R columns),
 // the MQA view of MLA ("Triton と MLA" page, vllm-arch-zh
 // ja/attention/triton-mla, section データフロー).
