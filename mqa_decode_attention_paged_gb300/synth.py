@@ -32,6 +32,8 @@ library is measured on):
                ceil(exp(N(ln 2048, 1))) clipped to [1, 16384].
   gqa_fp8_pth  the gqa batch with a per-token-head e4m3 cache.
   gqa_int8_pth the gqa batch with a per-token-head int8 cache.
+  gqa_int4_pth the gqa batch with a per-token-head int4 cache (two codes per
+               byte).
   mla_mtp      the mla_v2lite batch with 8 query tokens x 16 heads per request.
   mla_sparse   B=64, H=16, D=576, page 64, bf16, seq_lens uniform in
                [16384, 40960], 2048 distinct random positions per request
@@ -160,23 +162,33 @@ def _fill_blocks(rng, kv: np.ndarray, ids: np.ndarray, kv_dtype: str, k_scale: f
 
 
 # Per-token-head quantised GQA caches: code range each row is scaled into.
-PTH_DTYPES = {"fp8_e4m3_pth": E4M3_MAX, "int8_pth": 127.0}
+PTH_DTYPES = {"fp8_e4m3_pth": E4M3_MAX, "int8_pth": 127.0, "int4_pth": 7.0}
+
+
+def pth_code_bytes(D: int, kv_dtype: str) -> int:
+    """Bytes of codes per (token, KV head) row: D, or D / 2 for packed int4."""
+    return D // 2 if kv_dtype == "int4_pth" else D
 
 
 def encode_pth_rows(x: np.ndarray, kv_dtype: str) -> np.ndarray:
     """Quantise rows x[..., D] (float32) per row: scale = max|x| / code range
-    (1 for an all-zero row), codes = x / scale encoded as e4m3 (torch's cast)
-    or as int8 (round half to even, clipped to +-127); returns uint8
-    [..., D + 4]: the D codes followed by the scale as little-endian binary32."""
+    (1 for an all-zero row), codes = x / scale encoded as e4m3 (torch's cast),
+    as int8 (round half to even, clipped to +-127) or as int4 (the same,
+    clipped to [-8, 7], two per byte: element 2i in the low nibble of byte i);
+    returns uint8 [..., C + 4]: the C code bytes followed by the scale as
+    little-endian binary32."""
     top = PTH_DTYPES[kv_dtype]
     amax = np.abs(x).max(axis=-1, keepdims=True)
     sc = np.where(amax > 0, amax / np.float32(top), np.float32(1.0)).astype(np.float32)
     y = x / sc
     if kv_dtype == "fp8_e4m3_pth":
         codes = to_e4m3_codes(y)
+    elif kv_dtype == "int4_pth":
+        n = np.clip(np.rint(y), -8, 7).astype(np.int16) & 15
+        codes = (n[..., 0::2] | (n[..., 1::2] << 4)).astype(np.uint8)
     else:
         codes = np.clip(np.rint(y), -127, 127).astype(np.int8).view(np.uint8)
-    out = np.empty(x.shape[:-1] + (x.shape[-1] + 4,), dtype=np.uint8)
+    out = np.empty(x.shape[:-1] + (codes.shape[-1] + 4,), dtype=np.uint8)
     out[..., :-4] = codes
     out[..., -4:] = sc.astype("<f4").view(np.uint8).reshape(x.shape[:-1] + (4,))
     return out
@@ -185,7 +197,8 @@ def encode_pth_rows(x: np.ndarray, kv_dtype: str) -> np.ndarray:
 def _fill_blocks_pth(rng, kv: np.ndarray, ids: np.ndarray, kv_dtype: str, chunk_elems: int = 1 << 26):
     """Draw N(0,1) rows for the used blocks `ids` and quantise each (token, KV
     head) row of each plane with its own scale."""
-    shape = kv.shape[1:-1] + (kv.shape[-1] - 4,)
+    D = 2 * (kv.shape[-1] - 4) if kv_dtype == "int4_pth" else kv.shape[-1] - 4
+    shape = kv.shape[1:-1] + (D,)
     per_block = int(np.prod(shape))
     step = max(1, chunk_elems // max(per_block, 1))
     for i in range(0, len(ids), step):
@@ -239,7 +252,7 @@ def make_gqa_case(seq_lens, B=None, Hq=32, Hkv=8, D=128, page=16, kv_dtype="bf16
     table, nb, ids = build_block_table(rng, sl, page, pool_factor, extra_cols)
     q = to_bf16_bits(rng.standard_normal(size=(B, Hq, D), dtype=np.float32))
     if kv_dtype in PTH_DTYPES:
-        kv = np.zeros((nb, 2, page, Hkv, D + 4), dtype=np.uint8)
+        kv = np.zeros((nb, 2, page, Hkv, pth_code_bytes(D, kv_dtype) + 4), dtype=np.uint8)
         _fill_blocks_pth(rng, kv, ids, kv_dtype)
         return PagedCase("gqa", q, kv, table, sl, kv_dtype, float(scale), page=page, num_kv_heads=Hkv,
                          kv_lora_rank=0, name=name)
@@ -267,6 +280,8 @@ WORKLOADS = {
                         page=16, kv_dtype="fp8_e4m3_pth", seed=1008),
     "gqa_int8_pth": dict(kind="gqa", B=256, seq_lens=("lognormal", 2048, 1.0, 16384), Hq=32, Hkv=8, D=128,
                          page=16, kv_dtype="int8_pth", seed=1009),
+    "gqa_int4_pth": dict(kind="gqa", B=256, seq_lens=("lognormal", 2048, 1.0, 16384), Hq=32, Hkv=8, D=128,
+                         page=16, kv_dtype="int4_pth", seed=1011),
     # multi-token decode (speculative verification): the V2-Lite-like batch
     # with 8 new positions per request, 16 heads -> 128 query rows (q is
     # [B, q_len, H, D], stored here as its [B, q_len * H, D] view)

@@ -87,6 +87,7 @@ def _load():
         lib.oracle_gqa_paged_decode_pth.argtypes = [P, P, I, P, P, D, P, P, I, I, I, I, I, I, I]
         lib.oracle_int8_values.argtypes = [P, P, I64]
         lib.oracle_lse_merge.argtypes = [P, P, P, P, I, I, I, I]
+        lib.oracle_int4_values.argtypes = [P, P, I64]
         _lib = lib
         return lib
 
@@ -229,7 +230,16 @@ def mla_decode_multi(q, kv, kv_dtype, block_table, seq_lens, scale, k_scale=1.0,
     return out, lse
 
 
-PTH_KINDS = {"fp8_e4m3_pth": 0, "int8_pth": 1}
+PTH_KINDS = {"fp8_e4m3_pth": 0, "int8_pth": 1, "int4_pth": 2}
+
+
+def int4_values(packed: np.ndarray) -> np.ndarray:
+    """Values of packed int4 codes (uint8, element 2i in the low nibble of byte
+    i, two's complement): n bytes -> 2n values."""
+    b = np.ascontiguousarray(packed, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.float64)
+    _load().oracle_int4_values(_ptr(b), _ptr(out), b.size)
+    return out
 
 
 def int8_values(codes: np.ndarray) -> np.ndarray:
@@ -244,7 +254,8 @@ def gqa_paged_decode(q, kv, kv_dtype, block_table, seq_lens, scale, k_scale=1.0,
     """q [B,Hq,D] bf16 bits; kv [num_blocks, 2, P, Hkv, D] (bf16 bits or e4m3
     codes with per-tensor k_scale / v_scale), or, for kv_dtype "fp8_e4m3_pth"
     / "int8_pth", uint8 [num_blocks, 2, P, Hkv, D + 4] rows of D codes plus
-    their inline fp32 scale (k_scale / v_scale unused); returns
+    their inline fp32 scale, or "int4_pth", rows of D / 2 bytes of packed
+    4-bit codes plus the scale (k_scale / v_scale unused); returns
     (out [B,Hq,D], lse [B,Hq])."""
     if kv_dtype in PTH_KINDS:
         return _gqa_pth(q, kv, kv_dtype, block_table, seq_lens, scale)
@@ -276,8 +287,9 @@ def _gqa_pth(q, kv, kv_dtype, block_table, seq_lens, scale):
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     B, Hq, D = q.shape
     nb, two, P, Hkv, Dp = kv.shape
-    if two != 2 or Dp != D + 4:
-        raise ValueError("per-token-head cache must be [num_blocks, 2, page, num_kv_heads, head_size + 4]")
+    code_bytes = D // 2 if kv_dtype == "int4_pth" else D
+    if two != 2 or Dp != code_bytes + 4:
+        raise ValueError(f"per-token-head cache must be [num_blocks, 2, page, num_kv_heads, {code_bytes + 4}]")
     out = np.zeros((B, Hq, D), dtype=np.float64)
     lse = np.zeros((B, Hq), dtype=np.float64)
     rc = _load().oracle_gqa_paged_decode_pth(_ptr(q), _ptr(kv), PTH_KINDS[kv_dtype], _ptr(bt), _ptr(sl),

@@ -82,10 +82,12 @@
  *     new tokens, whose keys are already in the cache); a query that sees no
  *     key (kv_length < q_len - i) gives out = 0 and lse = -inf.
  *   - GQA query head h reads KV head h / (Hq / Hkv).
- *   - per-token-head caches: a (token, KV head) row is D + 4 bytes, the D
- *     codes followed by the row's scale as a little-endian IEEE binary32;
- *     element value = scale * code, with the code read as OCP e4m3fn or as a
- *     two's-complement int8.  K and V rows carry separate scales.
+ *   - per-token-head caches: a (token, KV head) row is its codes followed by
+ *     the row's scale as a little-endian IEEE binary32; element value =
+ *     scale * code, with the code read as OCP e4m3fn or as a two's-complement
+ *     int8 (D bytes of codes), or as a two's-complement 4-bit code, two per
+ *     byte, element 2i in the low nibble of byte i (D / 2 bytes).  K and V
+ *     rows carry separate scales.
  *   - split s of a sequence with n tokens covers the page-aligned token range
  *     [s*L, min((s+1)*L, n)), L = ceil(ceil(n/page)/S) * page.
  *
@@ -536,7 +538,14 @@ int oracle_gqa_paged_decode(const uint16_t* q, const void* kv, int kv_dtype,
 
 /* ---- per-token-head quantised GQA --------------------------------------- */
 
-enum { ORACLE_PTH_E4M3 = 0, ORACLE_PTH_INT8 = 1 };
+enum { ORACLE_PTH_E4M3 = 0, ORACLE_PTH_INT8 = 1, ORACLE_PTH_INT4 = 2 };
+
+/* Bytes of codes in one row of D elements: one per element, or two 4-bit
+ * codes per byte for int4. */
+static int pth_code_bytes(int D, int kind) { return kind == ORACLE_PTH_INT4 ? D / 2 : D; }
+
+/* Two's-complement nibble: 0..7 -> 0..7, 8..15 -> -8..-1. */
+static double int4_code_value(unsigned nib) { return nib < 8 ? (double)nib : (double)nib - 16.0; }
 
 /* Two's-complement byte, without relying on the signedness of char. */
 static double int8_code_value(uint8_t c) { return c < 128 ? (double)c : (double)c - 256.0; }
@@ -551,19 +560,38 @@ static double pth_row_scale(const uint8_t* row, int D) {
     return (double)f;
 }
 
-/* Dequantised row: out[d] = scale * value(code[d]). */
+/* Dequantised row: out[d] = scale * value(code of element d); int4 rows hold
+ * element 2i in the low nibble and element 2i + 1 in the high nibble of byte
+ * i; the scale follows the code bytes. */
 static void pth_row_values(const uint8_t* row, int D, int kind, double* out) {
-    double sc = pth_row_scale(row, D);
-    for (int d = 0; d < D; ++d)
-        out[d] = sc * (kind == ORACLE_PTH_INT8 ? int8_code_value(row[d]) : oracle_e4m3_value(row[d]));
+    double sc = pth_row_scale(row, pth_code_bytes(D, kind));
+    for (int d = 0; d < D; ++d) {
+        double v;
+        if (kind == ORACLE_PTH_INT4)
+            v = int4_code_value((d & 1) ? (unsigned)(row[d / 2] >> 4) : (unsigned)(row[d / 2] & 15u));
+        else if (kind == ORACLE_PTH_INT8)
+            v = int8_code_value(row[d]);
+        else
+            v = oracle_e4m3_value(row[d]);
+        out[d] = sc * v;
+    }
+}
+
+/* Values of packed int4 rows: n bytes -> 2n elements (low nibble first). */
+void oracle_int4_values(const uint8_t* bytes, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) {
+        out[2 * i] = int4_code_value(bytes[i] & 15u);
+        out[2 * i + 1] = int4_code_value(bytes[i] >> 4);
+    }
 }
 
 void oracle_int8_values(const uint8_t* codes, double* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = int8_code_value(codes[i]);
 }
 
-/* q: bf16 bits [B, Hq, D]; kv: bytes [num_blocks, 2, P, Hkv, D + 4] (plane 0 =
- * K, plane 1 = V, each row D codes + its scale); out: [B, Hq, D]; lse:
+/* q: bf16 bits [B, Hq, D]; kv: bytes [num_blocks, 2, P, Hkv, C + 4] (plane 0 =
+ * K, plane 1 = V, each row C code bytes + its scale, C = D, or D / 2 for
+ * int4); out: [B, Hq, D]; lse:
  * [B, Hq].  The direct definition: K_t, V_t dequantised row by row,
  * s_t = scale * <q, K_t>, lse = m + log sum exp(s_t - m),
  * out = sum_t exp(s_t - lse) V_t. */
@@ -571,9 +599,12 @@ int oracle_gqa_paged_decode_pth(const uint16_t* q, const uint8_t* kv, int kind,
                                 const int32_t* block_table, const int32_t* seq_lens, double scale,
                                 double* out, double* lse, int B, int Hq, int Hkv, int D,
                                 int num_blocks, int P, int max_blocks) {
-    if (Hkv <= 0 || Hq % Hkv != 0 || (kind != ORACLE_PTH_E4M3 && kind != ORACLE_PTH_INT8)) return -1;
+    if (Hkv <= 0 || Hq % Hkv != 0 ||
+        (kind != ORACLE_PTH_E4M3 && kind != ORACLE_PTH_INT8 && kind != ORACLE_PTH_INT4) ||
+        (kind == ORACLE_PTH_INT4 && D % 2 != 0))
+        return -1;
     const int group = Hq / Hkv;
-    const int64_t Dp = (int64_t)D + 4;
+    const int64_t Dp = (int64_t)pth_code_bytes(D, kind) + 4;
     int failed = 0;
     int64_t pairs = (int64_t)B * Hq;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)

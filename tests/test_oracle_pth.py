@@ -18,14 +18,27 @@ import torch
 import oracle
 from mqa_decode_attention_paged_gb300 import synth
 
-PTH = ["fp8_e4m3_pth", "int8_pth"]
+PTH = ["fp8_e4m3_pth", "int8_pth", "int4_pth"]
+
+
+def _unpack_int4(codes):
+    """uint8 [..., n] -> int [..., 2n]: element 2i from the low nibble of byte
+    i, as a signed 4-bit number (shift the nibble into the top of an int8)."""
+    lo = (codes << 4).view(np.int8) >> 4
+    hi = codes.view(np.int8) >> 4
+    out = np.empty(codes.shape[:-1] + (2 * codes.shape[-1],), dtype=np.int64)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
 
 
 def _decode_rows(rows, kv_dtype):
-    """rows uint8 [..., D + 4] -> float64 [..., D] by an independent route."""
+    """rows uint8 [..., C + 4] -> float64 [..., D] by an independent route."""
     codes = np.ascontiguousarray(rows[..., :-4])
     if kv_dtype == "fp8_e4m3_pth":
         vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    elif kv_dtype == "int4_pth":
+        vals = _unpack_int4(codes).astype(np.float64)
     else:
         vals = codes.view(np.int8).astype(np.float64)
     sc = np.ascontiguousarray(rows[..., -4:]).view("<f4").astype(np.float64)
@@ -62,6 +75,14 @@ def _run(case):
                                    case.scale)
 
 
+def test_int4_decoder_exhaustive():
+    codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    got = oracle.int4_values(codes[None, :])[0]
+    assert np.array_equal(got, _unpack_int4(codes[None, :])[0].astype(np.float64))
+    assert got[2 * 0x80] == 0 and got[2 * 0x80 + 1] == -8 and got[2 * 0x7F] == -1 and got[2 * 0x7F + 1] == 7
+    assert set(got.tolist()) == set(range(-8, 8))
+
+
 def test_int8_decoder_exhaustive():
     codes = np.arange(256, dtype=np.uint16).astype(np.uint8)
     assert np.array_equal(oracle.int8_values(codes), codes.view(np.int8).astype(np.float64))
@@ -73,14 +94,14 @@ def test_encoder_round_trip_is_within_half_a_code(kv_dtype):
     rng = np.random.default_rng(3)
     x = rng.standard_normal((5, 7, 128), dtype=np.float32)
     rows = synth.encode_pth_rows(x, kv_dtype)
-    assert rows.shape == (5, 7, 132) and rows.dtype == np.uint8
+    assert rows.shape == (5, 7, (64 if kv_dtype == "int4_pth" else 128) + 4) and rows.dtype == np.uint8
     sc = np.ascontiguousarray(rows[..., -4:]).view("<f4")[..., 0]
-    top = 448.0 if kv_dtype == "fp8_e4m3_pth" else 127.0
+    top = {"fp8_e4m3_pth": 448.0, "int8_pth": 127.0, "int4_pth": 7.0}[kv_dtype]
     assert np.allclose(sc, np.abs(x).max(axis=-1) / top, rtol=1e-6)
     y = _decode_rows(rows, kv_dtype)
     # e4m3: 3 mantissa bits -> relative error <= 2^-4; int8: half a code step
     err = np.abs(y - x)
-    if kv_dtype == "int8_pth":
+    if kv_dtype in ("int8_pth", "int4_pth"):
         assert (err <= 0.5 * sc[..., None] * (1 + 1e-6)).all()
     else:
         assert (err <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * sc[..., None]) * (1 + 1e-6)).all()
@@ -126,9 +147,10 @@ def test_one_token_closed_form(kv_dtype):
     _set_scale(kv, blk, 0, 0, 0, 0.25)
     _set_scale(kv, blk, 1, 0, 0, 3.0)
     out, lse = _run(synth.replace(case, kv=kv))
-    dec = oracle.e4m3_values if kv_dtype == "fp8_e4m3_pth" else oracle.int8_values
-    kc = dec(kv[blk, 0, 0, 0, :64])
-    vc = dec(kv[blk, 1, 0, 0, :64])
+    dec = {"fp8_e4m3_pth": oracle.e4m3_values, "int8_pth": oracle.int8_values,
+           "int4_pth": lambda c: oracle.int4_values(c[None, :])[0]}[kv_dtype]
+    kc = dec(kv[blk, 0, 0, 0, :-4])
+    vc = dec(kv[blk, 1, 0, 0, :-4])
     qd = oracle.bf16_values(case.q[0])
     for h in range(2):
         assert np.allclose(out[0, h], 3.0 * vc, rtol=0, atol=1e-12)
