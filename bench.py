@@ -107,7 +107,7 @@ def workload_stats(case, splits):
     else:
         Hkv = case.num_kv_heads
         # per-token-head rows carry their 4-byte scale after the codes
-        row = D + 4 if case.kv_dtype in ("fp8_e4m3_pth", "int8_pth") else D
+        row = {"fp8_e4m3_pth": D + 4, "int8_pth": D + 4, "int4_pth": D // 2 + 4}.get(case.kv_dtype, D)
         kv_bytes = tokens * 2 * Hkv * row * elt
         flops = 2.0 * H * tokens * 2 * D
         out_w = D
@@ -662,7 +662,8 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"bf16": "bf16", "fp8_e4m3": "bf16 (fp8-e4m3 KV)",
                   "fp8_e4m3_pth": "bf16 (fp8-e4m3 KV, per-token-head scales)",
-                  "int8_pth": "bf16 (int8 KV, per-token-head scales)"}[case.kv_dtype],
+                  "int8_pth": "bf16 (int8 KV, per-token-head scales)",
+                  "int4_pth": "bf16 (int4 KV, per-token-head scales)"}[case.kv_dtype],
         "data": "synthetic (seeded N(0,1) q/KV, random block permutation)",
         "config": workload_config(case, args.workload, splits),
         "roofline": roof, "cpu_baseline": cpu,

@@ -79,7 +79,8 @@ typedef enum mqa_kv_dtype {
      * (token, KV head) row of the K and V planes carries its own scale
      * inline, after its codes; see gqa_paged_decode. */
     MQA_KV_FP8_E4M3_PER_TOKEN_HEAD = 2,
-    MQA_KV_INT8_PER_TOKEN_HEAD = 3
+    MQA_KV_INT8_PER_TOKEN_HEAD = 3,
+    MQA_KV_INT4_PER_TOKEN_HEAD = 4
 } mqa_kv_dtype;
 
 /* ABI version of the loaded library (MQA_ABI_VERSION at build time). */
@@ -278,14 +279,19 @@ mqa_status mla_decode_noalloc(const void* q, const void* kv_cache, const int32_t
  *                                   or int8 (two's complement) codes, then
  *                                   the row's scale as a little-endian IEEE
  *                                   binary32; value = that scale * code
- *                                   (k_scale / v_scale are ignored).  The
- *                                   Triton backend's fp8_per_token_head /
- *                                   int8_per_token_head caches ("Triton と
- *                                   MLA" page, 設計動機 and 主要ファイル: the
- *                                   head dimension is padded to hold the
- *                                   inline scale; the 4-byte padding and the
- *                                   scale's position are this library's
- *                                   reading of that).
+ *                                   (k_scale / v_scale are ignored).
+ *                  MQA_KV_INT4_PER_TOKEN_HEAD
+ *                                   row = head_size / 2 + 4 bytes: 4-bit two's
+ *                                   complement codes, two per byte (element
+ *                                   2i in the low nibble of byte i), then the
+ *                                   scale as above.
+ *                                   These are the Triton backend's
+ *                                   fp8 / int8 / int4_per_token_head caches
+ *                                   ("Triton と MLA" page, 設計動機 and
+ *                                   主要ファイル: the head dimension is padded
+ *                                   to hold the inline scale; the packing,
+ *                                   the 4-byte padding and the scale's
+ *                                   position are this library's reading).
  *   k_scale, v_scale  finite; used by MQA_KV_FP8_E4M3 only.
  *   With an 8-bit cache the tensor cores take the query as f16 (the codes
  *   widen to f16 exactly): q entries must lie within +-65504.

@@ -24,8 +24,9 @@ KV_BF16 = 0
 KV_FP8_E4M3 = 1
 KV_FP8_E4M3_PER_TOKEN_HEAD = 2
 KV_INT8_PER_TOKEN_HEAD = 3
+KV_INT4_PER_TOKEN_HEAD = 4
 _KV_NAMES = {"bf16": KV_BF16, "fp8_e4m3": KV_FP8_E4M3, "fp8_e4m3_pth": KV_FP8_E4M3_PER_TOKEN_HEAD,
-             "int8_pth": KV_INT8_PER_TOKEN_HEAD}
+             "int8_pth": KV_INT8_PER_TOKEN_HEAD, "int4_pth": KV_INT4_PER_TOKEN_HEAD}
 
 LIB_PATH = _build.LIB_PATH
 
@@ -282,12 +283,14 @@ def gqa_paged_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, v_s
     """GQA paged decode through the C ABI.  q [B,Hq,D] bf16; kv_cache
     [num_blocks, 2, page, Hkv, D] bf16 or e4m3 (k_scale / v_scale), or, with
     kv_dtype "fp8_e4m3_pth" / "int8_pth", uint8 [num_blocks, 2, page, Hkv,
-    D + 4] rows of D codes followed by their fp32 scale."""
+    D + 4] rows of D codes followed by their fp32 scale, or "int4_pth", uint8
+    [..., D / 2 + 4] rows of packed 4-bit codes followed by the scale."""
     import torch
     B, Hq, D = q.shape
     nb, two, page, Hkv, D2 = kv_cache.shape
     code = _kv_code(kv_cache, kv_dtype)
-    row = D + 4 if code in (KV_FP8_E4M3_PER_TOKEN_HEAD, KV_INT8_PER_TOKEN_HEAD) else D
+    row = {KV_FP8_E4M3_PER_TOKEN_HEAD: D + 4, KV_INT8_PER_TOKEN_HEAD: D + 4,
+           KV_INT4_PER_TOKEN_HEAD: D // 2 + 4}.get(code, D)
     if two != 2 or D2 != row:
         raise ValueError(f"kv_cache must be [num_blocks, 2, page, num_kv_heads, {row}]")
     if out is None:

@@ -595,7 +595,7 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
     if (num_kv_heads > 8 || num_q_heads / num_kv_heads > 16) return MQA_ERR_UNSUPPORTED;
     if (page_size % 16 != 0) return MQA_ERR_UNSUPPORTED;
     if (kv_dtype != MQA_KV_BF16 && kv_dtype != MQA_KV_FP8_E4M3 && kv_dtype != MQA_KV_FP8_E4M3_PER_TOKEN_HEAD &&
-        kv_dtype != MQA_KV_INT8_PER_TOKEN_HEAD)
+        kv_dtype != MQA_KV_INT8_PER_TOKEN_HEAD && kv_dtype != MQA_KV_INT4_PER_TOKEN_HEAD)
         return MQA_ERR_UNSUPPORTED;
     if (kv_dtype == MQA_KV_FP8_E4M3 && (!std::isfinite(k_scale) || !std::isfinite(v_scale)))
         return MQA_ERR_INVALID_ARG;

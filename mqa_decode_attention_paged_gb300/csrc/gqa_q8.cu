@@ -6,8 +6,9 @@
 //   * e4m3 codes with one k_scale and one v_scale for the whole cache,
 //     [num_blocks, 2, page, Hkv, D] bytes;
 //   * per-token-head e4m3 or int8 codes, [num_blocks, 2, page, Hkv, D + 4]
-//     bytes: each (token, KV head) row holds its D codes followed by its own
-//     scale (little-endian fp32); element value = scale * code.
+//     bytes, or int4 codes two per byte, [num_blocks, 2, page, Hkv, D/2 + 4]:
+//     each (token, KV head) row holds its codes followed by its own scale
+//     (little-endian fp32); element value = scale * code.
 //
 // One thread block = Hkv consumer warps + 1 producer warp, persistent over a
 // work unit (plan.cuh), as in the bf16 kernel.  The producer stages 16-token
@@ -57,13 +58,15 @@ namespace {
 constexpr int kFmtE4m3 = MQA_KV_FP8_E4M3;
 constexpr int kFmtE4m3Pth = MQA_KV_FP8_E4M3_PER_TOKEN_HEAD;
 constexpr int kFmtInt8Pth = MQA_KV_INT8_PER_TOKEN_HEAD;
+constexpr int kFmtInt4Pth = MQA_KV_INT4_PER_TOKEN_HEAD;
 
 template <int D, int KIND>
 struct GqaQ8Cfg {
     static constexpr bool kPth = KIND != kFmtE4m3;
     static constexpr int kTile = 16;
     static constexpr int kMaxKvHeads = 8;
-    static constexpr int kDp = kPth ? D + 4 : D;  // bytes of one (token, KV head) row
+    static constexpr int kCodeBytes = KIND == kFmtInt4Pth ? D / 2 : D;  // codes of one row (int4: 2 per byte)
+    static constexpr int kDp = kPth ? kCodeBytes + 4 : D;  // bytes of one (token, KV head) row
     static constexpr int kKSteps = D / 16;
     static constexpr int kNb = D / 8;
     // widened f16 V tile rows: 16 bytes of padding keep ldmatrix conflict-free
@@ -122,10 +125,22 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     return pack_f16x2(f.x, f.y);
 }
 
-// Four codes (bytes of w, lowest first) -> four f16 values (exact).
+// Two packed int4 codes (the nibbles of byte b, low first) -> their f16 pair:
+// u = x + 8 in [0, 15] placed in the mantissa of 1024 (0x6400), minus 1032.
+__device__ __forceinline__ uint32_t int4_pair(uint32_t t, int b) {
+    // t: the codes with every nibble's sign bit flipped (x + 8)
+    const uint32_t lo = (t >> (8 * b)) & 0xfu, hi = (t >> (8 * b + 4)) & 0xfu;
+    return h2_bits(__hsub2(bits_h2(lo | (hi << 16) | 0x64006400u), bits_h2(0x64086408u)));
+}
+
+// Four codes (bytes of w, lowest first; for int4 the four nibbles of its low
+// 16 bits) -> four f16 values (exact).
 template <int KIND>
 __device__ __forceinline__ uint2 widen4(uint32_t w) {
-    if constexpr (KIND == kFmtInt8Pth) {
+    if constexpr (KIND == kFmtInt4Pth) {
+        const uint32_t t = w ^ 0x8888u;
+        return make_uint2(int4_pair(t, 0), int4_pair(t, 1));
+    } else if constexpr (KIND == kFmtInt8Pth) {
         // u = x + 128 in [0, 255] placed in the mantissa of 1024 (0x6400):
         // the f16 value 1024 + u is exact, minus 1152 gives x
         const uint32_t u = w ^ 0x80808080u;
@@ -140,22 +155,39 @@ __device__ __forceinline__ uint2 widen4(uint32_t w) {
     }
 }
 
-// Widen one KV head's 16 rows of codes (src: the head's first code in the
-// plane tile, rows `rbytes` apart) into an f16 tile with row stride kWStride.
-// Rows of tokens not in vmask become zeros without reading their bytes.
+// Widen one KV head's 16 rows of codes (src: the head's first code byte in
+// the plane tile, rows `rbytes` apart) into an f16 tile with row stride
+// kWStride.  Rows of tokens not in vmask become zeros without reading their
+// bytes.
 template <int D, int KIND>
 __device__ __forceinline__ void widen_rows(const uint8_t* src, uint8_t* dst, uint64_t vmask, int rbytes,
                                            int lane) {
     using C = GqaQ8Cfg<D, KIND>;
-    constexpr int kLanesPerRow = D / 4;
-    constexpr int kRowsPer = 32 / kLanesPerRow;
-    const int sub = lane / kLanesPerRow, ch = lane % kLanesPerRow;
+    if constexpr (KIND == kFmtInt4Pth) {
+        // a lane takes 4 bytes = 8 elements of a row
+        constexpr int kLanesPerRow = D / 8;
+        constexpr int kRowsPer = 32 / kLanesPerRow;
+        const int sub = lane / kLanesPerRow, ch = lane % kLanesPerRow;
 #pragma unroll
-    for (int r0 = 0; r0 < C::kTile; r0 += kRowsPer) {
-        const int r = r0 + sub;
-        const bool v = (vmask >> r) & 1ull;
-        const uint32_t w = v ? *reinterpret_cast<const uint32_t*>(src + r * rbytes + 4 * ch) : 0u;
-        *reinterpret_cast<uint2*>(dst + r * C::kWStride + 8 * ch) = widen4<KIND>(w);
+        for (int r0 = 0; r0 < C::kTile; r0 += kRowsPer) {
+            const int r = r0 + sub;
+            const bool v = (vmask >> r) & 1ull;
+            const uint32_t w = v ? *reinterpret_cast<const uint32_t*>(src + r * rbytes + 4 * ch) : 0u;  // code 0
+            const uint32_t t = w ^ 0x88888888u;
+            *reinterpret_cast<uint4*>(dst + r * C::kWStride + 16 * ch) =
+                make_uint4(int4_pair(t, 0), int4_pair(t, 1), int4_pair(t, 2), int4_pair(t, 3));
+        }
+    } else {
+        constexpr int kLanesPerRow = D / 4;
+        constexpr int kRowsPer = 32 / kLanesPerRow;
+        const int sub = lane / kLanesPerRow, ch = lane % kLanesPerRow;
+#pragma unroll
+        for (int r0 = 0; r0 < C::kTile; r0 += kRowsPer) {
+            const int r = r0 + sub;
+            const bool v = (vmask >> r) & 1ull;
+            const uint32_t w = v ? *reinterpret_cast<const uint32_t*>(src + r * rbytes + 4 * ch) : 0u;
+            *reinterpret_cast<uint2*>(dst + r * C::kWStride + 8 * ch) = widen4<KIND>(w);
+        }
     }
 }
 
@@ -346,10 +378,10 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), q8_
             // K and V scales of this lane's tokens g, g + 8 (0 when masked)
             float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
             if constexpr (C::kPth) {
-                ks0 = v0 ? *reinterpret_cast<const float*>(kb + g * rstride + D) : 0.f;
-                ks1 = v1 ? *reinterpret_cast<const float*>(kb + (g + 8) * rstride + D) : 0.f;
-                vs0 = v0 ? *reinterpret_cast<const float*>(vb + g * rstride + D) : 0.f;
-                vs1 = v1 ? *reinterpret_cast<const float*>(vb + (g + 8) * rstride + D) : 0.f;
+                ks0 = v0 ? *reinterpret_cast<const float*>(kb + g * rstride + C::kCodeBytes) : 0.f;
+                ks1 = v1 ? *reinterpret_cast<const float*>(kb + (g + 8) * rstride + C::kCodeBytes) : 0.f;
+                vs0 = v0 ? *reinterpret_cast<const float*>(vb + g * rstride + C::kCodeBytes) : 0.f;
+                vs1 = v1 ? *reinterpret_cast<const float*>(vb + (g + 8) * rstride + C::kCodeBytes) : 0.f;
             }
             __syncwarp();  // the previous tile's ldmatrix reads of wv are done
             widen_rows<D, KIND>(vb, wv, vmask, rstride, lane);
@@ -364,9 +396,14 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), q8_
                 for (int e = 0; e < 2; ++e) st[hb][e][0] = st[hb][e][1] = st[hb][e][2] = st[hb][e][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < C::kKSteps; ++ks) {
-                const uint2 k0 = widen4<KIND>(*reinterpret_cast<const uint32_t*>(kb + g * rstride + ks * 16 + 4 * c));
-                const uint2 k1 =
-                    widen4<KIND>(*reinterpret_cast<const uint32_t*>(kb + (g + 8) * rstride + ks * 16 + 4 * c));
+                uint2 k0, k1;
+                if constexpr (KIND == kFmtInt4Pth) {  // 4 elements = 2 bytes
+                    k0 = widen4<KIND>(*reinterpret_cast<const uint16_t*>(kb + g * rstride + ks * 8 + 2 * c));
+                    k1 = widen4<KIND>(*reinterpret_cast<const uint16_t*>(kb + (g + 8) * rstride + ks * 8 + 2 * c));
+                } else {
+                    k0 = widen4<KIND>(*reinterpret_cast<const uint32_t*>(kb + g * rstride + ks * 16 + 4 * c));
+                    k1 = widen4<KIND>(*reinterpret_cast<const uint32_t*>(kb + (g + 8) * rstride + ks * 16 + 4 * c));
+                }
                 const uint32_t af[4] = {k0.x, k1.x, k0.y, k1.y};
 #pragma unroll
                 for (int hb = 0; hb < NHB; ++hb) mma_f16_16816(st[hb][ks & 1], af, qb[hb][ks][0], qb[hb][ks][1]);
@@ -537,6 +574,7 @@ template <int D>
 cudaError_t launch_q8_kind(const GqaArgs& a, float out_scale, int kind, int grid, cudaStream_t stream) {
     if (kind == kFmtE4m3Pth) return launch_q8<D, kFmtE4m3Pth>(a, out_scale, grid, stream);
     if (kind == kFmtInt8Pth) return launch_q8<D, kFmtInt8Pth>(a, out_scale, grid, stream);
+    if (kind == kFmtInt4Pth) return launch_q8<D, kFmtInt4Pth>(a, out_scale, grid, stream);
     return launch_q8<D, kFmtE4m3>(a, out_scale, grid, stream);
 }
 
@@ -551,6 +589,7 @@ template <int D>
 size_t smem_kind(int kind, int hkv, int q_per_kv, int batch) {
     if (kind == kFmtE4m3Pth) return smem_of<D, kFmtE4m3Pth>(hkv, q_per_kv, batch);
     if (kind == kFmtInt8Pth) return smem_of<D, kFmtInt8Pth>(hkv, q_per_kv, batch);
+    if (kind == kFmtInt4Pth) return smem_of<D, kFmtInt4Pth>(hkv, q_per_kv, batch);
     return smem_of<D, kFmtE4m3>(hkv, q_per_kv, batch);
 }
 

@@ -8,7 +8,9 @@ namespace mqa {
 // Cache formats served by gqa_q8_stage1 (the values of mqa_kv_dtype):
 //   1  e4m3 codes, one k_scale / v_scale for the whole cache;
 //   2  e4m3 codes, per (token, KV head) row: D codes + its fp32 scale;
-//   3  int8 codes, per (token, KV head) row: D codes + its fp32 scale.
+//   3  int8 codes, per (token, KV head) row: D codes + its fp32 scale;
+//   4  int4 codes, per (token, KV head) row: D / 2 bytes of codes (element 2i
+//      in the low nibble of byte i) + its fp32 scale.
 // out_scale multiplies the output (v_scale for format 1, 1 otherwise); the
 // softmax scale in a.sl2 already holds k_scale for format 1.
 cudaError_t gqa_q8_stage1(const GqaArgs& a, float out_scale, int D, int kind, int grid, cudaStream_t stream);

@@ -157,6 +157,7 @@ def _gqa(**kw):
     (dict(kvd=7), mqa.ERR_UNSUPPORTED),
     (dict(kvd=2), mqa.ERR_UNSUPPORTED),                # per-token-head formats are GQA-only
     (dict(kvd=3), mqa.ERR_UNSUPPORTED),
+    (dict(kvd=4), mqa.ERR_UNSUPPORTED),
     (dict(H=129), mqa.ERR_UNSUPPORTED),
     (dict(B=4097), mqa.ERR_UNSUPPORTED),
     (dict(S=4, ws=None, wsb=0), mqa.ERR_WORKSPACE_TOO_SMALL),
@@ -172,13 +173,14 @@ def test_mla_validation(kw, code):
     (dict(D=96), mqa.ERR_UNSUPPORTED),
     (dict(Hkv=16, Hq=32), mqa.ERR_UNSUPPORTED),
     (dict(Hkv=1, Hq=32), mqa.ERR_UNSUPPORTED),         # at most 16 query heads per KV head
-    (dict(kvd=4), mqa.ERR_UNSUPPORTED),                # bf16, e4m3 and the per-token-head formats only
+    (dict(kvd=5), mqa.ERR_UNSUPPORTED),                # bf16, e4m3 and the per-token-head formats only
     (dict(kvd=-1), mqa.ERR_UNSUPPORTED),
     (dict(kvd=1, ks=float("nan")), mqa.ERR_INVALID_ARG),  # per-tensor fp8 needs finite scales
     (dict(kvd=1, vs=float("inf")), mqa.ERR_INVALID_ARG),
     (dict(kvd=1, S=2), mqa.ERR_WORKSPACE_TOO_SMALL),   # each accepted format reaches the workspace check
     (dict(kvd=2, S=2), mqa.ERR_WORKSPACE_TOO_SMALL),
     (dict(kvd=3, S=2, ks=float("nan")), mqa.ERR_WORKSPACE_TOO_SMALL),  # scales unused by per-token-head
+    (dict(kvd=4, S=2), mqa.ERR_WORKSPACE_TOO_SMALL),
     (dict(P=40), mqa.ERR_UNSUPPORTED),
     (dict(S=2), mqa.ERR_WORKSPACE_TOO_SMALL),
 ])

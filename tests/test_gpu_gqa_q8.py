@@ -17,8 +17,9 @@ pytestmark = pytest.mark.gpu
 
 FORMATS = [dict(kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.03),
            dict(kv_dtype="fp8_e4m3_pth"),
-           dict(kv_dtype="int8_pth")]
-IDS = ["e4m3", "e4m3_pth", "int8_pth"]
+           dict(kv_dtype="int8_pth"),
+           dict(kv_dtype="int4_pth")]
+IDS = ["e4m3", "e4m3_pth", "int8_pth", "int4_pth"]
 
 
 @pytest.mark.parametrize("fmt", FORMATS, ids=IDS)
@@ -76,7 +77,7 @@ def test_per_token_scales_are_applied_per_row():
     assert not np.array_equal(out[0, 4:], base_out[0, 4:])
 
 
-@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3_pth", "int8_pth"])
+@pytest.mark.parametrize("kv_dtype", ["fp8_e4m3_pth", "int8_pth", "int4_pth"])
 def test_extreme_scale_magnitudes(kv_dtype):
     # Rows whose scales span many orders of magnitude (tiny whole requests,
     # single huge V scales late in a sequence): the P.V power-of-two factor
@@ -121,7 +122,7 @@ def test_device_check_reports_bad_block_id():
     assert_close(out[[0]], lse[[0]], ref_out, ref_lse, fp8=True, what="bad block, other request")
 
 
-@pytest.mark.parametrize("name", ["gqa_fp8_pth", "gqa_int8_pth"])
+@pytest.mark.parametrize("name", ["gqa_fp8_pth", "gqa_int8_pth", "gqa_int4_pth"])
 def test_full_size_config_sampled(name):
     case = synth.workload(name)
     splits = 32
@@ -133,5 +134,5 @@ def test_full_size_config_sampled(name):
     # a convex combination of V rows: no entry above the largest |V| of the cache
     v = case.kv[:, 1]
     sc = np.ascontiguousarray(v[..., -4:]).view("<f4")[..., 0].astype(np.float64)
-    top = 448.0 if name == "gqa_fp8_pth" else 128.0
+    top = {"gqa_fp8_pth": 448.0, "gqa_int8_pth": 128.0, "gqa_int4_pth": 8.0}[name]
     assert np.abs(out).max() <= (sc.max() * top) * (1 + 1e-2)
