@@ -96,3 +96,41 @@ def test_reference_arm_rank_zero_prints_one_line(monkeypatch, capsys):
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["gpu_launches"] == 0
+
+
+def test_algorithmic_bytes_and_flops_per_workload():
+    # The roofline's numerator: cache bytes of the valid (or selected) tokens
+    # plus q, out and lse, in each cache format; FLOPs 2 H tokens (D + R) for
+    # MLA and 4 Hq tokens D for GQA.
+    import numpy as np
+    from mqa_decode_attention_paged_gb300 import synth
+    mla = synth.make_mla_case([37, 100], H=16, D=576, page=16, seed=1)
+    st = bench.workload_stats(mla, 1)
+    assert st["tokens"] == 137
+    assert st["kv_bytes"] == 137 * 576 * 2
+    assert st["alg_bytes"] == st["kv_bytes"] + 2 * 16 * 576 * 2 + 2 * 16 * 512 * 2 + 2 * 16 * 4
+    assert st["flops"] == 2.0 * 16 * 137 * (576 + 512)
+    fp8 = synth.make_mla_case([37, 100], H=16, D=576, page=16, kv_dtype="fp8_e4m3", k_scale=0.05, seed=1)
+    assert bench.workload_stats(fp8, 1)["kv_bytes"] == 137 * 576
+    for kv_dtype, row, elt in (("bf16", 128, 2), ("fp8_e4m3", 128, 1), ("fp8_e4m3_pth", 132, 1),
+                               ("int8_pth", 132, 1), ("int4_pth", 68, 1)):
+        g = synth.make_gqa_case([19, 40], Hq=8, Hkv=2, D=128, page=16, kv_dtype=kv_dtype, seed=2)
+        st = bench.workload_stats(g, 1)
+        assert st["kv_bytes"] == 59 * 2 * 2 * row * elt, kv_dtype
+        assert st["flops"] == 2.0 * 8 * 59 * 2 * 128
+    # sparse: only the selected entries count, plus the index lists and one
+    # block-table entry per selected row
+    sp = synth.make_mla_case([50, 10], H=16, D=576, page=16, seed=3)
+    idx = np.array([[0, 49, -1, 50], [3, 9, 9, 12]], dtype=np.int32)
+    sp.meta["indices"] = idx
+    st = bench.workload_stats(sp, 1)
+    assert st["tokens"] == 5  # 0, 49 | 3, 9, 9 (positions >= seq_len and -1 select nothing)
+    assert st["alg_bytes"] == 5 * 576 * 2 + 2 * 16 * 576 * 2 + 2 * 16 * 512 * 2 + 2 * 16 * 4 + idx.size * 4 + 5 * 4
+
+
+def test_merge_workload_bytes():
+    spec = bench.MERGE_WORKLOADS["dcp_merge_v3"]
+    st = bench.merge_stats(spec)
+    rows = spec["B"] * spec["H"]
+    assert st["alg_bytes"] == spec["G"] * rows * spec["R"] * 2 + spec["G"] * rows * 4 + rows * spec["R"] * 2 + rows * 4
+    assert st["in_bytes"] + st["out_bytes"] == st["alg_bytes"]
