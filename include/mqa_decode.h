@@ -293,8 +293,10 @@ mqa_status mla_decode_noalloc(const void* q, const void* kv_cache, const int32_t
  *                                   the 4-byte padding and the scale's
  *                                   position are this library's reading).
  *   k_scale, v_scale  finite; used by MQA_KV_FP8_E4M3 only.
- *   With an 8-bit cache the tensor cores take the query as f16 (the codes
- *   widen to f16 exactly): q entries must lie within +-65504.
+ *   With an 8-bit (or 4-bit) cache the tensor cores take the query as f16
+ *   (the codes widen to f16 exactly): q entries must lie within +-65504.
+ *   Per-token-head scales must be zero or normal fp32 numbers (magnitude at
+ *   least 2^-126).
  *   out          bf16 [batch, num_q_heads, head_size]; lse fp32 [batch,
  *                num_q_heads] or NULL.
  *   Query head h reads KV head h / (num_q_heads / num_kv_heads).
