@@ -227,6 +227,22 @@ mqa_status mla_decode_sparse(const void* q, const void* kv_cache, const int32_t*
 mqa_status mqa_lse_merge(const void* shard_out, const float* shard_lse, void* out, float* lse, int num_shards,
                          long long rows, int head_dim, void* stream);
 
+/* Test hook of the failure detection (the pages have no counterpart): a
+ * bf16-cache gqa_paged_decode in which the producer of work unit
+ * `withhold_unit` never fills or announces its first tile.  The waiting
+ * consumers give up after their time limit (2 s), MQA_ERR_DEVICE_TIMEOUT is
+ * written to *device_status, every block returns and the context stays
+ * usable; the outputs of the affected requests are undefined.  It exists so
+ * that the bounded waits can be tested without faulting or hanging a GPU.
+ * Arguments as for gqa_paged_decode (k_scale = v_scale = 1); withhold_unit
+ * >= 0 (with num_kv_splits == 1, unit b is request b). */
+mqa_status mqa_test_gqa_withheld_arrive(const void* q, const void* kv_cache, const int32_t* block_table,
+                                        const int32_t* seq_lens, float scale, void* out, float* lse, int batch,
+                                        int num_q_heads, int num_kv_heads, int head_size, int num_blocks,
+                                        int page_size, int max_blocks, int num_kv_splits, void* workspace,
+                                        size_t workspace_bytes, int* device_status, void* stream,
+                                        int withhold_unit);
+
 /* Size of the library-owned scratch array used by mla_decode_noalloc. */
 #define MQA_NOALLOC_SCRATCH_BYTES (64u << 20)
 

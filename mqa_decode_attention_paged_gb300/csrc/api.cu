@@ -13,6 +13,7 @@
 #include "args.cuh"
 #include "gqa_q8.cuh"
 #include "shard_merge.cuh"
+#include "gqa_test.cuh"
 
 namespace {
 
@@ -576,12 +577,16 @@ mqa_status mqa_lse_merge(const void* shard_out, const float* shard_lse, void* ou
     return MQA_OK;
 }
 
-mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* block_table,
-                            const int32_t* seq_lens, float scale, float k_scale, float v_scale,
-                            void* out, float* lse, int batch, int num_q_heads, int num_kv_heads,
-                            int head_size, int num_blocks, int page_size, int max_blocks,
-                            mqa_kv_dtype kv_dtype, int num_kv_splits, void* workspace,
-                            size_t workspace_bytes, int* device_status, void* stream) {
+}  // extern "C"
+
+// gqa_paged_decode; withhold >= 0 (bf16 caches only) is the test hook of the
+// bounded waits (see mqa_test_gqa_withheld_arrive).
+static mqa_status gqa_decode_impl(const void* q, const void* kv_cache, const int32_t* block_table,
+                                  const int32_t* seq_lens, float scale, float k_scale, float v_scale,
+                                  void* out, float* lse, int batch, int num_q_heads, int num_kv_heads,
+                                  int head_size, int num_blocks, int page_size, int max_blocks,
+                                  mqa_kv_dtype kv_dtype, int num_kv_splits, void* workspace,
+                                  size_t workspace_bytes, int* device_status, void* stream, int withhold) {
     if (!q || !kv_cache || !block_table || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
         !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (device_status && !aligned(device_status, 4)))
@@ -636,9 +641,12 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
     a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, resident);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (withhold >= 0 && kv_dtype != MQA_KV_BF16) return MQA_ERR_UNSUPPORTED;
     if (kv_dtype == MQA_KV_BF16) {
-        if (cudaError_t e = mqa::gqa_mma_stage1(a, head_size, a.plan.units, st); e != cudaSuccess)
-            return cuda_fail(e);
+        const cudaError_t e = withhold >= 0
+                                  ? mqa::gqa_mma_stage1_withheld(a, head_size, a.plan.units, withhold, st)
+                                  : mqa::gqa_mma_stage1(a, head_size, a.plan.units, st);
+        if (e != cudaSuccess) return cuda_fail(e);
     } else {
         // 8-bit codes: widened per KV head in shared memory; per-tensor fp8
         // folds k_scale into the softmax scale and v_scale into the output
@@ -662,6 +670,31 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
         if (cudaError_t e = mqa::lse_merge(m, st); e != cudaSuccess) return cuda_fail(e);
     }
     return MQA_OK;
+}
+
+extern "C" {
+
+mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* block_table,
+                            const int32_t* seq_lens, float scale, float k_scale, float v_scale,
+                            void* out, float* lse, int batch, int num_q_heads, int num_kv_heads,
+                            int head_size, int num_blocks, int page_size, int max_blocks,
+                            mqa_kv_dtype kv_dtype, int num_kv_splits, void* workspace,
+                            size_t workspace_bytes, int* device_status, void* stream) {
+    return gqa_decode_impl(q, kv_cache, block_table, seq_lens, scale, k_scale, v_scale, out, lse, batch,
+                           num_q_heads, num_kv_heads, head_size, num_blocks, page_size, max_blocks, kv_dtype,
+                           num_kv_splits, workspace, workspace_bytes, device_status, stream, -1);
+}
+
+mqa_status mqa_test_gqa_withheld_arrive(const void* q, const void* kv_cache, const int32_t* block_table,
+                                        const int32_t* seq_lens, float scale, void* out, float* lse, int batch,
+                                        int num_q_heads, int num_kv_heads, int head_size, int num_blocks,
+                                        int page_size, int max_blocks, int num_kv_splits, void* workspace,
+                                        size_t workspace_bytes, int* device_status, void* stream,
+                                        int withhold_unit) {
+    if (withhold_unit < 0) return MQA_ERR_INVALID_ARG;
+    return gqa_decode_impl(q, kv_cache, block_table, seq_lens, scale, 1.0f, 1.0f, out, lse, batch, num_q_heads,
+                           num_kv_heads, head_size, num_blocks, page_size, max_blocks, MQA_KV_BF16, num_kv_splits,
+                           workspace, workspace_bytes, device_status, stream, withhold_unit);
 }
 
 }  // extern "C"

@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "plan.cuh"
 #include "args.cuh"
+#include "gqa_test.cuh"
 
 namespace mqa {
 
@@ -38,9 +39,13 @@ struct GqaCfg {
     static size_t smem_bytes(int hkv, int batch) { return off_cum(hkv) + 4 * (2 * batch + 1); }
 };
 
+// withhold: test hook for the bounded waits (-1 in every normal call): the
+// producer of unit `withhold` never fills or announces its first tile, so the
+// consumers' wait for it runs out, they report MQA_ERR_DEVICE_TIMEOUT and
+// the block returns; nothing waits without a time limit.
 template <int D>
 __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
-    gqa_decode_mma_kernel(const GqaArgs a) {
+    gqa_decode_mma_kernel(const GqaArgs a, const int withhold) {
     using C = GqaCfg<D>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int Hkv = a.Hkv;
@@ -90,13 +95,27 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
         int t0 = cur.t0;
         bool val = have && t0 + r < cur.tok_end;
         int blk = val ? cur.bt[(t0 + r) / P] : 0;
+        bool withheld = static_cast<int>(blockIdx.x) == withhold;
         while (have) {
             const bool have_next = cur.next(a.plan, cum, lens, a.block_table);
             const bool nval = have_next && cur.t0 + r < cur.tok_end;
             const int nblk = nval ? cur.bt[(cur.t0 + r) / P] : 0;
-            if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            // warp-uniform: the lanes go on or leave together
+            if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1))) {
                 report(a.status, MQA_ERR_DEVICE_TIMEOUT);
                 break;
+            }
+            if (withheld) {  // test hook: this tile is never filled nor announced
+                withheld = false;
+                if (++stage == nstage) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+                have = have_next;
+                t0 = cur.t0;
+                val = nval;
+                blk = nblk;
+                continue;
             }
             uint8_t* dst = stages + stage * sbytes + (plane * C::kTile + r) * stride;
             bool valid = val;
@@ -175,7 +194,8 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
         float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
 
         for (int t0 = tok0; t0 < tok_end; t0 += C::kTile) {
-            const bool ok = mbar_wait(&full[stage], phase);
+            // warp-uniform: the lanes go on or leave together
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase));
             if (!ok) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
             const uint8_t* kbuf = stages + stage * sbytes;
             const uint8_t* vbuf = kbuf + C::kTile * stride;
@@ -302,21 +322,26 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
 }
 
 template <int D>
-static cudaError_t launch_gqa(const GqaArgs& a, int grid, cudaStream_t stream) {
+static cudaError_t launch_gqa(const GqaArgs& a, int grid, int withhold, cudaStream_t stream) {
     using C = GqaCfg<D>;
     const size_t smem = C::smem_bytes(a.Hkv, a.plan.batch);
     auto kern = gqa_decode_mma_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    e = launch_with_pdl(kern, dim3(grid), dim3(32 * (a.Hkv + 1)), smem, stream, a);
+    e = launch_with_pdl(kern, dim3(grid), dim3(32 * (a.Hkv + 1)), smem, stream, a, withhold);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t gqa_mma_stage1(const GqaArgs& a, int D, int grid, cudaStream_t stream) {
-    if (D == 128) return launch_gqa<128>(a, grid, stream);
-    return launch_gqa<64>(a, grid, stream);
+    if (D == 128) return launch_gqa<128>(a, grid, -1, stream);
+    return launch_gqa<64>(a, grid, -1, stream);
+}
+
+cudaError_t gqa_mma_stage1_withheld(const GqaArgs& a, int D, int grid, int withhold, cudaStream_t stream) {
+    if (D == 128) return launch_gqa<128>(a, grid, withhold, stream);
+    return launch_gqa<64>(a, grid, withhold, stream);
 }
 
 size_t gqa_mma_smem_bytes(int D, int hkv, int batch) {

@@ -68,7 +68,6 @@ struct GqaQ8Cfg {
     static constexpr int kCodeBytes = KIND == kFmtInt4Pth ? D / 2 : D;  // codes of one row (int4: 2 per byte)
     static constexpr int kDp = kPth ? kCodeBytes + 4 : D;  // bytes of one (token, KV head) row
     static constexpr int kKSteps = D / 16;
-    static constexpr int kNb = D / 8;
     // widened f16 V tile rows: 16 bytes of padding keep ldmatrix conflict-free
     static constexpr int kWStride = 2 * D + 16;
     static constexpr int kWBytes = kTile * kWStride;  // one warp's V tile

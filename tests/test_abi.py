@@ -212,3 +212,15 @@ def _merge(**kw):
 ])
 def test_lse_merge_validation(kw, code):
     assert _merge(**kw) == code
+
+
+def test_withheld_arrive_hook_validation():
+    fn = mqa.lib.mqa_test_gqa_withheld_arrive
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    fn.restype = I
+    fn.argtypes = [P, P, P, P, F, P, P, I, I, I, I, I, I, I, I, P, SZ, P, P, I]
+    f = ctypes.c_void_p(FAKE)
+    args = [f, f, f, f, 0.09, f, None, 2, 8, 2, 128, 10, 16, 8, 1, None, 0, None, None]
+    assert fn(*args, -1) == mqa.ERR_INVALID_ARG          # a unit to withhold is required
+    assert fn(*(args[:7] + [0] + args[8:]), 0) == mqa.ERR_INVALID_ARG  # the usual validation runs first
+    assert fn(*(args[:14] + [2] + args[15:]), 0) == mqa.ERR_WORKSPACE_TOO_SMALL
