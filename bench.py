@@ -1,9 +1,12 @@
 """Benchmark: paged MLA/GQA decode on GB300 through the C ABI.
 
 One step = one decode call (split-KV stage 1 + LSE merge) over one batch of the
-chosen workload, inputs resident in HBM.  Default workload: the MLA
-V2-Lite-like batch (B=64, H=16, head 576 = 512 + 64, bf16, seq_lens uniform in
-[1024, 8192], page 64, random block permutation over a 1.5x pool).
+chosen workload, inputs resident in HBM.  Default workload: the MLA V3-like
+batch (B=128, H=128, head 576 = 512 + 64, bf16 query, e4m3 KV cache with
+k_scale 0.05, seq_lens uniform in [4096, 32768], page 64, random block
+permutation), the largest of the MLA configurations and one that the 70 %
+roofline target is set on; `--workload` picks the others (mla_longctx,
+mla_v2lite, gqa, ...).
 
 Prints ONE JSON line (rank 0).  `value` is KV GB/s (algorithmic KV bytes of the
 valid tokens / device time, summed over ranks); `ms_per_step` gives the
@@ -141,8 +144,100 @@ def workload_config(case, name, splits):
     return cfg
 
 
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*): the ones a
+# run is judged by.
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+def decode_reasons(mask: int):
+    """Names of the judged NVML clock-event reasons set in `mask`."""
+    return sorted(n for bit, n in NVML_REASONS.items() if mask & bit)
+
+
+def summarize_clocks(samples, max_mhz, source):
+    """samples: [(sm_mhz, reason names)] taken while the timed region ran."""
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": max_mhz, "reasons": [], "samples": 0, "source": source}
+    reasons = sorted(set(r for _, rs in samples for r in rs))
+    return {"sm_mhz": statistics.median(m for m, _ in samples), "sm_max_mhz": max_mhz, "reasons": reasons,
+            "samples": len(samples), "source": source}
+
+
+class NvmlPoller:
+    """Reads the SM clock and the clock-event reasons of one GPU through NVML
+    (libnvidia-ml, part of the driver) every `period_s` on a background
+    thread.  Read-only: it changes no setting of the GPU."""
+
+    def __init__(self, pci_bus_id: str | None, index: int, period_s: float = 0.001):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        ok = False
+        if pci_bus_id:
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+
+    def read(self):
+        c = self.ct
+        mhz, rs = c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz)) != 0:
+            return None
+        if self.reason_fn(self.h, c.byref(rs)) != 0:
+            return None
+        return float(mhz.value), decode_reasons(int(rs.value))
+
+    def _run(self):
+        while not self._stop.is_set():
+            r = self.read()
+            if r is not None:
+                self.samples.append(r)
+            self._stop.wait(self.period)
+
+    def start(self):
+        import threading
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+        r = self.read()  # one reading at the end of the region as well
+        if r is not None:
+            self.samples.append(r)
+        self.lib.nvmlShutdown()
+
+
+def device_pci_bus_id(dev_index: int):
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev_index)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:
+        return None
+
+
 class ClockSampler:
-    """Samples nvidia-smi SM clocks and throttle reasons while running."""
+    """SM clocks and clock-event reasons of the GPU while the timed region
+    runs: NVML read every millisecond (so that even a timed region of a few
+    milliseconds is sampled), else nvidia-smi every 50 ms."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -151,11 +246,20 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.nvml = None
+        self.out = ""
 
     def __enter__(self):
         try:
+            self.nvml = NvmlPoller(device_pci_bus_id(self.index), self.index)
+            self.nvml.start()
+            return self
+        except (OSError, AttributeError):
+            self.nvml = None
+        try:
+            bus = device_pci_bus_id(self.index)
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", bus or str(self.index), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
@@ -163,7 +267,9 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
+        if self.nvml is not None:
+            self.nvml.stop()
+            return
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -173,24 +279,21 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        if self.nvml is not None:
+            return summarize_clocks(self.nvml.samples, self.nvml.max_mhz, "nvml, 1 ms")
+        samples, mx = [], None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in (self.out or "").strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 7:
                 continue
             try:
-                sm.append(float(parts[0]))
+                sm = float(parts[0])
                 mx = float(parts[1])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[3:7]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+            samples.append((sm, [n for n, v in zip(names, parts[3:7]) if v.lower().startswith("active")]))
+        return summarize_clocks(samples, mx, "nvidia-smi, 50 ms")
 
 
 def time_oracle(case, budget_s=12.0, min_reps=1):
@@ -687,7 +790,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="mla_v2lite")
+    ap.add_argument("--workload", default="mla_v3_fp8")
     ap.add_argument("--splits", type=int, default=0, help="num_kv_splits (0 = heuristic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")

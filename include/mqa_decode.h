@@ -227,22 +227,6 @@ mqa_status mla_decode_sparse(const void* q, const void* kv_cache, const int32_t*
 mqa_status mqa_lse_merge(const void* shard_out, const float* shard_lse, void* out, float* lse, int num_shards,
                          long long rows, int head_dim, void* stream);
 
-/* Test hook of the failure detection (the pages have no counterpart): a
- * bf16-cache gqa_paged_decode in which the producer of work unit
- * `withhold_unit` never fills or announces its first tile.  The waiting
- * consumers give up after their time limit (2 s), MQA_ERR_DEVICE_TIMEOUT is
- * written to *device_status, every block returns and the context stays
- * usable; the outputs of the affected requests are undefined.  It exists so
- * that the bounded waits can be tested without faulting or hanging a GPU.
- * Arguments as for gqa_paged_decode (k_scale = v_scale = 1); withhold_unit
- * >= 0 (with num_kv_splits == 1, unit b is request b). */
-mqa_status mqa_test_gqa_withheld_arrive(const void* q, const void* kv_cache, const int32_t* block_table,
-                                        const int32_t* seq_lens, float scale, void* out, float* lse, int batch,
-                                        int num_q_heads, int num_kv_heads, int head_size, int num_blocks,
-                                        int page_size, int max_blocks, int num_kv_splits, void* workspace,
-                                        size_t workspace_bytes, int* device_status, void* stream,
-                                        int withhold_unit);
-
 /* Size of the library-owned scratch array used by mla_decode_noalloc. */
 #define MQA_NOALLOC_SCRATCH_BYTES (64u << 20)
 
@@ -264,10 +248,12 @@ mqa_status mqa_test_gqa_withheld_arrive(const void* q, const void* kv_cache, con
  *     mla_decode_workspace_bytes(batch, num_heads, kv_lora_rank, num_kv_splits)
  *     <= MQA_NOALLOC_SCRATCH_BYTES (lower num_kv_splits to fit; e.g. B=64,
  *     H=16, R=512 fits up to 31 splits, B=4, H=128 up to 63).
- *   - The first call on a device looks up the array's device address (once,
- *     with that device current); make that first call before any stream
- *     capture.  The function allocates nothing and never calls cudaMalloc or
- *     cudaFree.
+ *   - Every call looks up the array's device address for the current device
+ *     (cudaGetSymbolAddress, a host-side query; so a device reset never
+ *     leaves a stale address behind).  The first call on a device also loads
+ *     the library's device code there: make that first call before any
+ *     stream capture.  The function allocates nothing and never calls
+ *     cudaMalloc or cudaFree.
  *   - All calls share the one array, which keeps the previous call's contents
  *     (nothing in it needs to start at zero).  Calls whose kernels may overlap
  *     on the GPU (other streams, other host threads) race on it and must be

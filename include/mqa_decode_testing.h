@@ -1,0 +1,44 @@
+/*
+ * mqa_decode_testing.h — test-only entry points of the GB300 paged
+ * decode-attention library (not part of the product interface in
+ * mqa_decode.h).  The pages have no counterpart to them.
+ *
+ * They exist so that the library's bounded waits can be tested on a GPU
+ * without faulting or hanging it: each runs a normal decode in which one
+ * role of one work unit deliberately never delivers what another role waits
+ * for.  The waiting role gives up after its time limit (2 s of the GPU's
+ * global timer), MQA_ERR_DEVICE_TIMEOUT is written to *device_status, every
+ * thread block returns, and the context stays usable; the outputs of the
+ * affected requests are undefined.
+ *
+ * Gate: every hook returns MQA_ERR_UNSUPPORTED, before anything is enqueued,
+ * unless the environment variable MQA_ENABLE_TEST_HOOKS is "1" at the time
+ * of the call, so that no product caller can start a deliberately stalled
+ * kernel by accident.  Argument validation runs after the gate, exactly as
+ * for the product entry point each hook mirrors.
+ */
+#ifndef MQA_DECODE_TESTING_H
+#define MQA_DECODE_TESTING_H
+
+#include "mqa_decode.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A bf16-cache gqa_paged_decode in which the producer of work unit
+ * `withhold_unit` fills and announces none of its tiles: its consumers' first
+ * wait runs out.  Arguments as for gqa_paged_decode (k_scale = v_scale = 1);
+ * withhold_unit >= 0 (with num_kv_splits == 1, unit b is request b). */
+mqa_status mqa_test_gqa_withheld_arrive(const void* q, const void* kv_cache, const int32_t* block_table,
+                                        const int32_t* seq_lens, float scale, void* out, float* lse, int batch,
+                                        int num_q_heads, int num_kv_heads, int head_size, int num_blocks,
+                                        int page_size, int max_blocks, int num_kv_splits, void* workspace,
+                                        size_t workspace_bytes, int* device_status, void* stream,
+                                        int withhold_unit);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQA_DECODE_TESTING_H */

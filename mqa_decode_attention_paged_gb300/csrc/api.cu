@@ -4,11 +4,13 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
 #include "common.cuh"
 #include "plan.cuh"
+#include "../../include/mqa_decode_testing.h"
 
 #include "args.cuh"
 #include "gqa_q8.cuh"
@@ -28,6 +30,12 @@ mqa_status cuda_fail(cudaError_t e) {
 constexpr int kMaxBatch = mqa::kMaxBatchSmem;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Test hooks run only when MQA_ENABLE_TEST_HOOKS is "1" (mqa_decode_testing.h).
+bool test_hooks_enabled() {
+    const char* v = std::getenv("MQA_ENABLE_TEST_HOOKS");
+    return v && v[0] == '1' && v[1] == '\0';
+}
 
 int sm_count_current() {
     int dev = 0;
@@ -691,6 +699,7 @@ mqa_status mqa_test_gqa_withheld_arrive(const void* q, const void* kv_cache, con
                                         int page_size, int max_blocks, int num_kv_splits, void* workspace,
                                         size_t workspace_bytes, int* device_status, void* stream,
                                         int withhold_unit) {
+    if (!test_hooks_enabled()) return MQA_ERR_UNSUPPORTED;
     if (withhold_unit < 0) return MQA_ERR_INVALID_ARG;
     return gqa_decode_impl(q, kv_cache, block_table, seq_lens, scale, 1.0f, 1.0f, out, lse, batch, num_q_heads,
                            num_kv_heads, head_size, num_blocks, page_size, max_blocks, MQA_KV_BF16, num_kv_splits,

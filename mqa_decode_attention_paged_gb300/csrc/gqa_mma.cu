@@ -40,8 +40,8 @@ struct GqaCfg {
 };
 
 // withhold: test hook for the bounded waits (-1 in every normal call): the
-// producer of unit `withhold` never fills or announces its first tile, so the
-// consumers' wait for it runs out, they report MQA_ERR_DEVICE_TIMEOUT and
+// producer of unit `withhold` fills and announces none of its tiles, so the
+// consumers' first wait runs out, they report MQA_ERR_DEVICE_TIMEOUT and
 // the block returns; nothing waits without a time limit.
 template <int D>
 __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
@@ -95,7 +95,10 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
         int t0 = cur.t0;
         bool val = have && t0 + r < cur.tok_end;
         int blk = val ? cur.bt[(t0 + r) / P] : 0;
-        bool withheld = static_cast<int>(blockIdx.x) == withhold;
+        // test hook: the producer of the withheld unit fills and announces
+        // nothing at all, so no copy of it is ever in flight and the
+        // consumers' first wait runs out
+        if (static_cast<int>(blockIdx.x) == withhold) have = false;
         while (have) {
             const bool have_next = cur.next(a.plan, cum, lens, a.block_table);
             const bool nval = have_next && cur.t0 + r < cur.tok_end;
@@ -104,18 +107,6 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
             if (!__all_sync(0xffffffffu, mbar_wait(&empty[stage], phase ^ 1))) {
                 report(a.status, MQA_ERR_DEVICE_TIMEOUT);
                 break;
-            }
-            if (withheld) {  // test hook: this tile is never filled nor announced
-                withheld = false;
-                if (++stage == nstage) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-                have = have_next;
-                t0 = cur.t0;
-                val = nval;
-                blk = nblk;
-                continue;
             }
             uint8_t* dst = stages + stage * sbytes + (plane * C::kTile + r) * stride;
             bool valid = val;
@@ -194,9 +185,16 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
         float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
 
         for (int t0 = tok0; t0 < tok_end; t0 += C::kTile) {
-            // warp-uniform: the lanes go on or leave together
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase));
-            if (!ok) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+            // warp-uniform: the lanes go on or leave together; a tile that
+            // never arrived is not read (its mask and rows were never
+            // written), but its stage is still handed back
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase))) {
+                report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+                aborted = true;
+                break;
+            }
             const uint8_t* kbuf = stages + stage * sbytes;
             const uint8_t* vbuf = kbuf + C::kTile * stride;
             const uint64_t vmask = mask_s[stage];
@@ -268,10 +266,6 @@ __global__ void __launch_bounds__(32 * (GqaCfg<D>::kMaxKvHeads + 1), 1)
             if (++stage == nstage) {
                 stage = 0;
                 phase ^= 1;
-            }
-            if (!ok) {
-                aborted = true;
-                break;
             }
         }
         if (aborted) break;

@@ -367,8 +367,16 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), q8_
         float p_fac = 1.f;     // 2^-e_run
 
         for (int t0 = tok0; t0 < tok_end; t0 += C::kTile) {
-            const bool ok = mbar_wait(&full[stage], phase);
-            if (!ok) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+            // warp-uniform: the lanes go on or leave together (the MMAs and
+            // shuffles below are warp-collective); a tile that never arrived
+            // is not read, but its stage is still handed back
+            if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase))) {
+                report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+                aborted = true;
+                break;
+            }
             const uint8_t* kb = stages + stage * sbytes + hoff;
             const uint8_t* vb = kb + pbytes;
             const uint64_t vmask = mask_s[stage];
@@ -496,10 +504,6 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), q8_
                 ldsm_x4_t(av[0], av[1], av[2], av[3], wv + tok * C::kWStride + col * 2);
 #pragma unroll
                 for (int hb = 0; hb < NHB; ++hb) mma_f16_16816(o[hb][mb], av, pb[hb][0], pb[hb][1]);
-            }
-            if (!ok) {
-                aborted = true;
-                break;
             }
         }
         if (aborted) break;

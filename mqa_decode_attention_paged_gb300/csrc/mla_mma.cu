@@ -401,7 +401,8 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
         float m_run = -INFINITY, l_run = 0.f;  // softmax role, head sh
 
         for (int t0 = tok0; t0 < tok_end; t0 += C::kTile) {
-            const bool ok = mbar_wait(&full[stage], phase);
+            // decided per warp: the MMAs below are warp-collective
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase));
             if (!ok) {
                 *abort_s = 1;
                 report(a.status, MQA_ERR_DEVICE_TIMEOUT);

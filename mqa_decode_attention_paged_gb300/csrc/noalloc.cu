@@ -13,41 +13,28 @@
 // The array is file-scope device memory of kNoallocScratchBytes bytes: every
 // GPU that loads this library holds it until the process exits.  Host code may
 // not use the array's name as an address (on the host it is only a stand-in
-// symbol), so the device address is looked up with cudaGetSymbolAddress once
-// per device, with that device current, on the first call made on it; make
-// that first call before any stream capture begins.  Every call shares the
-// array and it keeps the previous call's contents; the kernels write every
-// partial slot before reading it, so nothing needs to start at zero.  Calls
-// whose kernels may overlap on the GPU (different streams, or several host
-// threads) race on the array: serialise them.
-#include <atomic>
-#include <mutex>
-
+// symbol), so every call looks the device address up with
+// cudaGetSymbolAddress for the current device.  The lookup is a host-side
+// query that allocates nothing; it is made on every call rather than cached,
+// so a call after a device reset (a new primary context, a new array) never
+// uses the old address.  The first call on a device also loads the library's
+// device code there; make that first call before any stream capture begins.
+// Every call shares the array and it keeps the previous call's contents; the
+// kernels write every partial slot before reading it, so nothing needs to
+// start at zero.  Calls whose kernels may overlap on the GPU (different
+// streams, or several host threads) race on the array: serialise them.
 #include "common.cuh"
 
 namespace {
 
 constexpr size_t kNoallocScratchBytes = MQA_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
-std::mutex g_setup_mutex;
-std::atomic<void*> g_scratch_ptr[kMaxDevices];
-
-// Device address of g_noalloc_scratch on the current device (looked up once).
+// Device address of g_noalloc_scratch on the current device.
 mqa_status scratch_address(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MQA_ERR_CUDA;
-    void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
-    if (!p) {
-        std::lock_guard<std::mutex> lock(g_setup_mutex);
-        p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
-        if (!p) {
-            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MQA_ERR_CUDA;
-            g_scratch_ptr[dev].store(p, std::memory_order_release);
-        }
-    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MQA_ERR_CUDA;
     *out = p;
     return MQA_OK;
 }

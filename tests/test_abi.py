@@ -30,6 +30,10 @@ def _declared_functions():
 
 def test_header_symbols_are_exported():
     names = _declared_functions()
+    # the test hooks sit in their own header, not in the product interface
+    product = open(os.path.join(ROOT, "include", "mqa_decode.h")).read()
+    assert "mqa_test_" not in product
+    assert "mqa_test_gqa_withheld_arrive" in names
     assert {"mla_decode", "mla_decode_multi", "mla_decode_sparse", "gqa_paged_decode", "mqa_lse_merge",
             "mqa_num_kv_splits", "mla_decode_workspace_bytes",
             "gqa_paged_decode_workspace_bytes", "mqa_status_string", "mqa_abi_version",
@@ -214,13 +218,19 @@ def test_lse_merge_validation(kw, code):
     assert _merge(**kw) == code
 
 
-def test_withheld_arrive_hook_validation():
+def test_withheld_arrive_hook_validation(monkeypatch):
     fn = mqa.lib.mqa_test_gqa_withheld_arrive
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     fn.restype = I
     fn.argtypes = [P, P, P, P, F, P, P, I, I, I, I, I, I, I, I, P, SZ, P, P, I]
     f = ctypes.c_void_p(FAKE)
     args = [f, f, f, f, 0.09, f, None, 2, 8, 2, 128, 10, 16, 8, 1, None, 0, None, None]
+    # without the gate the hook refuses before looking at anything
+    monkeypatch.delenv("MQA_ENABLE_TEST_HOOKS", raising=False)
+    assert fn(*args, 0) == mqa.ERR_UNSUPPORTED
+    monkeypatch.setenv("MQA_ENABLE_TEST_HOOKS", "0")
+    assert fn(*args, 0) == mqa.ERR_UNSUPPORTED
+    monkeypatch.setenv("MQA_ENABLE_TEST_HOOKS", "1")
     assert fn(*args, -1) == mqa.ERR_INVALID_ARG          # a unit to withhold is required
     assert fn(*(args[:7] + [0] + args[8:]), 0) == mqa.ERR_INVALID_ARG  # the usual validation runs first
     assert fn(*(args[:14] + [2] + args[15:]), 0) == mqa.ERR_WORKSPACE_TOO_SMALL

@@ -134,3 +134,18 @@ def test_merge_workload_bytes():
     rows = spec["B"] * spec["H"]
     assert st["alg_bytes"] == spec["G"] * rows * spec["R"] * 2 + spec["G"] * rows * 4 + rows * spec["R"] * 2 + rows * 4
     assert st["in_bytes"] + st["out_bytes"] == st["alg_bytes"]
+
+
+def test_clock_reason_bits_and_summary():
+    # NVML clock-event reason bits (nvml.h): sw power cap 0x4, hw slowdown 0x8,
+    # sw thermal 0x20, hw thermal 0x40, hw power brake 0x80; idle (0x1) and
+    # application clocks (0x2) are not among the judged reasons
+    assert bench.decode_reasons(0) == []
+    assert bench.decode_reasons(0x1 | 0x2) == []
+    assert bench.decode_reasons(0x4) == ["sw_power_cap"]
+    assert bench.decode_reasons(0x8 | 0x40) == ["hw_slowdown", "hw_thermal_slowdown"]
+    assert bench.decode_reasons(0x20 | 0x80) == ["hw_power_brake_slowdown", "sw_thermal_slowdown"]
+    s = bench.summarize_clocks([(2070.0, []), (1980.0, ["sw_power_cap"]), (2070.0, [])], 2070.0, "test")
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3,
+                 "source": "test"}
+    assert bench.summarize_clocks([], 2070.0, "test")["samples"] == 0

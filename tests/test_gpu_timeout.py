@@ -1,6 +1,6 @@
 """Failure detection on the GPU without a fault or a hang: the library's test
-hook makes the producer of one work unit of the bf16 GQA kernel withhold its
-first tile, so the consumers' bounded wait (2 s) runs out.  The call must
+hook (include/mqa_decode_testing.h) makes the producer of one work unit of
+the bf16 GQA kernel withhold all its tiles, so the consumers' bounded wait (2 s) runs out.  The call must
 report MQA_ERR_DEVICE_TIMEOUT in the status word, every block must return,
 the other request must still be exact, and the context must stay usable."""
 import ctypes
@@ -17,7 +17,8 @@ from helpers import assert_close, run_gpu, run_oracle, subset, to_device
 pytestmark = pytest.mark.gpu
 
 
-def test_withheld_tile_times_out_and_reports():
+def test_withheld_tile_times_out_and_reports(monkeypatch):
+    monkeypatch.setenv("MQA_ENABLE_TEST_HOOKS", "1")
     lib = mqa.lib
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     fn = lib.mqa_test_gqa_withheld_arrive
