@@ -132,6 +132,14 @@ size_t gqa_paged_decode_workspace_bytes(int batch, int num_q_heads, int head_siz
  *   lse          fp32 [batch, num_heads] natural-log LSE of the scaled logits,
  *                or NULL.  (fp32 rather than the query dtype: a bf16 lse cannot
  *                carry the 1e-3 accuracy the merge across shards needs.)
+ *   With kv_dtype = MQA_KV_FP8_E4M3 and more than 32 query rows (num_heads
+ *   here, q_len * num_heads in mla_decode_multi) the tensor cores take the
+ *   query in f16 (the e4m3 codes widen to f16 exactly): every q entry must
+ *   lie within +-65504 (an entry beyond makes that row's out and lse
+ *   undefined, typically NaN; the other rows are unaffected), and entries
+ *   below 2^-14 in magnitude keep an absolute precision of 2^-24 only.  With a
+ *   bf16 cache, or 32 rows or fewer, the query is used in bf16 as given.
+ *   Valid tokens of an e4m3 cache hold finite codes (0x7F / 0xFF are NaN).
  *   head_size / kv_lora_rank must be 576/512 or 320/256 ("Triton と MLA" page,
  *   境界と失敗: head sizes 320 and 576 only).  page_size must be a multiple of
  *   16 ("AttentionBackend" page, "Limites et échecs": MultipleOf(16)).
