@@ -37,6 +37,18 @@ mqa_status mqa_test_gqa_withheld_arrive(const void* q, const void* kv_cache, con
                                         size_t workspace_bytes, int* device_status, void* stream,
                                         int withhold_unit);
 
+/* An mla_decode in which the producer of work unit `withhold_unit` fills and
+ * announces none of its tiles: with more than 32 heads the 2-CTA tensor-core
+ * cluster of that unit, else every 16-head block of that unit, waits in vain.
+ * Arguments as for mla_decode; withhold_unit >= 0 (with num_kv_splits == 1,
+ * unit b is request b). */
+mqa_status mqa_test_mla_withheld_arrive(const void* q, const void* kv_cache, const int32_t* block_table,
+                                        const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                                        int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
+                                        int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
+                                        void* workspace, size_t workspace_bytes, int* device_status, void* stream,
+                                        int withhold_unit);
+
 #ifdef __cplusplus
 }
 #endif

@@ -267,8 +267,9 @@ static mqa_status mla_decode_rows(const void* q, const void* kv_cache, const int
                       int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
                       int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
                       void* workspace, size_t workspace_bytes, int* device_status, void* stream,
-                      int q_len) {
-    // num_heads counts rows here: q_len query tokens x heads, token-major
+                      int q_len, int withhold = -1) {
+    // num_heads counts rows here: q_len query tokens x heads, token-major;
+    // withhold >= 0 only from the test hook mqa_test_mla_withheld_arrive
     if (!q || !kv_cache || !block_table || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
         !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (device_status && !aligned(device_status, 4)))
@@ -339,6 +340,7 @@ static mqa_status mla_decode_rows(const void* q, const void* kv_cache, const int
         t.H = num_heads;
         t.q_len = q_len;
         t.heads = num_heads / q_len;
+        t.withhold = withhold;
         t.num_blocks = num_blocks;
         t.plan.batch = batch;
         t.plan.page = page_size;
@@ -381,6 +383,7 @@ static mqa_status mla_decode_rows(const void* q, const void* kv_cache, const int
     a.H = num_heads;
     a.q_len = q_len;
     a.heads = num_heads / q_len;
+    a.withhold = withhold;
     a.num_blocks = num_blocks;
     a.plan.batch = batch;
     a.plan.page = page_size;
@@ -540,6 +543,7 @@ mqa_status mla_decode_sparse(const void* q, const void* kv_cache, const int32_t*
     a.H = num_heads;
     a.q_len = 1;
     a.heads = num_heads;
+    a.withhold = -1;
     a.num_blocks = num_blocks;
     const int tile = mqa::mla_mma_sparse_tile(fp8);
     a.plan.batch = batch;
@@ -691,6 +695,19 @@ mqa_status gqa_paged_decode(const void* q, const void* kv_cache, const int32_t* 
     return gqa_decode_impl(q, kv_cache, block_table, seq_lens, scale, k_scale, v_scale, out, lse, batch,
                            num_q_heads, num_kv_heads, head_size, num_blocks, page_size, max_blocks, kv_dtype,
                            num_kv_splits, workspace, workspace_bytes, device_status, stream, -1);
+}
+
+mqa_status mqa_test_mla_withheld_arrive(const void* q, const void* kv_cache, const int32_t* block_table,
+                                        const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                                        int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
+                                        int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
+                                        void* workspace, size_t workspace_bytes, int* device_status, void* stream,
+                                        int withhold_unit) {
+    if (!test_hooks_enabled()) return MQA_ERR_UNSUPPORTED;
+    if (withhold_unit < 0) return MQA_ERR_INVALID_ARG;
+    return mla_decode_rows(q, kv_cache, block_table, seq_lens, scale, k_scale, out, lse, batch, num_heads,
+                           head_size, kv_lora_rank, num_blocks, page_size, max_blocks, kv_dtype, num_kv_splits,
+                           workspace, workspace_bytes, device_status, stream, 1, withhold_unit);
 }
 
 mqa_status mqa_test_gqa_withheld_arrive(const void* q, const void* kv_cache, const int32_t* block_table,

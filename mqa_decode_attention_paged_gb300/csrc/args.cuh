@@ -44,6 +44,9 @@ struct MlaArgs {
     // cache_page tokens
     const int32_t* indices;
     int topk, cache_page, bt_stride;
+    // test hook of the bounded waits (-1 in every product call): the producer
+    // of work unit `withhold` fills and announces none of its tiles
+    int withhold;
     Plan plan;
 };
 
@@ -72,6 +75,7 @@ struct MlaTcArgs {
     float out_scale;
     int H, num_blocks;
     int q_len, heads;  // multi-token decode rows, as in MlaArgs
+    int withhold;      // test hook, as in MlaArgs (-1 in every product call)
     Plan plan;
 };
 

@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
             int issued[C::kStages];
             for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
             Look L0, L1, L2;
-            bool h0 = cur.next(a.plan, cum, lens, a.block_table);
+            bool h0 = unit != a.withhold && cur.next(a.plan, cum, lens, a.block_table);  // test hook
             if (h0) read_entries(cur, L0);
             bool h1 = h0 && cur.next(a.plan, cum, lens, a.block_table);
             if (h1) read_entries(cur, L1);
@@ -280,7 +280,9 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
             val = lane < nbox && tok < tc.tok_end;
             blk = val ? tc.bt[tok / P] : 0;
         };
-        bool have = cur.next(a.plan, cum, lens, a.block_table);
+        // test hook: the producer of the withheld unit fills and announces
+        // nothing, so its consumers' first wait runs out
+        bool have = unit != a.withhold && cur.next(a.plan, cum, lens, a.block_table);
         int blk = 0;
         bool val = false;
         int t0 = cur.t0, tend = cur.tok_end;

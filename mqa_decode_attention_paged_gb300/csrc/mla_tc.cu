@@ -250,7 +250,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         it.init(a.plan, cum, T, unit);
         Piece pc;
         int p = 0;
-        bool ok = true;
+        // test hook: the producer of the withheld unit fills and announces
+        // nothing, so its consumers' first waits run out
+        bool ok = unit != a.withhold;
         while (ok && it.next(cum, pc)) {
             int tok0, tok_end;
             const int npairs = piece_tiles(pc, tok0, tok_end) >> 1;

@@ -33,7 +33,7 @@ def test_header_symbols_are_exported():
     # the test hooks sit in their own header, not in the product interface
     product = open(os.path.join(ROOT, "include", "mqa_decode.h")).read()
     assert "mqa_test_" not in product
-    assert "mqa_test_gqa_withheld_arrive" in names
+    assert {"mqa_test_gqa_withheld_arrive", "mqa_test_mla_withheld_arrive"} <= set(names)
     assert {"mla_decode", "mla_decode_multi", "mla_decode_sparse", "gqa_paged_decode", "mqa_lse_merge",
             "mqa_num_kv_splits", "mla_decode_workspace_bytes",
             "gqa_paged_decode_workspace_bytes", "mqa_status_string", "mqa_abi_version",
@@ -234,3 +234,19 @@ def test_withheld_arrive_hook_validation(monkeypatch):
     assert fn(*args, -1) == mqa.ERR_INVALID_ARG          # a unit to withhold is required
     assert fn(*(args[:7] + [0] + args[8:]), 0) == mqa.ERR_INVALID_ARG  # the usual validation runs first
     assert fn(*(args[:14] + [2] + args[15:]), 0) == mqa.ERR_WORKSPACE_TOO_SMALL
+
+
+def test_mla_withheld_arrive_hook_validation(monkeypatch):
+    fn = mqa.lib.mqa_test_mla_withheld_arrive
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    fn.restype = I
+    fn.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P, I]
+    f = ctypes.c_void_p(FAKE)
+    args = [f, f, f, f, 0.07, 1.0, f, None, 2, 16, 576, 512, 10, 16, 8, 0, 1, None, 0, None, None]
+    monkeypatch.delenv("MQA_ENABLE_TEST_HOOKS", raising=False)
+    assert fn(*args, 0) == mqa.ERR_UNSUPPORTED          # gated
+    monkeypatch.setenv("MQA_ENABLE_TEST_HOOKS", "1")
+    assert fn(*args, -1) == mqa.ERR_INVALID_ARG         # a unit to withhold is required
+    assert fn(*(args[:8] + [0] + args[9:]), 0) == mqa.ERR_INVALID_ARG   # the usual validation runs first
+    assert fn(*(args[:10] + [320] + args[11:]), 0) == mqa.ERR_UNSUPPORTED
+    assert fn(*(args[:16] + [2] + args[17:]), 0) == mqa.ERR_WORKSPACE_TOO_SMALL

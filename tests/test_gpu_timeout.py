@@ -1,8 +1,11 @@
 """Failure detection on the GPU without a fault or a hang: the library's test
-hook (include/mqa_decode_testing.h) makes the producer of one work unit of
-the bf16 GQA kernel withhold all its tiles, so the consumers' bounded wait (2 s) runs out.  The call must
-report MQA_ERR_DEVICE_TIMEOUT in the status word, every block must return,
-the other request must still be exact, and the context must stay usable."""
+hooks (include/mqa_decode_testing.h) make the producer of one work unit
+withhold all its tiles, so the consumers' bounded waits (2 s) run out.  This
+is done for the bf16 GQA kernel and for both MLA kernels (the 2-CTA
+tensor-core kernel of more than 32 heads, the warp-MMA kernel of 16 heads),
+with bf16 and e4m3 caches.  The call must report MQA_ERR_DEVICE_TIMEOUT in
+the status word, every block must return, the other request must still be
+exact, and the context must stay usable for a normal call."""
 import ctypes
 
 import numpy as np
@@ -45,3 +48,41 @@ def test_withheld_tile_times_out_and_reports(monkeypatch):
     o2, l2 = run_gpu(case, 2)
     ref_out, ref_lse = run_oracle(case)
     assert_close(o2, l2, ref_out, ref_lse, what="after the timeout")
+
+
+def _mla_hook():
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    fn = mqa.lib.mqa_test_mla_withheld_arrive
+    fn.restype = I
+    fn.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P, I]
+    return fn
+
+
+@pytest.mark.parametrize("H,kv_dtype", [(128, "bf16"), (128, "fp8_e4m3"), (16, "bf16"), (16, "fp8_e4m3")])
+def test_mla_withheld_tile_times_out_and_reports(monkeypatch, H, kv_dtype):
+    # More than 32 heads: the 2-CTA tensor-core cluster of unit 0 (both CTAs)
+    # waits in vain for its first pair; 16 heads: the warp-MMA block of unit 0
+    # waits in vain for its first tile.  Unit 1 (request 1) is untouched.
+    monkeypatch.setenv("MQA_ENABLE_TEST_HOOKS", "1")
+    fn = _mla_hook()
+    case = synth.make_mla_case([300, 200], H=H, page=64, kv_dtype=kv_dtype, k_scale=0.05, seed=42)
+    q, kv, bt, sl = to_device(case)
+    B, Hh, D = q.shape
+    R = case.kv_lora_rank
+    out = torch.full((B, Hh, R), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, Hh), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    kvd = mqa.KV_BF16 if kv_dtype == "bf16" else mqa.KV_FP8_E4M3
+    rc = fn(ptr(q), ptr(kv), ptr(bt), ptr(sl), case.scale, case.k_scale, ptr(out), ptr(lse), B, Hh, D, R,
+            case.num_blocks, case.page, case.max_blocks, kvd, 1, None, 0, ptr(status), stream, 0)
+    assert rc == mqa.OK
+    torch.cuda.synchronize()  # returns: every wait has a time limit
+    assert int(status.item()) == mqa.ERR_DEVICE_TIMEOUT
+    ref_out, ref_lse = run_oracle(subset(case, [1]))
+    assert_close(out.double().cpu().numpy()[[1]], lse.double().cpu().numpy()[[1]], ref_out, ref_lse,
+                 fp8=kv_dtype != "bf16", what="other request")
+    o2, l2 = run_gpu(case, 3)
+    ref_out, ref_lse = run_oracle(case)
+    assert_close(o2, l2, ref_out, ref_lse, fp8=kv_dtype != "bf16", what="after the timeout")
