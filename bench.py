@@ -23,6 +23,10 @@ launching stream (the flush is outside the events).  Under torchrun every rank r
 has no cross-GPU exchange), the timed region is bracketed by a barrier and
 synchronize on both sides, and rank 0 reports the max over ranks.
 
+`--split-mode fixed` times the dense MLA workloads with one work unit per
+request and split (every request cut into num_kv_splits equal page ranges,
+`mla_decode_fixed_splits`) instead of the page-balanced units of `mla_decode`.
+
 `--impl reference` times the CPU oracle instead (no GPU work), on the same
 workload, with a bounded sample of requests per step.
 """
@@ -607,6 +611,9 @@ def run_ours(args):
     from mqa_decode_attention_paged_gb300 import synth
 
     case = synth.workload(args.workload)
+    if args.split_mode == "fixed" and (case.kind != "mla" or case.meta.get("indices") is not None
+                                       or case.meta.get("q_len", 1) > 1):
+        raise SystemExit("--split-mode fixed serves the dense single-token MLA workloads")
     st = workload_stats(case, 1)
     sms = mqa.device_sm_count()
     idx_np = case.meta.get("indices")
@@ -657,8 +664,9 @@ def run_ours(args):
                                  out=oo.view(B, q_len, hh, R), lse=ll.view(B, q_len, hh),
                                  num_kv_splits=splits, workspace=ws, kv_lora_rank=R, stream=stream)
         elif case.kind == "mla":
-            mqa.mla_decode(qq, kv, btt, sll, case.scale, case.k_scale, out=oo, lse=ll,
-                           num_kv_splits=splits, workspace=ws, kv_lora_rank=R, stream=stream)
+            fn = mqa.mla_decode_fixed_splits if args.split_mode == "fixed" else mqa.mla_decode
+            fn(qq, kv, btt, sll, case.scale, case.k_scale, out=oo, lse=ll, num_kv_splits=splits, workspace=ws,
+               kv_lora_rank=R, stream=stream)
         else:
             mqa.gqa_paged_decode(qq, kv, btt, sll, case.scale, case.k_scale, case.v_scale, out=oo,
                                  lse=ll, num_kv_splits=splits, workspace=ws, stream=stream,
@@ -733,7 +741,8 @@ def run_ours(args):
     traffic = None
     tr = NCU_TRAFFIC.get(args.workload)
     traffic_kernel = None
-    if tr and tr.get("src_sha") == kernel_sources_sha(tr["files"]) and tr.get("splits") == splits:
+    if (tr and tr.get("src_sha") == kernel_sources_sha(tr["files"]) and tr.get("splits") == splits
+            and args.split_mode == "balanced"):
         traffic = tr["bytes"]
         traffic_kernel = tr["kernel"] + " (stage 1 only)"
     if bound == "hbm":
@@ -768,7 +777,7 @@ def run_ours(args):
                   "int8_pth": "bf16 (int8 KV, per-token-head scales)",
                   "int4_pth": "bf16 (int4 KV, per-token-head scales)"}[case.kv_dtype],
         "data": "synthetic (seeded N(0,1) q/KV, random block permutation)",
-        "config": workload_config(case, args.workload, splits),
+        "config": dict(workload_config(case, args.workload, splits), split_mode=args.split_mode),
         "roofline": roof, "cpu_baseline": cpu,
         "e2e": {"value": round(job_throughput_gbs(world, st["kv_bytes"], e2e_ms), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -792,6 +801,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mla_v3_fp8")
     ap.add_argument("--splits", type=int, default=0, help="num_kv_splits (0 = heuristic)")
+    ap.add_argument("--split-mode", default="balanced", choices=["balanced", "fixed"],
+                    help="balanced: num_kv_splits is a partial budget over page-balanced units (mla_decode); "
+                         "fixed: one unit per request and split, equal page ranges (mla_decode_fixed_splits)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
     args = ap.parse_args()

@@ -155,6 +155,24 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
                       int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
                       void* workspace, size_t workspace_bytes, int* device_status, void* stream);
 
+/* mla_decode with the split of the Triton MLA backend taken literally: each
+ * request is cut into num_kv_splits page ranges of ceil(pages /
+ * num_kv_splits) pages and one work unit (thread block, or 2-CTA cluster
+ * with more than 32 heads) decodes each (request, range), whereas mla_decode
+ * treats num_kv_splits as a partial budget and cuts the batch's pages into
+ * units of equal size ("Triton と MLA" page, 主要ファイル / データフロー:
+ * one program per request and split; tutorial page lshu.cn/news/265860,
+ * §12).  A request's reduction order depends only on its own length and
+ * num_kv_splits, so the result is bitwise reproducible and independent of
+ * the rest of the batch at ANY num_kv_splits (mla_decode: only at 1).  Slower
+ * when the lengths are uneven.  Arguments, workspace, results and errors as
+ * for mla_decode; batch * num_kv_splits <= 2^24 (else MQA_ERR_UNSUPPORTED). */
+mqa_status mla_decode_fixed_splits(const void* q, const void* kv_cache, const int32_t* block_table,
+                                   const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                                   int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
+                                   int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
+                                   void* workspace, size_t workspace_bytes, int* device_status, void* stream);
+
 /* Multi-token MLA decode: q_len new positions of each request verified in
  * one call (speculative decoding).  The tutorial page (lshu.cn/news/265860)
  * §10 gives the structure: query i of q_len sits at absolute position
@@ -234,6 +252,88 @@ mqa_status mla_decode_sparse(const void* q, const void* kv_cache, const int32_t*
  *   Allocates nothing; enqueues one kernel on `stream`. */
 mqa_status mqa_lse_merge(const void* shard_out, const float* shard_lse, void* out, float* lse, int num_shards,
                          long long rows, int head_dim, void* stream);
+
+/* ---- Decode context parallelism: page placement and the exchange ---------
+ *
+ * The pages say that DCP shards of a sequence are merged by LogSumExp, which
+ * is why the decode returns a natural-log lse, and they name the merge
+ * cp_lse_ag_out_rs ("Triton と MLA" page, 設計動機; "AttentionBackend" page,
+ * Motivation de conception, on the lse base).  Where the pages stop, the
+ * library reads it as follows: every rank holds whole pages of a request
+ * (page-aligned shards, so each shard is an ordinary paged sequence that
+ * mla_decode / gqa_paged_decode take as is), the lse of every shard is
+ * all-gathered, and each rank scales its own shard output by its weight so
+ * that a sum reduce-scatter over the ranks yields the merged output, split by
+ * heads.  The alternative, all-gathering the outputs and calling
+ * mqa_lse_merge, is served as well.  Positions play no part in a q_len = 1
+ * decode, so a shard's decode is exact; the placement does not serve
+ * multi-token or index-sparse decode.  The collectives are the caller's. */
+
+typedef enum mqa_dcp_layout {
+    /* page j of a request lives on rank j % num_ranks: a page never moves as
+     * its sequence grows (the placement a serving system keeps) */
+    MQA_DCP_ROUND_ROBIN = 0,
+    /* rank g holds pages [g L, min((g + 1) L, n_pages)) with
+     * L = ceil(n_pages / num_ranks): contiguous runs, for a fixed sequence */
+    MQA_DCP_CONTIGUOUS = 1
+} mqa_dcp_layout;
+
+/* Columns of a rank's block table under either layout:
+ * ceil(max_blocks / num_ranks), or -1 if max_blocks < 1 or num_ranks < 1. */
+int mqa_dcp_shard_max_blocks(int max_blocks, int num_ranks);
+
+/* The pages rank `rank` of `num_ranks` holds, as a block table and lengths
+ * that the decode entry points take directly.  HOST pointers (the one
+ * exception to the device-pointer convention): no GPU is touched and nothing
+ * is enqueued.
+ *
+ *   block_table       int32 [batch, max_blocks]: the whole sequences' pages.
+ *   seq_lens          int32 [batch], 0 <= seq_lens[b] <= max_blocks * page_size.
+ *   shard_block_table int32 [batch, shard_max_blocks] out: the rank's pages of
+ *                     request b in sequence order, then -1.
+ *   shard_seq_lens    int32 [batch] out: tokens in those pages (every page
+ *                     full except the sequence's last one, which is always
+ *                     the last page of the rank that holds it).
+ *   shard_max_blocks  >= mqa_dcp_shard_max_blocks(max_blocks, num_ranks).
+ * Over the ranks the shards cover each sequence's tokens exactly once.
+ * Errors: MQA_ERR_INVALID_ARG for a null pointer, a bad size, rank outside
+ * [0, num_ranks), an unknown layout or a sequence length out of range
+ * (nothing is written then). */
+mqa_status mqa_dcp_shard(const int32_t* block_table, const int32_t* seq_lens, int batch, int max_blocks,
+                         int page_size, int num_ranks, int rank, mqa_dcp_layout layout,
+                         int32_t* shard_block_table, int shard_max_blocks, int32_t* shard_seq_lens);
+
+/* Where token `pos` of a sequence of seq_len tokens lives: the rank and its
+ * position in that rank's shard (the slot a cache writer fills).  Host only;
+ * pos in [0, seq_len), else MQA_ERR_INVALID_ARG. */
+mqa_status mqa_dcp_locate(int pos, int seq_len, int page_size, int num_ranks, mqa_dcp_layout layout, int* rank,
+                          int* shard_pos);
+
+/* The local step of the all-gather-lse / reduce-scatter-output merge: with
+ * every rank's shard lse gathered, rank `rank` scales its normalised shard
+ * output by its weight in the merge,
+ *   lse = m + ln sum_g e^{lse_g - m},  m = max_g lse_g,
+ *   scaled = e^{lse_rank - lse} * shard_out     (0 where lse_rank = -inf),
+ * so that the sum over the ranks of `scaled` is the merged output of
+ * mqa_lse_merge.  `scaled` is written in the order a sum reduce-scatter over
+ * the ranks wants (NCCL's reduce-scatter splits its input into num_ranks
+ * consecutive chunks): chunk c holds heads [c H / num_ranks, (c + 1) H /
+ * num_ranks) of every request, so after it rank c holds its heads' merged
+ * output.
+ *
+ *   shard_out     bf16 [batch, num_heads, head_dim]: this rank's shard result.
+ *   gathered_lse  fp32 [num_ranks, batch, num_heads]: every rank's shard lse.
+ *   scaled        [num_ranks, batch, num_heads / num_ranks, head_dim], fp32
+ *                 if scaled_fp32, else bf16 (half the exchange bytes, one
+ *                 more rounding per term).
+ *   lse           fp32 [batch, num_heads] or NULL: the merged lse (-inf where
+ *                 no rank holds a token; scaled is 0 there).
+ *   num_heads a multiple of num_ranks; head_dim a multiple of 8 in [8, 4096];
+ *   0 <= rank < num_ranks; device pointers, 16-byte aligned.  Allocates
+ *   nothing; enqueues one kernel on `stream`. */
+mqa_status mqa_dcp_scale_shard(const void* shard_out, const float* gathered_lse, void* scaled, float* lse,
+                               int num_ranks, int rank, int batch, int num_heads, int head_dim, int scaled_fp32,
+                               void* stream);
 
 /* Size of the library-owned scratch array used by mla_decode_noalloc. */
 #define MQA_NOALLOC_SCRATCH_BYTES (64u << 20)

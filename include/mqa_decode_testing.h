@@ -49,6 +49,22 @@ mqa_status mqa_test_mla_withheld_arrive(const void* q, const void* kv_cache, con
                                         void* workspace, size_t workspace_bytes, int* device_status, void* stream,
                                         int withhold_unit);
 
+/* An e4m3-cache mla_decode with more than 32 heads (the 2-CTA tensor-core
+ * kernel) in which softmax warp `warp` (2..9) of both CTAs of work unit
+ * `unit` gives up before its first pair as if one of its waits had expired,
+ * while the other warps of its group go on: the group's widening barriers
+ * must not block them (the warp that gives up makes its remaining arrivals
+ * there), every wait that then misses that warp's arrivals runs out, and the
+ * call reports MQA_ERR_DEVICE_TIMEOUT.  Arguments as for mla_decode with
+ * kv_dtype = MQA_KV_FP8_E4M3; MQA_ERR_INVALID_ARG for unit < 0, a warp
+ * outside 2..9 or num_heads <= 32. */
+mqa_status mqa_test_mla_warp_gives_up(const void* q, const void* kv_cache, const int32_t* block_table,
+                                      const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                                      int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
+                                      int page_size, int max_blocks, int num_kv_splits, void* workspace,
+                                      size_t workspace_bytes, int* device_status, void* stream, int unit,
+                                      int warp);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,7 +16,7 @@ def _load_binding():
 
 def __getattr__(name):
     exported = {
-        "mla_decode", "mla_decode_multi", "mla_decode_sparse", "gqa_paged_decode", "lse_merge", "num_kv_splits",
+        "mla_decode", "mla_decode_fixed_splits", "mla_decode_multi", "mla_decode_sparse", "gqa_paged_decode", "lse_merge", "num_kv_splits",
         "mla_decode_workspace_bytes", "gqa_paged_decode_workspace_bytes", "status_string", "abi_version", "device_sm_count",
         "MqaError",
     }

@@ -65,6 +65,8 @@ def _load() -> ctypes.CDLL:
     lib.gqa_paged_decode_workspace_bytes.argtypes = [I, I, I, I]
     lib.mla_decode.restype = I
     lib.mla_decode.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
+    lib.mla_decode_fixed_splits.restype = I
+    lib.mla_decode_fixed_splits.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
     lib.mla_decode_multi.restype = I
     lib.mla_decode_multi.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
     lib.mla_decode_sparse.restype = I
@@ -75,6 +77,14 @@ def _load() -> ctypes.CDLL:
     lib.gqa_paged_decode.argtypes = [P, P, P, P, F, F, F, P, P, I, I, I, I, I, I, I, I, I, P, SZ, P, P]
     lib.mqa_lse_merge.restype = I
     lib.mqa_lse_merge.argtypes = [P, P, P, P, I, ctypes.c_longlong, I, P]
+    lib.mqa_dcp_shard_max_blocks.restype = I
+    lib.mqa_dcp_shard_max_blocks.argtypes = [I, I]
+    lib.mqa_dcp_shard.restype = I
+    lib.mqa_dcp_shard.argtypes = [P, P, I, I, I, I, I, I, P, I, P]
+    lib.mqa_dcp_locate.restype = I
+    lib.mqa_dcp_locate.argtypes = [I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]
+    lib.mqa_dcp_scale_shard.restype = I
+    lib.mqa_dcp_scale_shard.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
     return lib
 
 
@@ -183,6 +193,23 @@ def mla_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *, out=No
     """MLA decode through the C ABI.  q [B,H,D] bf16, kv_cache [num_blocks, page, D],
     block_table [B, max_blocks] int32, seq_lens [B] int32 (all on one CUDA device).
     Allocates out / lse / workspace with torch when they are not given."""
+    return _mla_decode(lib.mla_decode, "mla_decode", q, kv_cache, block_table, seq_lens, scale, k_scale, out,
+                       lse, num_kv_splits, workspace, kv_lora_rank, kv_dtype, device_status, stream, return_lse)
+
+
+def mla_decode_fixed_splits(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *, out=None, lse=None,
+                            num_kv_splits=1, workspace=None, kv_lora_rank=None, kv_dtype=None,
+                            device_status=None, stream=None, return_lse=True):
+    """``mla_decode`` with one work unit per (request, split): every request
+    cut into num_kv_splits equal page ranges (batch-invariant at any split
+    count).  Same arguments and results as :func:`mla_decode`."""
+    return _mla_decode(lib.mla_decode_fixed_splits, "mla_decode_fixed_splits", q, kv_cache, block_table,
+                       seq_lens, scale, k_scale, out, lse, num_kv_splits, workspace, kv_lora_rank, kv_dtype,
+                       device_status, stream, return_lse)
+
+
+def _mla_decode(fn, name, q, kv_cache, block_table, seq_lens, scale, k_scale, out, lse, num_kv_splits, workspace,
+                kv_lora_rank, kv_dtype, device_status, stream, return_lse):
     import torch
     B, H, D = q.shape
     nb, page, D2 = kv_cache.shape
@@ -200,12 +227,11 @@ def mla_decode(q, kv_cache, block_table, seq_lens, scale, k_scale=1.0, *, out=No
     _check_common(q, kv_cache, code, block_table, seq_lens, out, (B, H, R), lse, (B, H), workspace,
                   device_status)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib.mla_decode(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), float(scale),
-                        float(k_scale), _ptr(out), _ptr(lse), B, H, D, R, nb, page,
-                        block_table.shape[1], code, int(num_kv_splits), _ptr(workspace), ws_bytes,
-                        _ptr(device_status), _stream(stream))
+    rc = fn(_ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), float(scale), float(k_scale), _ptr(out),
+            _ptr(lse), B, H, D, R, nb, page, block_table.shape[1], code, int(num_kv_splits), _ptr(workspace),
+            ws_bytes, _ptr(device_status), _stream(stream))
     if rc != OK:
-        raise MqaError(rc, "mla_decode")
+        raise MqaError(rc, name)
     return out, lse
 
 
@@ -341,6 +367,83 @@ def lse_merge(shard_out, shard_lse, *, out=None, lse=None, stream=None, return_l
     if rc != OK:
         raise MqaError(rc, "mqa_lse_merge")
     return out, lse
+
+
+DCP_LAYOUTS = {"round_robin": 0, "contiguous": 1}
+
+
+def _dcp_layout(layout):
+    if layout not in DCP_LAYOUTS:
+        raise ValueError(f"layout must be one of {sorted(DCP_LAYOUTS)}, got {layout!r}")
+    return DCP_LAYOUTS[layout]
+
+
+def dcp_shard_max_blocks(max_blocks: int, num_ranks: int) -> int:
+    n = int(lib.mqa_dcp_shard_max_blocks(int(max_blocks), int(num_ranks)))
+    if n < 0:
+        raise ValueError("max_blocks and num_ranks must be >= 1")
+    return n
+
+
+def dcp_shard(block_table, seq_lens, page_size, num_ranks, rank, layout="round_robin"):
+    """Pages of rank `rank` of `num_ranks` under decode context parallelism
+    (host arrays, C ABI ``mqa_dcp_shard``): block_table int32 [B, max_blocks]
+    and seq_lens int32 [B] (numpy or CPU tensors) give the whole sequences;
+    returns numpy (shard_block_table int32 [B, ceil(max_blocks / num_ranks)],
+    shard_seq_lens int32 [B]) for the decode entry points."""
+    import numpy as np
+    bt = np.ascontiguousarray(np.asarray(block_table), dtype=np.int32)
+    sl = np.ascontiguousarray(np.asarray(seq_lens), dtype=np.int32)
+    if bt.ndim != 2 or sl.shape != (bt.shape[0],):
+        raise ValueError("block_table must be [B, max_blocks] and seq_lens [B]")
+    B, mb = bt.shape
+    width = dcp_shard_max_blocks(mb, num_ranks)
+    table = np.empty((B, width), dtype=np.int32)
+    lens = np.empty(B, dtype=np.int32)
+    rc = lib.mqa_dcp_shard(bt.ctypes.data, sl.ctypes.data, B, mb, int(page_size), int(num_ranks), int(rank),
+                           _dcp_layout(layout), table.ctypes.data, width, lens.ctypes.data)
+    if rc != OK:
+        raise MqaError(rc, "mqa_dcp_shard")
+    return table, lens
+
+
+def dcp_locate(pos, seq_len, page_size, num_ranks, layout="round_robin"):
+    """(rank, position in that rank's shard) of token `pos` of a sequence of
+    seq_len tokens (C ABI ``mqa_dcp_locate``)."""
+    r, p = ctypes.c_int(), ctypes.c_int()
+    rc = lib.mqa_dcp_locate(int(pos), int(seq_len), int(page_size), int(num_ranks), _dcp_layout(layout),
+                            ctypes.byref(r), ctypes.byref(p))
+    if rc != OK:
+        raise MqaError(rc, "mqa_dcp_locate")
+    return r.value, p.value
+
+
+def dcp_scale_shard(shard_out, gathered_lse, rank, *, scaled=None, lse=None, scaled_fp32=True, stream=None,
+                    return_lse=True):
+    """This rank's share of the merged output, laid out for a sum
+    reduce-scatter over the ranks (C ABI ``mqa_dcp_scale_shard``):
+    shard_out bf16 [B, H, D], gathered_lse fp32 [G, B, H]; returns (scaled
+    [G, B, H / G, D] fp32 or bf16, merged lse [B, H] fp32)."""
+    import torch
+    B, H, D = shard_out.shape
+    G = gathered_lse.shape[0]
+    if H % G != 0:
+        raise ValueError("the head count must be a multiple of the number of ranks")
+    sdt = torch.float32 if scaled_fp32 else torch.bfloat16
+    if scaled is None:
+        scaled = torch.empty((G, B, H // G, D), dtype=sdt, device=shard_out.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=shard_out.device)
+    _check(shard_out, "shard_out", (torch.bfloat16,))
+    _check(gathered_lse, "gathered_lse", (torch.float32,), shape=(G, B, H))
+    _check(scaled, "scaled", (sdt,), shape=(G, B, H // G, D))
+    _check(lse, "lse", (torch.float32,), shape=(B, H), optional=True)
+    _on_device([("shard_out", shard_out), ("gathered_lse", gathered_lse), ("scaled", scaled), ("lse", lse)])
+    rc = lib.mqa_dcp_scale_shard(_ptr(shard_out), _ptr(gathered_lse), _ptr(scaled), _ptr(lse), int(G), int(rank),
+                                 int(B), int(H), int(D), int(bool(scaled_fp32)), _stream(stream))
+    if rc != OK:
+        raise MqaError(rc, "mqa_dcp_scale_shard")
+    return scaled, lse
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20

@@ -15,6 +15,7 @@
 #include "args.cuh"
 #include "gqa_q8.cuh"
 #include "shard_merge.cuh"
+#include "dcp.cuh"
 #include "gqa_test.cuh"
 
 namespace {
@@ -267,9 +268,11 @@ static mqa_status mla_decode_rows(const void* q, const void* kv_cache, const int
                       int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
                       int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
                       void* workspace, size_t workspace_bytes, int* device_status, void* stream,
-                      int q_len, int withhold = -1) {
+                      int q_len, int withhold = -1, bool fixed_splits = false, int give_up = -1) {
     // num_heads counts rows here: q_len query tokens x heads, token-major;
-    // withhold >= 0 only from the test hook mqa_test_mla_withheld_arrive
+    // withhold >= 0 only from the test hook mqa_test_mla_withheld_arrive;
+    // fixed_splits: one unit per (request, range) instead of page-balanced units;
+    // give_up >= 0 only from the test hook mqa_test_mla_warp_gives_up
     if (!q || !kv_cache || !block_table || !seq_lens || !out) return MQA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(block_table, 4) ||
         !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (device_status && !aligned(device_status, 4)))
@@ -290,10 +293,15 @@ static mqa_status mla_decode_rows(const void* q, const void* kv_cache, const int
     if (need > 0 && (!workspace || workspace_bytes < need)) return MQA_ERR_WORKSPACE_TOO_SMALL;
     if (need > 0 && !aligned(workspace, 16)) return MQA_ERR_INVALID_ARG;
 
+    // fixed-split mode launches batch * num_kv_splits units (times the head
+    // groups on the warp-MMA path)
+    if (fixed_splits && static_cast<long long>(batch) * num_kv_splits > (1LL << 24)) return MQA_ERR_UNSUPPORTED;
+
     const int sms = sm_count_current();
     if (sms < 1) return MQA_ERR_CUDA;
     const bool fp8 = kv_dtype == MQA_KV_FP8_E4M3;
     const int groups = (num_heads + 15) / 16;
+    const bool fixed = fixed_splits && num_kv_splits > 1;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t slots_tc = static_cast<size_t>(batch) * num_kv_splits;
@@ -341,12 +349,16 @@ static mqa_status mla_decode_rows(const void* q, const void* kv_cache, const int
         t.q_len = q_len;
         t.heads = num_heads / q_len;
         t.withhold = withhold;
+        t.give_up = give_up;
         t.num_blocks = num_blocks;
         t.plan.batch = batch;
         t.plan.page = page_size;
         t.plan.max_blocks = max_blocks;
         t.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
-        t.plan.units = t.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms / 2);
+        t.plan.fixed_splits = fixed ? num_kv_splits : 0;
+        t.plan.units = t.plan.per_seq ? batch
+                       : fixed        ? batch * num_kv_splits
+                                      : balanced_units(batch, num_kv_splits, sms / 2);
         if (cudaError_t e = mqa::mla_tc_stage1(t, head_size, fp8, t.plan.units, st); e != cudaSuccess)
             return cuda_fail(e);
         if (!t.plan.per_seq) {
@@ -389,7 +401,10 @@ static mqa_status mla_decode_rows(const void* q, const void* kv_cache, const int
     a.plan.page = page_size;
     a.plan.max_blocks = max_blocks;
     a.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
-    a.plan.units = a.plan.per_seq ? batch : balanced_units(batch, num_kv_splits, sms / groups);
+    a.plan.fixed_splits = fixed ? num_kv_splits : 0;
+    a.plan.units = a.plan.per_seq ? batch
+                   : fixed        ? batch * num_kv_splits
+                                  : balanced_units(batch, num_kv_splits, sms / groups);
 
     {
         // tensor boxes never straddle a page: 64 rows when pages are multiples
@@ -470,6 +485,16 @@ mqa_status mla_decode(const void* q, const void* kv_cache, const int32_t* block_
     return mla_decode_rows(q, kv_cache, block_table, seq_lens, scale, k_scale, out, lse, batch, num_heads,
                            head_size, kv_lora_rank, num_blocks, page_size, max_blocks, kv_dtype, num_kv_splits,
                            workspace, workspace_bytes, device_status, stream, 1);
+}
+
+mqa_status mla_decode_fixed_splits(const void* q, const void* kv_cache, const int32_t* block_table,
+                                  const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                                  int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
+                                  int page_size, int max_blocks, mqa_kv_dtype kv_dtype, int num_kv_splits,
+                                  void* workspace, size_t workspace_bytes, int* device_status, void* stream) {
+    return mla_decode_rows(q, kv_cache, block_table, seq_lens, scale, k_scale, out, lse, batch, num_heads,
+                           head_size, kv_lora_rank, num_blocks, page_size, max_blocks, kv_dtype, num_kv_splits,
+                           workspace, workspace_bytes, device_status, stream, 1, -1, true);
 }
 
 mqa_status mla_decode_multi(const void* q, const void* kv_cache, const int32_t* block_table,
@@ -584,6 +609,25 @@ mqa_status mqa_lse_merge(const void* shard_out, const float* shard_lse, void* ou
     if (cudaError_t e = mqa::shard_merge(static_cast<const __nv_bfloat16*>(shard_out), shard_lse,
                                          static_cast<__nv_bfloat16*>(out), lse, num_shards, rows, head_dim,
                                          static_cast<cudaStream_t>(stream));
+        e != cudaSuccess)
+        return cuda_fail(e);
+    return MQA_OK;
+}
+
+mqa_status mqa_dcp_scale_shard(const void* shard_out, const float* gathered_lse, void* scaled, float* lse,
+                               int num_ranks, int rank, int batch, int num_heads, int head_dim, int scaled_fp32,
+                               void* stream) {
+    if (!shard_out || !gathered_lse || !scaled) return MQA_ERR_INVALID_ARG;
+    if (!aligned(shard_out, 16) || !aligned(gathered_lse, 16) || !aligned(scaled, 16) || (lse && !aligned(lse, 16)))
+        return MQA_ERR_INVALID_ARG;
+    if (num_ranks < 1 || rank < 0 || rank >= num_ranks || batch < 1 || num_heads < 1 ||
+        num_heads % num_ranks != 0 || head_dim < 8 || head_dim > 4096 || head_dim % 8 != 0)
+        return MQA_ERR_INVALID_ARG;
+    // grid of batch * num_heads / 4 blocks
+    if (static_cast<long long>(batch) * num_heads > 4LL * 0x7fffffffLL) return MQA_ERR_UNSUPPORTED;
+    if (cudaError_t e = mqa::dcp_scale(static_cast<const __nv_bfloat16*>(shard_out), gathered_lse, scaled, lse,
+                                       num_ranks, rank, batch, num_heads, head_dim, scaled_fp32 != 0,
+                                       static_cast<cudaStream_t>(stream));
         e != cudaSuccess)
         return cuda_fail(e);
     return MQA_OK;
@@ -708,6 +752,21 @@ mqa_status mqa_test_mla_withheld_arrive(const void* q, const void* kv_cache, con
     return mla_decode_rows(q, kv_cache, block_table, seq_lens, scale, k_scale, out, lse, batch, num_heads,
                            head_size, kv_lora_rank, num_blocks, page_size, max_blocks, kv_dtype, num_kv_splits,
                            workspace, workspace_bytes, device_status, stream, 1, withhold_unit);
+}
+
+mqa_status mqa_test_mla_warp_gives_up(const void* q, const void* kv_cache, const int32_t* block_table,
+                                      const int32_t* seq_lens, float scale, float k_scale, void* out, float* lse,
+                                      int batch, int num_heads, int head_size, int kv_lora_rank, int num_blocks,
+                                      int page_size, int max_blocks, int num_kv_splits, void* workspace,
+                                      size_t workspace_bytes, int* device_status, void* stream, int unit,
+                                      int warp) {
+    if (!test_hooks_enabled()) return MQA_ERR_UNSUPPORTED;
+    // the tensor-core kernel's softmax warps are warps 2..9 of each CTA
+    if (unit < 0 || warp < 2 || warp > 9 || num_heads <= 32) return MQA_ERR_INVALID_ARG;
+    return mla_decode_rows(q, kv_cache, block_table, seq_lens, scale, k_scale, out, lse, batch, num_heads,
+                           head_size, kv_lora_rank, num_blocks, page_size, max_blocks, MQA_KV_FP8_E4M3,
+                           num_kv_splits, workspace, workspace_bytes, device_status, stream, 1, -1, false,
+                           unit * 16 + warp);
 }
 
 mqa_status mqa_test_gqa_withheld_arrive(const void* q, const void* kv_cache, const int32_t* block_table,

@@ -76,6 +76,9 @@ struct MlaTcArgs {
     int H, num_blocks;
     int q_len, heads;  // multi-token decode rows, as in MlaArgs
     int withhold;      // test hook, as in MlaArgs (-1 in every product call)
+    // test hook (-1 in every product call): softmax warp give_up % 16 of unit
+    // give_up / 16 gives up before its first pair as if a wait had expired
+    int give_up;
     Plan plan;
 };
 

@@ -62,11 +62,24 @@ __global__ void __launch_bounds__(32 * kMergeWarps, G == 4 ? 6 : 1) lse_merge_ke
     const long long orow = (static_cast<long long>(b) * a.H + h) * R;
     const int col = q * kMergeCols + 4 * lane;  // first column of the lane's group k: col + 128 k
 
-    int gf = 0, gl = 0;
-    if (n_b > 0) {
+    // the request's partials: np consecutive slots from slot0
+    const int S = a.plan.fixed_splits;
+    int gf = 0, np = 0, slot0 = 0;
+    if (S > 0) {
+        // fixed-split mode: ranges of L pages, range s in slot b S + s; range
+        // 0 wrote the output directly when it held the whole request (or the
+        // request has no page)
+        if (n_b == 0) return;
+        const int L = (n_b + S - 1) / S;
+        if (L >= n_b) return;
+        np = (n_b + L - 1) / L;
+        slot0 = b * S;
+    } else if (n_b > 0) {
         gf = unit_of_page(a.plan.units, total, before);
-        gl = unit_of_page(a.plan.units, total, before + n_b - 1);
+        const int gl = unit_of_page(a.plan.units, total, before + n_b - 1);
         if (gf == gl) return;  // one unit covered the request and wrote it directly
+        np = gl - gf + 1;
+        slot0 = gf + b;
     }
     pdl_wait();  // stage-1 partials (and the outputs' previous readers) are done
     if (n_b == 0) {  // empty request: out = 0, lse = -inf
@@ -77,14 +90,14 @@ __global__ void __launch_bounds__(32 * kMergeWarps, G == 4 ? 6 : 1) lse_merge_ke
         return;
     }
 
-    // Units between gf and gl overlap request b unless their page range is
-    // empty (more units than pages); empty units wrote no partial.
-    const int np = gl - gf + 1;
+    // Balanced mode: units between gf and gl overlap request b unless their
+    // page range is empty (more units than pages); empty units wrote no
+    // partial.  Fixed-split mode: every one of the np ranges holds pages.
     auto unit_lse = [&](int i) {
         const int g = gf + i;
-        const bool has = static_cast<long long>(g) * total / a.plan.units <
-                         static_cast<long long>(g + 1) * total / a.plan.units;
-        return has ? a.ws_lse[static_cast<long long>(g + b) * a.H + h] : -INFINITY;
+        const bool has = S > 0 || static_cast<long long>(g) * total / a.plan.units <
+                                      static_cast<long long>(g + 1) * total / a.plan.units;
+        return has ? a.ws_lse[static_cast<long long>(slot0 + i) * a.H + h] : -INFINITY;
     };
     float m = -INFINITY;
     for (int i = lane; i < np; i += 32) m = fmaxf(m, unit_lse(i));
@@ -94,7 +107,7 @@ __global__ void __launch_bounds__(32 * kMergeWarps, G == 4 ? 6 : 1) lse_merge_ke
     float4 acc[G];
 #pragma unroll
     for (int k = 0; k < G; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float* base = a.ws_o + (static_cast<long long>(gf + b) * a.H + h) * R + col;
+    const float* base = a.ws_o + (static_cast<long long>(slot0) * a.H + h) * R + col;
     const long long step = static_cast<long long>(a.H) * R;
     float wsum = 0.f;
     for (int j0 = 0; j0 < np; j0 += 32) {

@@ -21,10 +21,13 @@
 //   O = alpha O + P V (each warp owns R/8 output columns).
 // fp8-e4m3 tiles are first widened to bf16 in shared memory (exact); k_scale
 // is folded into the logit scale and into the output.
+#include <cuda_fp8.h>
+
+#include <type_traits>
+
 #include "common.cuh"
 #include "plan.cuh"
 #include "args.cuh"
-#include <cuda_fp8.h>
 
 namespace mqa {
 
@@ -103,11 +106,14 @@ struct MlaMmaCfg {
 };
 
 // MULTI: multi-token decode (per-row key limits); the plain-decode kernels
-// are compiled without that code
-template <int D, int R, bool FP8, int TILE, bool MULTI, bool SPARSE>
+// are compiled without that code.  FIXED: fixed-split mode (one unit per
+// request and range), separate instantiations.
+template <int D, int R, bool FP8, int TILE, bool MULTI, bool SPARSE, bool FIXED>
 __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 1)
     mla_decode_mma_kernel(const __grid_constant__ MlaArgs a) {
     using C = MlaMmaCfg<D, R, FP8, TILE, SPARSE>;
+    using PIter = std::conditional_t<FIXED, FixedPieceIter, PieceIter>;
+    using Cursor = TileCursorT<PIter>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned window: the 128-byte swizzle pattern is a function of
     // address bits 7..9.
@@ -175,7 +181,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
                 bool val[kPer];  // position selects a row of a mapped page
             };
             // first lookup: the tile's entries and its request's length
-            auto read_entries = [&](const TileCursor& tc, Look& L) {
+            auto read_entries = [&](const Cursor& tc, Look& L) {
                 L.b = tc.pc.b;
                 L.n = __ldg(a.seq_lens + L.b);
 #pragma unroll
@@ -201,7 +207,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
                                  : 0;
                 }
             };
-            TileCursor cur;
+            Cursor cur;
             cur.init(a.plan, cum, T, unit, C::kTile);
             int stage = 0;
             uint32_t phase = 0;
@@ -264,7 +270,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
                     report(a.status, MQA_ERR_DEVICE_TIMEOUT);
             return;
         }
-        TileCursor cur;
+        Cursor cur;
         cur.init(a.plan, cum, T, unit, C::kTile);
         int stage = 0;
         uint32_t phase = 0;
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
         constexpr int kRowBytes = D * (FP8 ? 1 : 2);
 
         // Block id of box `lane` of the next tile, fetched one tile ahead.
-        auto fetch = [&](const TileCursor& tc, int& blk, bool& val) {
+        auto fetch = [&](const Cursor& tc, int& blk, bool& val) {
             const int tok = tc.t0 + lane * BR;
             val = lane < nbox && tok < tc.tok_end;
             blk = val ? tc.bt[tok / P] : 0;
@@ -371,7 +377,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
         }
     };
 
-    PieceIter it;
+    PIter it;
     it.init(a.plan, cum, T, unit);
     Piece pc;
     int stage = 0;
@@ -647,12 +653,12 @@ struct MlaTile {
     static constexpr int value = MQA_MLA_TILE;
 };
 
-template <int D, int R, bool FP8, bool MULTI, bool SPARSE>
+template <int D, int R, bool FP8, bool MULTI, bool SPARSE, bool FIXED = false>
 static cudaError_t launch_form(const MlaArgs& a, int grid, cudaStream_t stream) {
     constexpr int kTile = MlaTile<D, FP8, SPARSE>::value;
     using C = MlaMmaCfg<D, R, FP8, kTile, SPARSE>;
     const size_t smem = C::smem_bytes(a.plan.batch);
-    auto kern = mla_decode_mma_kernel<D, R, FP8, kTile, MULTI, SPARSE>;
+    auto kern = mla_decode_mma_kernel<D, R, FP8, kTile, MULTI, SPARSE, FIXED>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -665,6 +671,7 @@ template <int D, int R, bool FP8>
 static cudaError_t launch_mla_mma(const MlaArgs& a, int grid, cudaStream_t stream) {
     if (a.indices) return launch_form<D, R, FP8, false, true>(a, grid, stream);
     if (a.q_len > 1) return launch_form<D, R, FP8, true, false>(a, grid, stream);
+    if (a.plan.fixed_splits) return launch_form<D, R, FP8, false, false, true>(a, grid, stream);
     return launch_form<D, R, FP8, false, false>(a, grid, stream);
 }
 

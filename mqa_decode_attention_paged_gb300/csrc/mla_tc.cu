@@ -44,6 +44,8 @@
 #include "plan.cuh"
 #include "tc_ptx.cuh"
 
+#include <type_traits>
+
 namespace mqa {
 
 template <int D, int R>
@@ -146,11 +148,14 @@ __device__ __forceinline__ void issue_qk(uint32_t d, uint32_t q_tmem, uint64_t k
 }
 
 // MULTI: multi-token decode (per-row key limits); the plain-decode kernels
-// are compiled without that code
-template <int D, int R, bool FP8, bool MULTI>
+// are compiled without that code.  FIXED: fixed-split mode (one unit per
+// request and range), separate instantiations so that the page-balanced
+// kernels keep their code.
+template <int D, int R, bool FP8, bool MULTI, bool FIXED>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThreads, 1)
     mla_decode_tc_kernel(const __grid_constant__ MlaTcArgs a) {
     using C = MlaTcCfg<D, R>;
+    using PIter = std::conditional_t<FIXED, FixedPieceIter, PieceIter>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* q_s = smem + C::kOffQ;
@@ -246,7 +251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         // without division; other page sizes divide
         const bool pages_fit = BR == P || BR == C::kPair;
         const CUtensorMap* pair_map = &a.kv_pair_map[0];
-        PieceIter it;
+        PIter it;
         it.init(a.plan, cum, T, unit);
         Piece pc;
         int p = 0;
@@ -360,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         if (lane == 0) {
             constexpr uint32_t kIdPV = FP8 ? umma_idesc_f16(128, C::kOCols, 1) : umma_idesc_bf16(128, C::kOCols, 1);
             const uint64_t vdesc0 = umma_desc(smem_u32(stages), C::kKvPanelBytes, 1024);
-            PieceIter vi;
+            PIter vi;
             vi.init(a.plan, cum, T, unit);
             Piece vpc;
             int vp = 0, vc = 0;  // next pair, pieces with tokens begun
@@ -403,7 +408,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             const uint64_t kdesc0 = umma_desc(smem_u32(stages), 16, 1024);
             const uint64_t krope0 = umma_desc_sw64(smem_u32(stages) + C::kFull * C::kKvPanelBytes);
             const uint64_t qrope = umma_desc_sw64(smem_u32(q_s));
-            PieceIter qi;
+            PIter qi;
             qi.init(a.plan, cum, T, unit);
             Piece qpc;
             int qp = 0, qc = 0;
@@ -458,19 +463,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         const uint32_t xfull_remote = map_to_rank(&bars[kXFull + g], peer);
         const uint32_t xfree_remote = map_to_rank(&bars[kXFree + g], peer);
         // warp-uniform bounded waits: TMEM accesses are warp-collective, so a
-        // lane never leaves the loop on its own.  (A warp whose wait expires
-        // does leave it; in the e4m3 kernel the other warps of its group can
-        // then block in the widening's named barrier, which has no time
-        // limit.  Waits expire only on a broken hand-off or a GPU stalled for
+        // lane never leaves the loop on its own.  A warp whose wait expires
+        // does leave it; in the e4m3 kernel it first makes the rest of its
+        // group's widening barrier arrivals (see `widen`), so that no other
+        // warp of the group blocks there, and every other wait is bounded.
+        // Waits expire only on a broken hand-off or a GPU stalled for
         // seconds, never on caller input: bad block ids and lengths are
-        // masked before any wait.)
+        // masked before any wait.
         auto wait_all = [&](uint64_t* bar, uint32_t parity, bool cluster_scope) {
             const bool done = cluster_scope ? mbar_wait_cluster(bar, parity) : mbar_wait(bar, parity);
             return __all_sync(0xffffffffu, done);
         };
         // Q row h of the next piece that holds tokens (after `from`) into
         // TMEM, one 32-bit column per pair of consecutive dims (low half = even)
-        auto stage_q = [&](PieceIter from) {
+        auto stage_q = [&](PIter from) {
             Piece nx;
             int tok0, tok_end;
             while (from.next(cum, nx)) {
@@ -538,6 +544,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         // barrier q % 4: a group starts the step that widens q + 4 only after
         // Q.K^T(q + 1) could run, i.e. after every thread that widened q did,
         // so one barrier's phases never overlap.
+        //
+        // The reads and writes of the group's threads are separated by named
+        // barrier 1 + g, kFull + 1 times per widened pair.  A named barrier
+        // has no time limit, so a warp that gives up (an expired wait) first
+        // makes the group's remaining arrivals there (`drain_widen`): which
+        // pairs a group widens is fixed by the unit's pair count, so every
+        // warp of the group then arrives equally often, and the others go on
+        // to their own bounded waits instead of blocking.
         auto widen = [&](int q) -> bool {
             // ---- widen the pair's e4m3 panels to f16 in place: thread t
             // takes row t / 2, bytes 32 (t % 2) .. + 31 of each full
@@ -591,21 +605,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
         // pairs of the whole unit (for the look-ahead widening)
         int total_pairs = 0;
         {
-            PieceIter ti;
+            PIter ti;
             ti.init(a.plan, cum, T, unit);
             Piece tp;
             int t0_, te_;
             while (ti.next(cum, tp)) total_pairs += piece_tiles(tp, t0_, te_) >> 1;
         }
 
-        PieceIter it;
+        // Group 0 widens pair 0 and the odd pairs, group 1 the even pairs
+        // from 2: the pairs up to pair q (q < total_pairs) that group g widens.
+        auto widened_upto = [&](int q) {
+            return q < 0 ? 0 : g == 0 ? 1 + (q + 1) / 2 : q / 2;
+        };
+        // After an expired wait: the widening barrier arrivals this warp still
+        // owes its group, when it has widened every pair of its up to pair
+        // `done` (computed on the way out, so the fast path keeps no count).
+        auto drain_widen = [&](int done) {
+            const int last = total_pairs - 1;
+            const int owed = (C::kFull + 1) * (widened_upto(last) - widened_upto(done < last ? done : last));
+            for (int i = 0; i < owed; ++i) named_bar_sync(1 + g, C::kGroupThreads);
+        };
+        // set only on the way out after an expired wait (see drain_widen), so
+        // that it occupies no register while the pairs go through
+        int widened;
+
+        PIter it;
         it.init(a.plan, cum, T, unit);
         Piece pc;
         int gp = 0;      // global index of the current piece's first pair
         int kpiece = 0;  // pieces with tokens so far
         bool ok = true;
         if (g == 0) stage_q(it);
-        if (FP8 && g == 0 && total_pairs > 0 && !widen(0)) ok = false;
+        if (FP8 && g == 0 && total_pairs > 0 && !widen(0)) {
+            ok = false;
+            widened = -1;
+        }
+        // test hook: softmax warp give_up % 16 of unit give_up / 16 stops here
+        // as if a wait had expired; the rest of its group goes on
+        if (ok && a.give_up >= 0 && unit == (a.give_up >> 4) && warp == (a.give_up & 15)) {
+            ok = false;
+            widened = 0;  // pair 0, if any, was widened (group 0) or is not the group's (group 1)
+        }
         while (ok && it.next(cum, pc)) {
             int tok0, tok_end;
             const int nt = piece_tiles(pc, tok0, tok_end);
@@ -624,12 +664,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 const int p = gp + j, pb = p & 1;
                 if (FP8 && p + 1 < total_pairs && !widen(p + 1)) {
                     ok = false;
+                    widened = p;  // pair p + 1 was not widened
                     break;
                 }
                 // ---- logits of the pair: own partial from TMEM
                 float s[C::kPair];
                 if (!wait_all(&bars[kSFull + pb], (p >> 1) & 1, false)) {
                     ok = false;
+                    widened = p + 1;
                     break;
                 }
                 tc_fence_after();
@@ -650,6 +692,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 if (h == 0) mbar_arrive_expect_tx(&bars[kXFull + g], C::kXBytes);
                 if (p >= 2 && !wait_all(&bars[kXFree + g], ((p >> 1) & 1) ^ 1, true)) {
                     ok = false;
+                    widened = p + 1;
                     break;
                 }
 #pragma unroll
@@ -658,6 +701,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 // valid tokens of the pair (set by the producer before kv_full)
                 if (!wait_all(&bars[kKvFull + p % C::kStages], (p / C::kStages) & 1, false)) {
                     ok = false;
+                    widened = p + 1;
                     break;
                 }
                 const uint64_t vm = mask_s[p % C::kStages];
@@ -672,6 +716,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 }
                 if (!wait_all(&bars[kXFull + g], (p >> 1) & 1, true)) {
                     ok = false;
+                    widened = p + 1;
                     break;
                 }
 #pragma unroll
@@ -710,6 +755,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 if (p >= 1) {
                     if (!wait_all(&bars[kMReady + ((p - 1) & 1)], ((p - 1) >> 1) & 1, false)) {
                         ok = false;
+                        widened = p + 1;
                         break;
                     }
                     m_prev = m_s[((p - 1) & 1) * C::kHeads + h];
@@ -729,6 +775,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                     if ((p >= 2 && !wait_own_pv(p - 2)) ||
                         !wait_all(&bars[kPEmpty + (g ^ 1)], ((p - 1) >> 1) & 1, false)) {
                         ok = false;
+                        widened = p + 1;
                         break;
                     }
                     tc_fence_after();
@@ -748,6 +795,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 // ---- P of the pair into TMEM buffer pb (last read by P.V(p - 2))
                 if (p >= 2 && !wait_own_pv(p - 2)) {
                     ok = false;
+                    widened = p + 1;
                     break;
                 }
                 const float m_use = m_run == -INFINITY ? 0.f : m_run;
@@ -797,6 +845,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 // hand this group's sum over (after the previous epilogue read the slot)
                 if (kpiece >= 1 && !wait_all(&bars[kOFree], (kpiece - 1) & 1, false)) {
                     ok = false;
+                    widened = gp + npairs;
                     break;
                 }
                 lh_s[h] = l_part;
@@ -805,6 +854,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             } else {
                 if (!wait_all(&bars[kLReady], kpiece & 1, false) || !wait_own_pv(plast)) {
                     ok = false;
+                    widened = gp + npairs;
                     break;
                 }
                 const float lo = lh_s[h], mo = mh_s[h];
@@ -852,7 +902,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
             gp += npairs;
             ++kpiece;
         }
-        if (!ok) report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+        if (!ok) {
+            report(a.status, MQA_ERR_DEVICE_TIMEOUT);
+            if constexpr (FP8) drain_widen(widened);
+        }
     }
 
     // teardown: every role is done with TMEM, shared memory and the peer's
@@ -870,7 +923,9 @@ template <int D, int R, bool FP8>
 static cudaError_t launch_mla_tc(const MlaTcArgs& a, int clusters, cudaStream_t stream) {
     using C = MlaTcCfg<D, R>;
     const size_t smem = C::smem_bytes(a.plan.batch);
-    auto kern = a.q_len > 1 ? mla_decode_tc_kernel<D, R, FP8, true> : mla_decode_tc_kernel<D, R, FP8, false>;
+    auto kern = a.q_len > 1            ? mla_decode_tc_kernel<D, R, FP8, true, false>
+                : a.plan.fixed_splits ? mla_decode_tc_kernel<D, R, FP8, false, true>
+                                      : mla_decode_tc_kernel<D, R, FP8, false, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -17,6 +17,15 @@
 //    Along the staircase of overlaps g + b strictly increases, so slots are
 //    unique and lie below units + B - 1 <= B * num_kv_splits when
 //    units <= B * (num_kv_splits - 1) + 1 (the host enforces this).
+//  * fixed-split mode (fixed_splits = S >= 2, its own kernel instantiations
+//    through FixedPieceIter): every request is cut into S page ranges of
+//    L = ceil(pages / S) pages, the split of the Triton MLA backend (one
+//    program per request and split: "Triton と MLA" page, 主要ファイル /
+//    データフロー; tutorial page §12), and unit g takes range g % S of
+//    request g / S, writing its partial to slot g.  A request's reduction
+//    order then depends on nothing but its own length and S: the result is
+//    batch-invariant at any S.  Range 0 of a request that fits one range (or
+//    has no page) writes the final output directly.
 #pragma once
 
 #include "common.cuh"
@@ -29,7 +38,8 @@ struct Plan {
     int max_blocks;
     int units;
     int per_seq;
-    int fixed_len;  // > 0: every request has this length (sparse decode: its index list)
+    int fixed_len;     // > 0: every request has this length (sparse decode: its index list)
+    int fixed_splits;  // >= 2: fixed-split mode with this many ranges per request, else 0
 };
 
 // The length the plan gives request b: fixed_len, or its clamped seq_len.
@@ -162,12 +172,43 @@ struct PieceIter {
     }
 };
 
+// Fixed-split mode's iterator: unit g yields one piece, range g % S of
+// request g / S (possibly without pages), with the interface of PieceIter.
+struct FixedPieceIter {
+    int g, b, j0, j1, whole, done;
+
+    __device__ __forceinline__ void init(const Plan& plan, const int* cum, int, int unit) {
+        const int S = plan.fixed_splits;
+        g = unit;
+        b = unit / S;
+        const int s = unit - b * S;
+        const int np = cum[b + 1] - cum[b];
+        const int L = (np + S - 1) / S;
+        j0 = min(s * L, np);
+        j1 = min(j0 + L, np);
+        whole = (s == 0 && j1 == np) ? 1 : 0;
+        done = 0;
+    }
+
+    __device__ __forceinline__ bool next(const int*, Piece& pc) {
+        if (done) return false;
+        done = 1;
+        pc.b = b;
+        pc.j0 = j0;
+        pc.j1 = j1;
+        pc.whole = whole;
+        pc.slot = g;
+        return true;
+    }
+};
+
 // Producer-side flat walk over the tiles of a unit: `tile` tokens at a time,
 // skipping pieces that hold no token.  After next() returns true, tokens
 // [t0, min(t0 + tile, tok_end)) of request pc.b are the current tile and `bt`
 // points at that request's block-table row.
-struct TileCursor {
-    PieceIter it;
+template <class Iter>
+struct TileCursorT {
+    Iter it;
     Piece pc;
     int t0, tok_end, tile;
     const int32_t* bt;
@@ -193,5 +234,6 @@ struct TileCursor {
         return true;
     }
 };
+using TileCursor = TileCursorT<PieceIter>;
 
 }  // namespace mqa

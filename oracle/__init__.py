@@ -87,6 +87,7 @@ def _load():
         lib.oracle_gqa_paged_decode_pth.argtypes = [P, P, I, P, P, D, P, P, I, I, I, I, I, I, I]
         lib.oracle_int8_values.argtypes = [P, P, I64]
         lib.oracle_lse_merge.argtypes = [P, P, P, P, I, I, I, I]
+        lib.oracle_lse_share.argtypes = [P, P, I, P, P, I, I, I, I]
         lib.oracle_int4_values.argtypes = [P, P, I64]
         _lib = lib
         return lib
@@ -298,6 +299,26 @@ def _gqa_pth(q, kv, kv_dtype, block_table, seq_lens, scale):
     if rc != 0:
         raise ValueError("oracle: bad block table or head counts")
     return out, lse
+
+
+def lse_share(out_g, lses, g):
+    """Shard g's share of the merged output for an exchange that all-gathers
+    the lse and sums the outputs: out_g [B, H, R] (shard g's normalised
+    output), lses [G, B, H]; returns (share [B, H, R], merged lse [B, H]) with
+    share = e^{lse_g - lse} out_g.  The shares of all shards sum to
+    ``lse_merge``'s output."""
+    o = np.ascontiguousarray(out_g, dtype=np.float64)
+    l = np.ascontiguousarray(lses, dtype=np.float64)
+    G, B, H = l.shape
+    if o.ndim != 3 or o.shape[:2] != (B, H):
+        raise ValueError("out_g must be [B, H, R] with lses [G, B, H]")
+    if not 0 <= g < G:
+        raise ValueError("g must be a shard index")
+    R = o.shape[2]
+    share = np.zeros((B, H, R), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    _load().oracle_lse_share(_ptr(o), _ptr(l), int(g), _ptr(share), _ptr(lse), G, B, H, R)
+    return share, lse
 
 
 def lse_merge(outs, lses):

@@ -58,6 +58,13 @@
  *   normalised partials) and the "Triton と MLA" page, 設計動機 (lse is
  *   returned so that DCP shards can be merged by cp_lse_ag_out_rs).
  *
+ *   The same merge taken apart for an exchange that all-gathers the lse and
+ *   sums the outputs across ranks: shard g's share of the merged output is
+ *   its weight times its output, e^{lse_g - lse} O_g with lse the merged lse,
+ *   and the shares of all shards add up to O.  Source: the merge above; the
+ *   name cp_lse_ag_out_rs (lse all-gather, output reduce-scatter) on the
+ *   "Triton と MLA" page, 設計動機.
+ *
  *   GQA paged decode over a [num_blocks, 2, page, num_kv_heads, head_size]
  *   cache.  Source: "AttentionBackend" page (vllm-arch-zh, fr/attention/backend),
  *   section "Motivation de conception" (FlashAttention cache layout).
@@ -691,5 +698,31 @@ void oracle_lse_merge(const double* outs, const double* lses, double* out, doubl
         }
         for (int r = 0; r < R; ++r) o[r] /= wsum;
         lse[row] = m + log(wsum);
+    }
+}
+
+/* Shard g's share of the merged output: lses [G, B, H] natural-log shard
+ * LSEs (-inf for a shard with no token), out_g [B, H, R] shard g's normalised
+ * output; share [B, H, R] = e^{lse_g - lse} out_g (0 when lse_g = -inf, and
+ * out_g is then not read) with lse = ln sum_g' e^{lse_g'} (-inf when every
+ * shard is empty), written to lse [B, H]. */
+void oracle_lse_share(const double* out_g, const double* lses, int g, double* share, double* lse, int G, int B,
+                      int H, int R) {
+    int64_t rows = (int64_t)B * H;
+    for (int64_t row = 0; row < rows; ++row) {
+        double m = -INFINITY;
+        for (int k = 0; k < G; ++k)
+            if (lses[(int64_t)k * rows + row] > m) m = lses[(int64_t)k * rows + row];
+        double total = -INFINITY;
+        if (m != -INFINITY) {
+            double wsum = 0.0;
+            for (int k = 0; k < G; ++k)
+                if (lses[(int64_t)k * rows + row] != -INFINITY) wsum += exp(lses[(int64_t)k * rows + row] - m);
+            total = m + log(wsum);
+        }
+        lse[row] = total;
+        double lg = lses[(int64_t)g * rows + row];
+        double w = lg == -INFINITY ? 0.0 : exp(lg - total);
+        for (int r = 0; r < R; ++r) share[row * R + r] = w == 0.0 ? 0.0 : w * out_g[row * R + r];
     }
 }

@@ -33,11 +33,13 @@ def test_header_symbols_are_exported():
     # the test hooks sit in their own header, not in the product interface
     product = open(os.path.join(ROOT, "include", "mqa_decode.h")).read()
     assert "mqa_test_" not in product
-    assert {"mqa_test_gqa_withheld_arrive", "mqa_test_mla_withheld_arrive"} <= set(names)
-    assert {"mla_decode", "mla_decode_multi", "mla_decode_sparse", "gqa_paged_decode", "mqa_lse_merge",
+    assert {"mqa_test_gqa_withheld_arrive", "mqa_test_mla_withheld_arrive",
+            "mqa_test_mla_warp_gives_up"} <= set(names)
+    assert {"mla_decode", "mla_decode_fixed_splits", "mla_decode_multi", "mla_decode_sparse", "gqa_paged_decode", "mqa_lse_merge",
             "mqa_num_kv_splits", "mla_decode_workspace_bytes",
             "gqa_paged_decode_workspace_bytes", "mqa_status_string", "mqa_abi_version",
-            "mqa_device_sm_count"} <= set(names)
+            "mqa_device_sm_count", "mqa_dcp_shard_max_blocks", "mqa_dcp_shard", "mqa_dcp_locate",
+            "mqa_dcp_scale_shard"} <= set(names)
     lib = ctypes.CDLL(mqa.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
@@ -250,3 +252,41 @@ def test_mla_withheld_arrive_hook_validation(monkeypatch):
     assert fn(*(args[:8] + [0] + args[9:]), 0) == mqa.ERR_INVALID_ARG   # the usual validation runs first
     assert fn(*(args[:10] + [320] + args[11:]), 0) == mqa.ERR_UNSUPPORTED
     assert fn(*(args[:16] + [2] + args[17:]), 0) == mqa.ERR_WORKSPACE_TOO_SMALL
+
+
+def test_dcp_scale_shard_validation():
+    # argument errors come back before anything is enqueued (no GPU needed)
+    f = mqa.lib.mqa_dcp_scale_shard
+    P = lambda v: None if v is None else ctypes.c_void_p(v)  # noqa: E731
+
+    def call(so=FAKE, gl=FAKE, dst=FAKE, lse=None, G=2, r=0, B=3, H=16, D=512, f32=1):
+        return f(P(so), P(gl), P(dst), P(lse), G, r, B, H, D, f32, None)
+
+    assert call(so=None) == mqa.ERR_INVALID_ARG
+    assert call(dst=None) == mqa.ERR_INVALID_ARG
+    assert call(so=FAKE + 8) == mqa.ERR_INVALID_ARG        # unaligned
+    assert call(lse=FAKE + 4) == mqa.ERR_INVALID_ARG
+    assert call(r=2) == mqa.ERR_INVALID_ARG
+    assert call(r=-1) == mqa.ERR_INVALID_ARG
+    assert call(G=3) == mqa.ERR_INVALID_ARG                # 16 heads over 3 ranks
+    assert call(G=0) == mqa.ERR_INVALID_ARG
+    assert call(D=12) == mqa.ERR_INVALID_ARG
+    assert call(D=8192) == mqa.ERR_INVALID_ARG
+    assert call(B=0) == mqa.ERR_INVALID_ARG
+
+
+def test_mla_warp_gives_up_hook_validation(monkeypatch):
+    fn = mqa.lib.mqa_test_mla_warp_gives_up
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    fn.restype = I
+    fn.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, P, SZ, P, P, I, I]
+    f = ctypes.c_void_p(FAKE)
+    args = [f, f, f, f, 0.07, 1.0, f, None, 2, 128, 576, 512, 10, 64, 8, 1, None, 0, None, None]
+    monkeypatch.delenv("MQA_ENABLE_TEST_HOOKS", raising=False)
+    assert fn(*args, 0, 3) == mqa.ERR_UNSUPPORTED          # gated
+    monkeypatch.setenv("MQA_ENABLE_TEST_HOOKS", "1")
+    assert fn(*args, -1, 3) == mqa.ERR_INVALID_ARG
+    assert fn(*args, 0, 1) == mqa.ERR_INVALID_ARG          # not a softmax warp
+    assert fn(*args, 0, 10) == mqa.ERR_INVALID_ARG
+    assert fn(*(args[:9] + [32] + args[10:]), 0, 3) == mqa.ERR_INVALID_ARG   # no tensor-core kernel
+    assert fn(*(args[:8] + [0] + args[9:]), 0, 3) == mqa.ERR_INVALID_ARG    # the usual validation runs

@@ -86,3 +86,37 @@ def test_mla_withheld_tile_times_out_and_reports(monkeypatch, H, kv_dtype):
     o2, l2 = run_gpu(case, 3)
     ref_out, ref_lse = run_oracle(case)
     assert_close(o2, l2, ref_out, ref_lse, fp8=kv_dtype != "bf16", what="after the timeout")
+
+
+@pytest.mark.parametrize("warp", [2, 3, 7])
+def test_mla_one_softmax_warp_gives_up(monkeypatch, warp):
+    # e4m3 cache, 128 heads: one softmax warp of unit 0 stops before its first
+    # pair while the other warps of its group go on into the in-place
+    # widening, whose named barriers wait for all four warps.  The warp that
+    # gives up makes its remaining barrier arrivals, so nothing blocks there;
+    # the waits that miss its arrivals run out instead.
+    monkeypatch.setenv("MQA_ENABLE_TEST_HOOKS", "1")
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    fn = mqa.lib.mqa_test_mla_warp_gives_up
+    fn.restype = I
+    fn.argtypes = [P, P, P, P, F, F, P, P, I, I, I, I, I, I, I, I, P, SZ, P, P, I, I]
+    case = synth.make_mla_case([700, 300], H=128, page=64, kv_dtype="fp8_e4m3", k_scale=0.05, seed=43)
+    q, kv, bt, sl = to_device(case)
+    B, H, D = q.shape
+    R = case.kv_lora_rank
+    out = torch.full((B, H, R), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H), float("nan"), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    rc = fn(ptr(q), ptr(kv), ptr(bt), ptr(sl), case.scale, case.k_scale, ptr(out), ptr(lse), B, H, D, R,
+            case.num_blocks, case.page, case.max_blocks, 1, None, 0, ptr(status), stream, 0, warp)
+    assert rc == mqa.OK
+    torch.cuda.synchronize()  # returns: no barrier is left waiting for the warp that gave up
+    assert int(status.item()) == mqa.ERR_DEVICE_TIMEOUT
+    ref_out, ref_lse = run_oracle(subset(case, [1]))
+    assert_close(out.double().cpu().numpy()[[1]], lse.double().cpu().numpy()[[1]], ref_out, ref_lse, fp8=True,
+                 what="other request")
+    o2, l2 = run_gpu(case, 3)
+    ref_out, ref_lse = run_oracle(case)
+    assert_close(o2, l2, ref_out, ref_lse, fp8=True, what="after the timeout")

@@ -79,3 +79,52 @@ def test_closed_forms():
     # nothing anywhere: zeros and -inf
     out, lse = oracle.lse_merge(o, np.full((3, 2, 4), -np.inf))
     assert (out == 0).all() and np.isneginf(lse).all()
+
+
+@pytest.mark.parametrize("G", [2, 3, 5])
+def test_shares_of_shards_sum_to_whole_sequence(G):
+    # lse all-gather / output reduce-scatter: each shard's share
+    # e^{lse_g - lse} O_g, summed over the shards, is the decode of the whole
+    # sequence (an independent pin: the whole decode never merges anything)
+    case = synth.make_mla_case([37, 100, 16, 1, 0, 250], H=4, D=576, page=16, seed=55)
+    out, lse = _decode(case)
+    parts = [_decode(sh) for sh in synth.shard_case(case, G)]
+    lses = np.stack([p[1] for p in parts])
+    total = np.zeros_like(out)
+    for g, p in enumerate(parts):
+        share, l = oracle.lse_share(p[0], lses, g)
+        total += share
+        fin = np.isfinite(lse)
+        assert np.array_equal(np.isfinite(l), fin)
+        assert np.abs(l[fin] - lse[fin]).max() <= 1e-12
+    assert np.abs(total - out).max() <= 1e-12 * max(1.0, np.abs(out).max())
+
+
+def test_share_closed_forms():
+    rng = np.random.default_rng(6)
+    o = rng.standard_normal((3, 2, 4, 8))
+    lses = rng.standard_normal((3, 2, 4))
+    # the shares add up to the merge, shard by shard in any order
+    merged, mlse = oracle.lse_merge(o, lses)
+    shares = [oracle.lse_share(o[g], lses, g) for g in range(3)]
+    assert np.abs(sum(s[0] for s in shares) - merged).max() < 1e-14
+    assert all(np.abs(s[1] - mlse).max() < 1e-15 for s in shares)
+    # one shard: its own output, its own lse
+    s, l = oracle.lse_share(o[0], lses[:1], 0)
+    assert np.abs(s - o[0]).max() < 1e-15 and np.abs(l - lses[0]).max() < 1e-15
+    # two shards of equal lse: half each, lse + ln 2
+    eq = np.full((2, 2, 4), -1.5)
+    s, l = oracle.lse_share(o[1], eq, 1)
+    assert np.abs(s - 0.5 * o[1]).max() < 1e-15 and np.abs(l - (-1.5 + math.log(2))).max() < 1e-15
+    # weights e^{lse_g - lse}: shard 0 of lse 0 against shard 1 of lse ln 3 -> 1/4
+    l2 = np.stack([np.zeros((2, 4)), np.full((2, 4), math.log(3.0))])
+    s, _ = oracle.lse_share(o[0], l2, 0)
+    assert np.abs(s - 0.25 * o[0]).max() < 1e-15
+    # an empty shard: share 0 whatever its output holds; the others keep theirs
+    l3 = lses.copy()
+    l3[2] = -np.inf
+    s, _ = oracle.lse_share(np.full((2, 4, 8), np.nan), l3, 2)
+    assert (s == 0).all()
+    # nothing anywhere: zeros and -inf
+    s, l = oracle.lse_share(o[0], np.full((3, 2, 4), -np.inf), 0)
+    assert (s == 0).all() and np.isneginf(l).all()
