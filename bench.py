@@ -58,21 +58,26 @@ MMA_FILES = ("mla_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
 TC_FILES = ("mla_tc.cu", "tc_ptx.cuh", "common.cuh", "plan.cuh", "args.cuh")
 Q8_FILES = ("gqa_q8.cu", "gqa_q8.cuh", "common.cuh", "plan.cuh", "args.cuh")
 MERGE_FILES = ("shard_merge.cu", "shard_merge.cuh", "common.cuh")
+GQA_FILES = ("gqa_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
 NCU_TRAFFIC = {
-    "mla_v2lite": {"files": MMA_FILES, "src_sha": "469c1abab8d15a69", "splits": 16, "bytes": 329795584 + 3687424,
-                   "kernel": "mla_decode_mma_kernel<576,512,0,64>"},
-    "mla_longctx": {"files": TC_FILES, "src_sha": "db7d88cc3b68ce52", "splits": 256, "bytes": 485207808 + 4084992,
-                    "kernel": "mla_decode_tc_kernel<576,512,0>"},
-    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "db7d88cc3b68ce52", "splits": 64, "bytes": 1423465728 + 25308416,
-                   "kernel": "mla_decode_tc_kernel<576,512,1>"},
-    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "8566ab172970c1e5", "splits": 32, "bytes": 1535300864 + 5419264,
+    "mla_v2lite": {"files": MMA_FILES, "src_sha": "768b00c4d516d186", "splits": 16, "bytes": 329795840 + 3204864,
+                   "kernel": "mla_decode_mma_kernel<576,512,0,64,0,0,0>"},
+    "mla_longctx": {"files": TC_FILES, "src_sha": "9061a7098f0c67e5", "splits": 256, "bytes": 485164032 + 4065792,
+                    "kernel": "mla_decode_tc_kernel<576,512,0,0,0>"},
+    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "9061a7098f0c67e5", "splits": 64, "bytes": 1423378432 + 25886976,
+                   "kernel": "mla_decode_tc_kernel<576,512,1,0,0>"},
+    "mla_mtp": {"files": TC_FILES, "src_sha": "9061a7098f0c67e5", "splits": 16, "bytes": 362980352 + 7184384,
+                "kernel": "mla_decode_tc_kernel<576,512,0,1,0>"},
+    "gqa": {"files": GQA_FILES, "src_sha": "b0fc4fa9309adfaf", "splits": 32, "bytes": 3241168896 + 4567808,
+            "kernel": "gqa_decode_mma_kernel<128>"},
+    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "10c7188635637814", "splits": 32, "bytes": 1535302656 + 5671680,
                     "kernel": "gqa_decode_q8_kernel<128,2,1>"},
-    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "8566ab172970c1e5", "splits": 32, "bytes": 1689826560 + 5800192,
+    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "10c7188635637814", "splits": 32, "bytes": 1689982720 + 5605120,
                      "kernel": "gqa_decode_q8_kernel<128,3,1>"},
     "dcp_merge_v3": {"files": MERGE_FILES, "src_sha": "8c157f962d4da4f4", "bytes": 126340608 + 7121920,
                      "kernel": "shard_merge_kernel"},
-    "mla_sparse": {"files": MMA_FILES, "src_sha": "469c1abab8d15a69", "splits": 4, "bytes": 152899072 + 3118592,
-                   "kernel": "mla_decode_mma_kernel<576,512,0,64,0,1>"},
+    "mla_sparse": {"files": MMA_FILES, "src_sha": "768b00c4d516d186", "splits": 4, "bytes": 152899328 + 3346688,
+                   "kernel": "mla_decode_mma_kernel<576,512,0,64,0,1,0>"},
 }
 
 
@@ -125,8 +130,19 @@ def workload_stats(case, splits):
                 q_bytes=B * H * D * 2, out_bytes=B * H * out_w * 2, lse_bytes=B * H * 4)
 
 
+def load_workload(synth, args):
+    """The named workload, with its batch overridden by --batch (a smaller
+    case of the same shape, e.g. for a profiler capture)."""
+    if not getattr(args, "batch", 0):
+        return synth.workload(args.workload)
+    if "B" not in synth.WORKLOADS[args.workload]:
+        raise SystemExit(f"--batch: workload {args.workload} has explicit sequence lengths")
+    return synth.workload(args.workload, B=args.batch)
+
+
 def workload_config(case, name, splits):
-    spec = __import__("mqa_decode_attention_paged_gb300.synth", fromlist=["WORKLOADS"]).WORKLOADS[name]
+    import synth
+    spec = synth.WORKLOADS[name]
     cfg = {"workload": name, "kind": case.kind, "batch": case.batch, "num_heads": case.num_heads,
            "head_size": case.head_size, "page_size": case.page, "kv_dtype": case.kv_dtype,
            "seq_lens": spec["seq_lens"] if not isinstance(spec["seq_lens"], tuple) else list(spec["seq_lens"]),
@@ -303,7 +319,7 @@ class ClockSampler:
 def time_oracle(case, budget_s=12.0, min_reps=1):
     """Time the fp64 oracle on bounded request samples; returns (GB/s, cores, sample text)."""
     import oracle
-    from mqa_decode_attention_paged_gb300 import synth
+    import synth
     cores = oracle.max_threads()
     rng = np.random.default_rng(0)
     order = rng.permutation(case.batch)
@@ -379,8 +395,8 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    from mqa_decode_attention_paged_gb300 import synth
-    case = synth.workload(args.workload)
+    import synth
+    case = load_workload(synth, args)
     # The oracle computes the direct definition whatever the split count; the
     # line names the split count the GPU arm uses on this machine (the heuristic
     # with the device's SM count, 152 on a GB300 when no device is visible)
@@ -430,7 +446,7 @@ MERGE_WORKLOADS = {"dcp_merge_v3": dict(G=8, B=128, H=128, R=512, seed=1010)}
 def merge_inputs(spec):
     rng = np.random.default_rng(spec["seed"])
     G, rows, R = spec["G"], spec["B"] * spec["H"], spec["R"]
-    from mqa_decode_attention_paged_gb300 import synth
+    import synth
     outs = synth.to_bf16_bits(rng.standard_normal((G, rows, R), dtype=np.float32))
     lses = (10.0 + 3.0 * rng.standard_normal((G, rows))).astype(np.float32)
     lses[rng.random((G, rows)) < 1.0 / 16] = -np.inf
@@ -608,9 +624,9 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
 
     from mqa_decode_attention_paged_gb300 import _binding as mqa
-    from mqa_decode_attention_paged_gb300 import synth
+    import synth
 
-    case = synth.workload(args.workload)
+    case = load_workload(synth, args)
     if args.split_mode == "fixed" and (case.kind != "mla" or case.meta.get("indices") is not None
                                        or case.meta.get("q_len", 1) > 1):
         raise SystemExit("--split-mode fixed serves the dense single-token MLA workloads")
@@ -742,7 +758,7 @@ def run_ours(args):
     tr = NCU_TRAFFIC.get(args.workload)
     traffic_kernel = None
     if (tr and tr.get("src_sha") == kernel_sources_sha(tr["files"]) and tr.get("splits") == splits
-            and args.split_mode == "balanced"):
+            and args.split_mode == "balanced" and not getattr(args, "batch", 0)):
         traffic = tr["bytes"]
         traffic_kernel = tr["kernel"] + " (stage 1 only)"
     if bound == "hbm":
@@ -804,6 +820,8 @@ def main():
     ap.add_argument("--split-mode", default="balanced", choices=["balanced", "fixed"],
                     help="balanced: num_kv_splits is a partial budget over page-balanced units (mla_decode); "
                          "fixed: one unit per request and split, equal page ranges (mla_decode_fixed_splits)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (same shape otherwise; 0 = as defined)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
     args = ap.parse_args()

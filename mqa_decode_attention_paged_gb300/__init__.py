@@ -2,9 +2,11 @@
 
 The compute path is the CUDA library ``_lib/libmqa_decode.so`` behind the C ABI
 in ``include/mqa_decode.h``; this package adds a thin ctypes binding
-(:mod:`._binding`), the in-tree build (:mod:`.build`) and seeded synthetic
-workloads (:mod:`.synth`).  Importing the binding fails loudly when the
-library has not been built.
+(:mod:`._binding`), the in-tree build (:mod:`.build`) and the exchange of
+decode context parallelism (:mod:`.dcp`).  Importing the binding fails
+loudly when the library has not been built.  (The seeded synthetic workloads
+of the tests and the benchmark live outside the package, in ``synth.py`` at
+the repository root.)
 """
 from .build import LIB_PATH  # noqa: F401
 

@@ -124,22 +124,26 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     return pack_f16x2(f.x, f.y);
 }
 
-// Two packed int4 codes (the nibbles of byte b, low first) -> their f16 pair:
-// u = x + 8 in [0, 15] placed in the mantissa of 1024 (0x6400), minus 1032.
-__device__ __forceinline__ uint32_t int4_pair(uint32_t t, int b) {
-    // t: the codes with every nibble's sign bit flipped (x + 8)
-    const uint32_t lo = (t >> (8 * b)) & 0xfu, hi = (t >> (8 * b + 4)) & 0xfu;
-    return h2_bits(__hsub2(bits_h2(lo | (hi << 16) | 0x64006400u), bits_h2(0x64086408u)));
+// The eight int4 codes of w (nibble i = element i, two's complement) -> four
+// f16 pairs, elements (0, 4), (1, 5), (2, 6), (3, 7), exact: one mask-and-xor
+// per pair (a single LOP3) puts x + 8 = nibble ^ 8 of elements i and i + 4
+// into the mantissas of two f16 1024s (0x6400), then 1032 is subtracted.
+// The callers absorb the element order (the K operand's reduction order, V's
+// tile columns).
+__device__ __forceinline__ uint4 int4x8_to_f16_pairs(uint32_t w) {
+    const __half2 k = bits_h2(0x64086408u);
+    auto pair = [&](uint32_t x) { return h2_bits(__hsub2(bits_h2((x & 0x000f000fu) ^ 0x64086408u), k)); };
+    return make_uint4(pair(w), pair(w >> 4), pair(w >> 8), pair(w >> 12));
 }
 
-// Four codes (bytes of w, lowest first; for int4 the four nibbles of its low
-// 16 bits) -> four f16 values (exact).
+// Tile column m (0..7) of an 8-column group of widened int4 V holds element
+// perm(m) of the group: the order int4x8_to_f16_pairs stores.
+__device__ __forceinline__ int int4_col_dim(int m) { return (m >> 1) + 4 * (m & 1); }
+
+// Four 8-bit codes (bytes of w, lowest first) -> four f16 values (exact).
 template <int KIND>
 __device__ __forceinline__ uint2 widen4(uint32_t w) {
-    if constexpr (KIND == kFmtInt4Pth) {
-        const uint32_t t = w ^ 0x8888u;
-        return make_uint2(int4_pair(t, 0), int4_pair(t, 1));
-    } else if constexpr (KIND == kFmtInt8Pth) {
+    if constexpr (KIND == kFmtInt8Pth) {
         // u = x + 128 in [0, 255] placed in the mantissa of 1024 (0x6400):
         // the f16 value 1024 + u is exact, minus 1152 gives x
         const uint32_t u = w ^ 0x80808080u;
@@ -163,7 +167,8 @@ __device__ __forceinline__ void widen_rows(const uint8_t* src, uint8_t* dst, uin
                                            int lane) {
     using C = GqaQ8Cfg<D, KIND>;
     if constexpr (KIND == kFmtInt4Pth) {
-        // a lane takes 4 bytes = 8 elements of a row
+        // a lane takes 4 bytes = 8 elements of a row; the tile's 8 columns
+        // from 8 ch hold them in the order of int4x8_to_f16_pairs
         constexpr int kLanesPerRow = D / 8;
         constexpr int kRowsPer = 32 / kLanesPerRow;
         const int sub = lane / kLanesPerRow, ch = lane % kLanesPerRow;
@@ -172,9 +177,7 @@ __device__ __forceinline__ void widen_rows(const uint8_t* src, uint8_t* dst, uin
             const int r = r0 + sub;
             const bool v = (vmask >> r) & 1ull;
             const uint32_t w = v ? *reinterpret_cast<const uint32_t*>(src + r * rbytes + 4 * ch) : 0u;  // code 0
-            const uint32_t t = w ^ 0x88888888u;
-            *reinterpret_cast<uint4*>(dst + r * C::kWStride + 16 * ch) =
-                make_uint4(int4_pair(t, 0), int4_pair(t, 1), int4_pair(t, 2), int4_pair(t, 3));
+            *reinterpret_cast<uint4*>(dst + r * C::kWStride + 16 * ch) = int4x8_to_f16_pairs(w);
         }
     } else {
         constexpr int kLanesPerRow = D / 4;
@@ -336,19 +339,34 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), q8_
         const int hq0 = gk * grp;
 
         // Q^T operand, f16, in the permuted reduction order (step ks, lane c:
-        // head dims 16 ks + 4c .. + 3): query head hb * 8 + g
+        // head dims 16 ks + 4c .. + 3; int4: steps 2j and 2j + 1 take dims
+        // 32 j + 8c + (0, 4, 1, 5) and + (2, 6, 3, 7), the order in which
+        // int4x8_to_f16_pairs widens one 4-byte word of K codes): query head
+        // hb * 8 + g
         uint32_t qb[NHB][C::kKSteps][2];
         {
             const __nv_bfloat16* qrow = a.q + (static_cast<long long>(pc.b) * a.Hq + hq0) * D;
 #pragma unroll
             for (int hb = 0; hb < NHB; ++hb) {
                 const int h = hb * 8 + g;
+                if constexpr (KIND == kFmtInt4Pth) {
 #pragma unroll
-                for (int ks = 0; ks < C::kKSteps; ++ks) {
-                    const uint2 v = h < grp ? *reinterpret_cast<const uint2*>(qrow + h * D + ks * 16 + 4 * c)
-                                            : make_uint2(0u, 0u);
-                    qb[hb][ks][0] = bf16x2_to_f16x2(v.x);
-                    qb[hb][ks][1] = bf16x2_to_f16x2(v.y);
+                    for (int j = 0; j < C::kKSteps / 2; ++j) {
+                        const uint4 v = h < grp ? *reinterpret_cast<const uint4*>(qrow + h * D + j * 32 + 8 * c)
+                                                : make_uint4(0u, 0u, 0u, 0u);
+                        qb[hb][2 * j][0] = bf16x2_to_f16x2(__byte_perm(v.x, v.z, 0x5410));      // dims 0, 4
+                        qb[hb][2 * j][1] = bf16x2_to_f16x2(__byte_perm(v.x, v.z, 0x7632));      // 1, 5
+                        qb[hb][2 * j + 1][0] = bf16x2_to_f16x2(__byte_perm(v.y, v.w, 0x5410));  // 2, 6
+                        qb[hb][2 * j + 1][1] = bf16x2_to_f16x2(__byte_perm(v.y, v.w, 0x7632));  // 3, 7
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < C::kKSteps; ++ks) {
+                        const uint2 v = h < grp ? *reinterpret_cast<const uint2*>(qrow + h * D + ks * 16 + 4 * c)
+                                                : make_uint2(0u, 0u);
+                        qb[hb][ks][0] = bf16x2_to_f16x2(v.x);
+                        qb[hb][ks][1] = bf16x2_to_f16x2(v.y);
+                    }
                 }
             }
         }
@@ -401,12 +419,18 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), q8_
             for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) st[hb][e][0] = st[hb][e][1] = st[hb][e][2] = st[hb][e][3] = 0.f;
+            uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;  // int4: one word of codes per two steps
 #pragma unroll
             for (int ks = 0; ks < C::kKSteps; ++ks) {
                 uint2 k0, k1;
-                if constexpr (KIND == kFmtInt4Pth) {  // 4 elements = 2 bytes
-                    k0 = widen4<KIND>(*reinterpret_cast<const uint16_t*>(kb + g * rstride + ks * 8 + 2 * c));
-                    k1 = widen4<KIND>(*reinterpret_cast<const uint16_t*>(kb + (g + 8) * rstride + ks * 8 + 2 * c));
+                if constexpr (KIND == kFmtInt4Pth) {  // 8 elements = 4 bytes per two steps
+                    if ((ks & 1) == 0) {
+                        w0 = int4x8_to_f16_pairs(*reinterpret_cast<const uint32_t*>(kb + g * rstride + ks * 8 + 4 * c));
+                        w1 = int4x8_to_f16_pairs(
+                            *reinterpret_cast<const uint32_t*>(kb + (g + 8) * rstride + ks * 8 + 4 * c));
+                    }
+                    k0 = (ks & 1) ? make_uint2(w0.z, w0.w) : make_uint2(w0.x, w0.y);
+                    k1 = (ks & 1) ? make_uint2(w1.z, w1.w) : make_uint2(w1.x, w1.y);
                 } else {
                     k0 = widen4<KIND>(*reinterpret_cast<const uint32_t*>(kb + g * rstride + ks * 16 + 4 * c));
                     k1 = widen4<KIND>(*reinterpret_cast<const uint32_t*>(kb + (g + 8) * rstride + ks * 16 + 4 * c));
@@ -508,7 +532,9 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), q8_
         }
         if (aborted) break;
 
-        // epilogue: head hb * 8 + 2c + j, head dims 16 mb + g (+ 8)
+        // epilogue: head hb * 8 + 2c + j, head dims 16 mb + dg (+ 8); int4 V
+        // tiles hold their columns in int4x8_to_f16_pairs order
+        const int dg = KIND == kFmtInt4Pth ? int4_col_dim(g) : g;
         const float osc = (C::kPth && e_run != -1000000) ? ldexpf(out_scale, e_run) : out_scale;
 #pragma unroll
         for (int hb = 0; hb < NHB; ++hb) {
@@ -538,15 +564,15 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), q8_
                     __nv_bfloat16* orow = a.out + (static_cast<long long>(pc.b) * a.Hq + hq0 + h) * D;
 #pragma unroll
                     for (int mb = 0; mb < C::kKSteps; ++mb) {
-                        orow[mb * 16 + g] = __float2bfloat16_rn(o[hb][mb][j] * inv[j]);
-                        orow[mb * 16 + g + 8] = __float2bfloat16_rn(o[hb][mb][2 + j] * inv[j]);
+                        orow[mb * 16 + dg] = __float2bfloat16_rn(o[hb][mb][j] * inv[j]);
+                        orow[mb * 16 + dg + 8] = __float2bfloat16_rn(o[hb][mb][2 + j] * inv[j]);
                     }
                 } else {
                     float* wrow = a.ws_o + (static_cast<long long>(pc.slot) * a.Hq + hq0 + h) * D;
 #pragma unroll
                     for (int mb = 0; mb < C::kKSteps; ++mb) {
-                        wrow[mb * 16 + g] = o[hb][mb][j] * inv[j];
-                        wrow[mb * 16 + g + 8] = o[hb][mb][2 + j] * inv[j];
+                        wrow[mb * 16 + dg] = o[hb][mb][j] * inv[j];
+                        wrow[mb * 16 + dg + 8] = o[hb][mb][2 + j] * inv[j];
                     }
                 }
             }

@@ -11,7 +11,7 @@ import numpy as np
 import torch
 
 import oracle
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 OUT_ABS = 1e-2
 OUT_REL_BF16 = 2e-2

@@ -103,7 +103,7 @@ def test_algorithmic_bytes_and_flops_per_workload():
     # plus q, out and lse, in each cache format; FLOPs 2 H tokens (D + R) for
     # MLA and 4 Hq tokens D for GQA.
     import numpy as np
-    from mqa_decode_attention_paged_gb300 import synth
+    import synth
     mla = synth.make_mla_case([37, 100], H=16, D=576, page=16, seed=1)
     st = bench.workload_stats(mla, 1)
     assert st["tokens"] == 137

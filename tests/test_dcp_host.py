@@ -36,7 +36,7 @@ def _free_port():
 
 
 def _case():
-    from mqa_decode_attention_paged_gb300 import synth
+    import synth
     return synth.make_mla_case([37, 100, 0, 300, 16], H=6, D=576, page=16, seed=71)
 
 
@@ -47,7 +47,8 @@ def _rank_main(rank, world, port, out_dir, layout):
     try:
         import oracle
         from mqa_decode_attention_paged_gb300 import _binding as mqa
-        from mqa_decode_attention_paged_gb300 import dcp, synth
+        from mqa_decode_attention_paged_gb300 import dcp
+        import synth
         case = _case()
         table, lens = mqa.dcp_shard(case.block_table, case.seq_lens, case.page, world, rank, layout)
         shard = synth.replace(case, block_table=table, seq_lens=lens)

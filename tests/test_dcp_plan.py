@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 
 from mqa_decode_attention_paged_gb300 import _binding as mqa
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 LAYOUTS = ["round_robin", "contiguous"]
 

@@ -18,7 +18,7 @@ import torch
 
 import oracle
 from mqa_decode_attention_paged_gb300 import _binding as mqa
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 from helpers import assert_close, run_gpu, run_oracle
 

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from mqa_decode_attention_paged_gb300 import _binding as mqa
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 from helpers import assert_close, run_gpu, run_oracle, subset, to_device
 

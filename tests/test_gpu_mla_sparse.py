@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 from helpers import assert_close, subset, to_device
 

@@ -12,7 +12,7 @@ run to run as well."""
 import numpy as np
 import pytest
 
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 from helpers import assert_close, run_gpu, run_oracle, subset, to_device
 

@@ -15,7 +15,7 @@ import numpy as np
 import pytest
 import torch
 
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 from helpers import assert_close, run_gpu, run_oracle
 

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 from helpers import assert_close, run_gpu, run_oracle, subset
 

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 
 def _dense_multi(case, q_len):

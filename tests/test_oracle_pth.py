@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 PTH = ["fp8_e4m3_pth", "int8_pth", "int4_pth"]
 

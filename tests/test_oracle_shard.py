@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import oracle
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 
 def _decode(case):

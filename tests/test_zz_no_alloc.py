@@ -16,7 +16,7 @@ import pytest
 import torch
 
 from mqa_decode_attention_paged_gb300 import _binding as mqa
-from mqa_decode_attention_paged_gb300 import synth
+import synth
 
 from helpers import OUT_ABS, OUT_REL_BF16, OUT_REL_FP8, LSE_ABS, to_device
 
