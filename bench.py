@@ -70,10 +70,12 @@ NCU_TRAFFIC = {
                 "kernel": "mla_decode_tc_kernel<576,512,0,1,0>"},
     "gqa": {"files": GQA_FILES, "src_sha": "b0fc4fa9309adfaf", "splits": 32, "bytes": 3241168896 + 4567808,
             "kernel": "gqa_decode_mma_kernel<128>"},
-    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "10c7188635637814", "splits": 32, "bytes": 1535302656 + 5671680,
+    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "de9d3c10083698de", "splits": 32, "bytes": 1535305728 + 5585152,
                     "kernel": "gqa_decode_q8_kernel<128,2,1>"},
-    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "10c7188635637814", "splits": 32, "bytes": 1689982720 + 5605120,
+    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "de9d3c10083698de", "splits": 32, "bytes": 1689827840 + 5622272,
                      "kernel": "gqa_decode_q8_kernel<128,3,1>"},
+    "gqa_int4_pth": {"files": Q8_FILES, "src_sha": "de9d3c10083698de", "splits": 32, "bytes": 843228672 + 5700096,
+                     "kernel": "gqa_decode_q8_kernel<128,4,1>"},
     "dcp_merge_v3": {"files": MERGE_FILES, "src_sha": "8c157f962d4da4f4", "bytes": 126340608 + 7121920,
                      "kernel": "shard_merge_kernel"},
     "mla_sparse": {"files": MMA_FILES, "src_sha": "768b00c4d516d186", "splits": 4, "bytes": 152899328 + 3346688,

@@ -52,10 +52,10 @@ mqa_status mqa_test_mla_withheld_arrive(const void* q, const void* kv_cache, con
 /* An e4m3-cache mla_decode with more than 32 heads (the 2-CTA tensor-core
  * kernel) in which softmax warp `warp` (2..9) of both CTAs of work unit
  * `unit` gives up before its first pair as if one of its waits had expired,
- * while the other warps of its group go on: the group's widening barriers
- * must not block them (the warp that gives up makes its remaining arrivals
- * there), every wait that then misses that warp's arrivals runs out, and the
- * call reports MQA_ERR_DEVICE_TIMEOUT.  Arguments as for mla_decode with
+ * while the other warps of its group go on: nothing may block on the warp
+ * that left (every wait for it is a bounded mbarrier wait), every wait that
+ * then misses that warp's arrivals runs out, and the call reports
+ * MQA_ERR_DEVICE_TIMEOUT.  Arguments as for mla_decode with
  * kv_dtype = MQA_KV_FP8_E4M3; MQA_ERR_INVALID_ARG for unit < 0, a warp
  * outside 2..9 or num_heads <= 32. */
 mqa_status mqa_test_mla_warp_gives_up(const void* q, const void* kv_cache, const int32_t* block_table,

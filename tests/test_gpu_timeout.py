@@ -91,10 +91,9 @@ def test_mla_withheld_tile_times_out_and_reports(monkeypatch, H, kv_dtype):
 @pytest.mark.parametrize("warp", [2, 3, 7])
 def test_mla_one_softmax_warp_gives_up(monkeypatch, warp):
     # e4m3 cache, 128 heads: one softmax warp of unit 0 stops before its first
-    # pair while the other warps of its group go on into the in-place
-    # widening, whose named barriers wait for all four warps.  The warp that
-    # gives up makes its remaining barrier arrivals, so nothing blocks there;
-    # the waits that miss its arrivals run out instead.
+    # pair while the other warps of its group go on.  Nothing in the kernel
+    # may wait for that warp except a bounded mbarrier wait: the waits that
+    # miss its arrivals run out, and the call returns with a timeout.
     monkeypatch.setenv("MQA_ENABLE_TEST_HOOKS", "1")
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     fn = mqa.lib.mqa_test_mla_warp_gives_up
