@@ -32,8 +32,9 @@
 //               continue the running maximum handed over by the other group
 //               (lazy rescaling of O only when it grows by more than 2^8),
 //               write P into TMEM; the group of a piece's last pair writes the
-//               output, and the group that reads a piece's last logits loads
-//               the next piece's Q; with an e4m3 cache, the group owning pair
+//               output, and the next piece's Q is loaded by the group that
+//               reads the piece's last logits (bf16 cache) or by the other
+//               group once those logits are in TMEM (e4m3 cache); with an e4m3 cache, the group owning pair
 //               q - 1 first widens pair q to f16 in place;
 //   warp 10     single-thread P.V issuer: O += P V per pair in pair order
 //               (A = P from TMEM, V read MN-major from the slot).
@@ -483,20 +484,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 if (piece_tiles(nx, tok0, tok_end) == 0) continue;
                 const __nv_bfloat16* qrow = a.q + (static_cast<long long>(nx.b) * a.H + (live_row ? h : 0)) * D;
                 const uint4* src = reinterpret_cast<const uint4*>(qrow + pbase * 64);
-                // 8 columns (16 dims) per TMEM store
                 if constexpr (FP8) {
-                    for (int c = 0; c < 4 * C::kFull; ++c) {
-                        const uint4 v0 = live_row ? __ldg(src + 2 * c) : make_uint4(0, 0, 0, 0);
-                        const uint4 v1 = live_row ? __ldg(src + 2 * c + 1) : make_uint4(0, 0, 0, 0);
-                        uint32_t r[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    // staged by the group that does not own the piece's last
+                    // pair, with no logits live: the rope half's loads go
+                    // first, then the loads of four TMEM stores (8 columns, 16
+                    // dims, each) are issued before any of them
+                    const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + rope0);
+                    uint4 rv[4];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) r[i] = bf16x2_to_f16x2(r[i]);
-                        tmem_st8(lane_addr + C::kTmemQ + c * 8, r);
+                    for (int c = 0; c < 4; ++c) rv[c] = live_row ? __ldg(rsrc + c) : make_uint4(0, 0, 0, 0);
+                    constexpr int kBatch = 4;
+                    for (int c0 = 0; c0 < 4 * C::kFull; c0 += kBatch) {
+                        uint4 v[2 * kBatch];
+#pragma unroll
+                        for (int i = 0; i < 2 * kBatch; ++i)
+                            v[i] = live_row ? __ldg(src + 2 * c0 + i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int c = 0; c < kBatch; ++c) {
+                            uint32_t r[8] = {v[2 * c].x, v[2 * c].y, v[2 * c].z, v[2 * c].w,
+                                             v[2 * c + 1].x, v[2 * c + 1].y, v[2 * c + 1].z, v[2 * c + 1].w};
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) r[i] = bf16x2_to_f16x2(r[i]);
+                            tmem_st8(lane_addr + C::kTmemQ + (c0 + c) * 8, r);
+                        }
                     }
+                    // the rope half: the K-major operand in shared memory with
+                    // the 64-byte swizzle
+                    uint8_t* row = q_s + h * 64;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4*>(row + ((c ^ ((h >> 1) & 3)) << 4)) =
+                            make_uint4(bf16x2_to_f16x2(rv[c].x), bf16x2_to_f16x2(rv[c].y), bf16x2_to_f16x2(rv[c].z),
+                                       bf16x2_to_f16x2(rv[c].w));
+                    fence_proxy_async_smem();
                 } else {
-                    // the loads of four stores are issued before any of them
-                    // (a TMEM store orders memory); the e4m3 kernel above keeps
-                    // one store's loads at a time, which times faster there
+                    // 8 columns (16 dims) per TMEM store; the loads of four
+                    // stores are issued before any of them (a TMEM store
+                    // orders memory)
                     constexpr int kBatch = 4;
                     for (int c0 = 0; c0 < 4 * C::kFull; c0 += kBatch) {
                         uint4 v[2 * kBatch];
@@ -510,18 +534,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                             tmem_st8(lane_addr + C::kTmemQ + (c0 + c) * 8, r);
                         }
                     }
-                }
-                {
                     // the rank's rope half (32 dims = 64 bytes), the K-major
                     // operand in shared memory with the 64-byte swizzle
                     const uint4* rsrc = reinterpret_cast<const uint4*>(qrow + rope0);
                     uint8_t* row = q_s + h * 64;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        uint4 v = live_row ? __ldg(rsrc + c) : make_uint4(0, 0, 0, 0);
-                        if constexpr (FP8)
-                            v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                                           bf16x2_to_f16x2(v.w));
+                        const uint4 v = live_row ? __ldg(rsrc + c) : make_uint4(0, 0, 0, 0);
                         *reinterpret_cast<uint4*>(row + ((c ^ ((h >> 1) & 3)) << 4)) = v;
                     }
                     fence_proxy_async_smem();
@@ -685,9 +704,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 }
                 tc_fence_before();
                 mbar_arrive(&bars[kSEmpty]);
-                // the piece's last logit pair is in: every Q.K^T that read the
-                // TMEM Q panels has completed, so stage the next piece's Q
-                if (j == npairs - 1) stage_q(it);
+                // bf16 cache: the piece's last logit pair is in, so every
+                // Q.K^T that read the TMEM Q panels has completed: stage the
+                // next piece's Q right away (the e4m3 kernel hands this to the
+                // other group, see the piece epilogue)
+                if (!FP8 && j == npairs - 1) stage_q(it);
                 // ---- send the partial to the peer, receive and add the peer's
                 if (h == 0) mbar_arrive_expect_tx(&bars[kXFull + g], C::kXBytes);
                 if (p >= 2 && !wait_all(&bars[kXFree + g], ((p >> 1) & 1) ^ 1, true)) {
@@ -851,6 +872,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThr
                 lh_s[h] = l_part;
                 mh_s[h] = m_l;
                 mbar_arrive(&bars[kLReady]);
+                // e4m3 cache: stage the next piece's Q once the piece's last
+                // Q.K^T has completed (no Q.K^T reads the TMEM Q panels any
+                // more).  The owner of the last pair is the busier group here
+                // (it widens as well), so this one takes the staging, with no
+                // logits live; in the bf16 kernel the owner staging at once is
+                // faster.  The wait cannot alias: the barrier's next phase
+                // needs a Q.K^T of the next piece, i.e. this staging.
+                if constexpr (FP8) {
+                    if (!wait_all(&bars[kSFull + (plast & 1)], (plast >> 1) & 1, false)) {
+                        ok = false;
+                        widened = gp + npairs;
+                        break;
+                    }
+                    tc_fence_after();
+                    stage_q(it);
+                }
             } else {
                 if (!wait_all(&bars[kLReady], kpiece & 1, false) || !wait_own_pv(plast)) {
                     ok = false;
