@@ -62,12 +62,12 @@ GQA_FILES = ("gqa_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
 NCU_TRAFFIC = {
     "mla_v2lite": {"files": MMA_FILES, "src_sha": "768b00c4d516d186", "splits": 16, "bytes": 329795840 + 3204864,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64,0,0,0>"},
-    "mla_longctx": {"files": TC_FILES, "src_sha": "18f1a01327eb1fa9", "splits": 256, "bytes": 485161728 + 3965696,
-                    "kernel": "mla_decode_tc_kernel<576,512,0,0,0>"},
-    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "18f1a01327eb1fa9", "splits": 64, "bytes": 1423595264 + 25589248,
+    "mla_longctx": {"files": TC_FILES, "src_sha": "e5b65c697f1f6c69", "splits": 256, "bytes": 484526848 + 3496704,
+                    "kernel": "mla_decode_tc_kernel<576,512,0,0,2>"},
+    "mla_v3_fp8": {"files": TC_FILES, "src_sha": "e5b65c697f1f6c69", "splits": 64, "bytes": 1423863552 + 25623040,
                    "kernel": "mla_decode_tc_kernel<576,512,1,0,0>"},
-    "mla_mtp": {"files": TC_FILES, "src_sha": "18f1a01327eb1fa9", "splits": 16, "bytes": 362871552 + 7255552,
-                "kernel": "mla_decode_tc_kernel<576,512,0,1,0>"},
+    "mla_mtp": {"files": TC_FILES, "src_sha": "e5b65c697f1f6c69", "splits": 16, "bytes": 362287360 + 6680320,
+                "kernel": "mla_decode_tc_kernel<576,512,0,1,2>"},
     "gqa": {"files": GQA_FILES, "src_sha": "b0fc4fa9309adfaf", "splits": 32, "bytes": 3241168896 + 4567808,
             "kernel": "gqa_decode_mma_kernel<128>"},
     "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "de9d3c10083698de", "splits": 32, "bytes": 1535305728 + 5585152,

@@ -52,6 +52,14 @@ size_t partial_bytes(int batch, int heads, int width, int splits) {
     return static_cast<size_t>(batch) * heads * splits * (static_cast<size_t>(width) + 1) * 4;
 }
 
+// Pages that a request start costs a unit in the balanced plan of the bf16
+// H > 32 tensor-core kernel: 512 tokens' worth, the best of 256, 512 and 1024
+// on the long-context and multi-token batches.  (A new request costs that
+// kernel its query staging behind the last Q.K^T of the previous one and a
+// pipeline fill.  The e4m3 kernel stages the query on its idle group and is
+// faster with plain page balance.)
+int tc_piece_cost(int page_size) { return (512 + page_size - 1) / page_size; }
+
 // Work units for balanced mode: about `resident` thread blocks per head
 // group, never more than the workspace's partial budget allows.
 int balanced_units(int batch, int splits, int resident_per_group) {
@@ -356,6 +364,8 @@ static mqa_status mla_decode_rows(const void* q, const void* kv_cache, const int
         t.plan.max_blocks = max_blocks;
         t.plan.per_seq = num_kv_splits == 1 ? 1 : 0;
         t.plan.fixed_splits = fixed ? num_kv_splits : 0;
+        // bf16 cache: balanced units also charge every request start
+        t.plan.piece_cost = (t.plan.per_seq || fixed || fp8) ? 0 : tc_piece_cost(page_size);
         t.plan.units = t.plan.per_seq ? batch
                        : fixed        ? batch * num_kv_splits
                                       : balanced_units(batch, num_kv_splits, sms / 2);

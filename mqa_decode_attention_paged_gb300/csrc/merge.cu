@@ -75,6 +75,11 @@ __global__ void __launch_bounds__(32 * kMergeWarps, G == 4 ? 6 : 1) lse_merge_ke
         np = (n_b + L - 1) / L;
         slot0 = b * S;
     } else if (n_b > 0) {
+        // balanced mode: a page's position is its page index plus piece_cost
+        // per request up to and including its own (0: plain page balance)
+        const int c = a.plan.piece_cost;
+        total += c * a.plan.batch;
+        before += c * (b + 1);
         gf = unit_of_page(a.plan.units, total, before);
         const int gl = unit_of_page(a.plan.units, total, before + n_b - 1);
         if (gf == gl) return;  // one unit covered the request and wrote it directly

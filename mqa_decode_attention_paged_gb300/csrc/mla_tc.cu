@@ -149,14 +149,18 @@ __device__ __forceinline__ void issue_qk(uint32_t d, uint32_t q_tmem, uint64_t k
 }
 
 // MULTI: multi-token decode (per-row key limits); the plain-decode kernels
-// are compiled without that code.  FIXED: fixed-split mode (one unit per
-// request and range), separate instantiations so that the page-balanced
-// kernels keep their code.
-template <int D, int R, bool FP8, bool MULTI, bool FIXED>
+// are compiled without that code.  MODE: the work plan's iterator, 0 for
+// page-balanced units (PieceIter, which per-request mode also takes), 1 for
+// the fixed-split mode (one unit per request and range), 2 for units
+// balanced on pages plus a cost per request start (CostPieceIter); separate
+// instantiations, so that each keeps its own code.
+enum TcPlanMode { kModeBalanced = 0, kModeFixed = 1, kModeCost = 2 };
+template <int D, int R, bool FP8, bool MULTI, int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MlaTcCfg<D, R>::kThreads, 1)
     mla_decode_tc_kernel(const __grid_constant__ MlaTcArgs a) {
     using C = MlaTcCfg<D, R>;
-    using PIter = std::conditional_t<FIXED, FixedPieceIter, PieceIter>;
+    using PIter = std::conditional_t<MODE == kModeFixed, FixedPieceIter,
+                                     std::conditional_t<MODE == kModeCost, CostPieceIter, PieceIter>>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     uint8_t* q_s = smem + C::kOffQ;
@@ -960,9 +964,15 @@ template <int D, int R, bool FP8>
 static cudaError_t launch_mla_tc(const MlaTcArgs& a, int clusters, cudaStream_t stream) {
     using C = MlaTcCfg<D, R>;
     const size_t smem = C::smem_bytes(a.plan.batch);
-    auto kern = a.q_len > 1            ? mla_decode_tc_kernel<D, R, FP8, true, false>
-                : a.plan.fixed_splits ? mla_decode_tc_kernel<D, R, FP8, false, true>
-                                      : mla_decode_tc_kernel<D, R, FP8, false, false>;
+    // the cost-balanced plan serves the bf16 kernel only (the host sets no
+    // piece cost for an e4m3 cache), so no e4m3 kernel is built with it
+    constexpr int kCostMode = FP8 ? kModeBalanced : kModeCost;
+    const bool cost = a.plan.piece_cost > 0 && !a.plan.per_seq;
+    auto kern = a.q_len > 1 ? (cost ? mla_decode_tc_kernel<D, R, FP8, true, kCostMode>
+                                    : mla_decode_tc_kernel<D, R, FP8, true, kModeBalanced>)
+                : a.plan.fixed_splits ? mla_decode_tc_kernel<D, R, FP8, false, kModeFixed>
+                : cost                ? mla_decode_tc_kernel<D, R, FP8, false, kCostMode>
+                                      : mla_decode_tc_kernel<D, R, FP8, false, kModeBalanced>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -40,6 +40,7 @@ struct Plan {
     int per_seq;
     int fixed_len;     // > 0: every request has this length (sparse decode: its index list)
     int fixed_splits;  // >= 2: fixed-split mode with this many ranges per request, else 0
+    int piece_cost;    // balanced mode through CostPieceIter: pages charged per request start
 };
 
 // The length the plan gives request b: fixed_len, or its clamped seq_len.
@@ -169,6 +170,55 @@ struct PieceIter {
         pc.slot = g + b;
         p = end;
         return true;
+    }
+};
+
+// Balanced mode in which every request also costs c = piece_cost pages for
+// its start (a new request costs its units a query staging and a pipeline
+// fill): request b spans the positions [cum[b] + c b, cum[b + 1] + c (b + 1)),
+// its pages the last cum[b + 1] - cum[b] of them, and unit g takes the
+// positions [g CT / units, (g + 1) CT / units), CT = T + c B.  A unit then
+// holds fewer pages the more requests it starts.  Pieces, whole-request flags
+// and slots (g + b along the same staircase) are as in PieceIter, which this
+// is with c = 0; the merge maps pages to units by the same positions.
+struct CostPieceIter {
+    int g, B, c, x0, x1, b;
+
+    __device__ __forceinline__ void init(const Plan& plan, const int* cum, int T, int unit) {
+        g = unit;
+        B = plan.batch;
+        c = plan.piece_cost;
+        const long long CT = T + static_cast<long long>(c) * B;
+        x0 = static_cast<int>(static_cast<long long>(unit) * CT / plan.units);
+        x1 = static_cast<int>(static_cast<long long>(unit + 1) * CT / plan.units);
+        int lo = 0, hi = B - 1;  // the last request starting at or before x0
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (cum[mid] + c * mid <= x0)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        b = lo;
+    }
+
+    __device__ __forceinline__ bool next(const int* cum, Piece& pc) {
+        while (b < B && cum[b] + c * b < x1) {
+            const int first = cum[b] + c * (b + 1);  // position of the request's page 0
+            const int np = cum[b + 1] - cum[b];
+            const int j0 = max(x0 - first, 0);
+            const int j1 = min(x1 - first, np);
+            const int bb = b++;
+            if (j1 > j0) {
+                pc.b = bb;
+                pc.j0 = j0;
+                pc.j1 = j1;
+                pc.whole = (j0 == 0 && j1 == np) ? 1 : 0;
+                pc.slot = g + bb;
+                return true;
+            }
+        }
+        return false;
     }
 };
 
