@@ -60,7 +60,7 @@ Q8_FILES = ("gqa_q8.cu", "gqa_q8.cuh", "common.cuh", "plan.cuh", "args.cuh")
 MERGE_FILES = ("shard_merge.cu", "shard_merge.cuh", "common.cuh")
 GQA_FILES = ("gqa_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
 NCU_TRAFFIC = {
-    "mla_v2lite": {"files": MMA_FILES, "src_sha": "768b00c4d516d186", "splits": 16, "bytes": 329795840 + 3204864,
+    "mla_v2lite": {"files": MMA_FILES, "src_sha": "901398989d61db2d", "splits": 16, "bytes": 329796864 + 3698432,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64,0,0,0>"},
     "mla_longctx": {"files": TC_FILES, "src_sha": "e5b65c697f1f6c69", "splits": 256, "bytes": 484526848 + 3496704,
                     "kernel": "mla_decode_tc_kernel<576,512,0,0,2>"},
@@ -68,17 +68,17 @@ NCU_TRAFFIC = {
                    "kernel": "mla_decode_tc_kernel<576,512,1,0,0>"},
     "mla_mtp": {"files": TC_FILES, "src_sha": "e5b65c697f1f6c69", "splits": 16, "bytes": 362287360 + 6680320,
                 "kernel": "mla_decode_tc_kernel<576,512,0,1,2>"},
-    "gqa": {"files": GQA_FILES, "src_sha": "b0fc4fa9309adfaf", "splits": 32, "bytes": 3241168896 + 4567808,
+    "gqa": {"files": GQA_FILES, "src_sha": "5279abc033f1ca5a", "splits": 32, "bytes": 3241169152 + 4573696,
             "kernel": "gqa_decode_mma_kernel<128>"},
-    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "de9d3c10083698de", "splits": 32, "bytes": 1535305728 + 5585152,
+    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "579cbb1cf7ae770f", "splits": 32, "bytes": 1535302144 + 5715712,
                     "kernel": "gqa_decode_q8_kernel<128,2,1>"},
-    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "de9d3c10083698de", "splits": 32, "bytes": 1689827840 + 5622272,
+    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "579cbb1cf7ae770f", "splits": 32, "bytes": 1689870592 + 5828864,
                      "kernel": "gqa_decode_q8_kernel<128,3,1>"},
-    "gqa_int4_pth": {"files": Q8_FILES, "src_sha": "de9d3c10083698de", "splits": 32, "bytes": 843228672 + 5700096,
+    "gqa_int4_pth": {"files": Q8_FILES, "src_sha": "579cbb1cf7ae770f", "splits": 32, "bytes": 843483392 + 5781760,
                      "kernel": "gqa_decode_q8_kernel<128,4,1>"},
     "dcp_merge_v3": {"files": MERGE_FILES, "src_sha": "8c157f962d4da4f4", "bytes": 126340608 + 7121920,
                      "kernel": "shard_merge_kernel"},
-    "mla_sparse": {"files": MMA_FILES, "src_sha": "768b00c4d516d186", "splits": 4, "bytes": 152899328 + 3346688,
+    "mla_sparse": {"files": MMA_FILES, "src_sha": "901398989d61db2d", "splits": 4, "bytes": 152899584 + 3334656,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64,0,1,0>"},
 }
 
