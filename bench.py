@@ -59,8 +59,9 @@ TC_FILES = ("mla_tc.cu", "tc_ptx.cuh", "common.cuh", "plan.cuh", "args.cuh")
 Q8_FILES = ("gqa_q8.cu", "gqa_q8.cuh", "common.cuh", "plan.cuh", "args.cuh")
 MERGE_FILES = ("shard_merge.cu", "shard_merge.cuh", "common.cuh")
 GQA_FILES = ("gqa_mma.cu", "common.cuh", "plan.cuh", "args.cuh")
+SPARSE_FILES = MMA_FILES + ("api.cu",)  # the gather's tensor map is encoded there
 NCU_TRAFFIC = {
-    "mla_v2lite": {"files": MMA_FILES, "src_sha": "901398989d61db2d", "splits": 16, "bytes": 329796864 + 3698432,
+    "mla_v2lite": {"files": MMA_FILES, "src_sha": "0a3a858fdff4ea58", "splits": 16, "bytes": 329795328 + 3672832,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64,0,0,0>"},
     "mla_longctx": {"files": TC_FILES, "src_sha": "e5b65c697f1f6c69", "splits": 256, "bytes": 484526848 + 3496704,
                     "kernel": "mla_decode_tc_kernel<576,512,0,0,2>"},
@@ -78,7 +79,7 @@ NCU_TRAFFIC = {
                      "kernel": "gqa_decode_q8_kernel<128,4,1>"},
     "dcp_merge_v3": {"files": MERGE_FILES, "src_sha": "8c157f962d4da4f4", "bytes": 126340608 + 7121920,
                      "kernel": "shard_merge_kernel"},
-    "mla_sparse": {"files": MMA_FILES, "src_sha": "901398989d61db2d", "splits": 4, "bytes": 152899584 + 3334656,
+    "mla_sparse": {"files": SPARSE_FILES, "src_sha": "4949d7ed343be6ee", "splits": 4, "bytes": 152941056 + 3016192,
                    "kernel": "mla_decode_mma_kernel<576,512,0,64,0,1,0>"},
 }
 

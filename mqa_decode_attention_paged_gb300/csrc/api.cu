@@ -238,6 +238,31 @@ bool rope_half_map(CUtensorMap* out, const void* base, int cols, long long rows,
     return true;
 }
 
+// 2D view {row_bytes / 8, rows} of the cache as 8-byte elements, unswizzled,
+// with a box one row high and box_elems wide, for four-row gathers: a box
+// wider than the row is filled with zeros past it (bf16 sparse decode pads
+// its staged rows that way).
+bool gather_row_map(CUtensorMap* out, const void* base, int row_bytes, long long rows, int box_elems) {
+    const MapKey key{base, rows, row_bytes, box_elems, 8};
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    if (map_lookup(key, out)) return true;
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof m);
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / 8), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_elems), 1};
+    const cuuint32_t elem[2] = {1, 1};
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, const_cast<void*>(base), dims, strides, box, elem,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    map_store(key, m);
+    *out = m;
+    return true;
+}
+
 // Encodes (or returns a cached copy of) a 3D view of a row-major MLA cache
 // [rows, cols] whose box is `box_rows` whole rows: bf16 rows are viewed as
 // {64 elements, cols/64 panels, rows} with the 128-byte swizzle, e4m3 rows as
@@ -580,6 +605,11 @@ mqa_status mla_decode_sparse(const void* q, const void* kv_cache, const int32_t*
     a.heads = num_heads;
     a.withhold = -1;
     a.num_blocks = num_blocks;
+    // four-row gathers of whole rows; bf16 rows get 32 bytes of zero fill
+    const int row_bytes = head_size * (fp8 ? 1 : 2);
+    if (!gather_row_map(&a.tmap, kv_cache, row_bytes, static_cast<long long>(num_blocks) * page_size,
+                        (row_bytes + (fp8 ? 0 : 32)) / 8))
+        return MQA_ERR_CUDA;
     const int tile = mqa::mla_mma_sparse_tile(fp8);
     a.plan.batch = batch;
     a.plan.page = tile;

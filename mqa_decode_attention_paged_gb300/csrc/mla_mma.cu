@@ -6,8 +6,9 @@
 // the next tile's block ids while it waits for a free stage) and stages
 // kTile-token tiles of latent rows [kv_c | k_pe] into shared memory: one 3D
 // tensor copy per box of whole rows of a page (128-byte swizzle), or, for
-// sparse decode, one bulk copy per selected row.  Rows past the sequence end
-// (or unselected) are masked and their V columns zeroed by the consumers.
+// sparse decode, one four-row gather per four selected rows.  Rows past the
+// sequence end (or unselected) are masked and their V columns zeroed by the
+// consumers.
 // The same staged tile serves as K (all D columns) and V (first R columns),
 // the MQA view of MLA ("Triton と MLA" page, vllm-arch-zh
 // ja/attention/triton-mla, section データフロー).
@@ -31,18 +32,35 @@
 
 namespace mqa {
 
+// Four-row gather of a 2D tensor (box one row high) into shared memory: rows
+// y0 .. y3, columns x .. x + box - 1 each, landing back to back; completes its
+// bytes (four boxes, out-of-range fill included) on `bar`.  x must be a
+// multiple of 16 bytes' worth of elements; dst 128-byte aligned.
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int x, int y0, int y1, int y2, int y3,
+                                            uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // Shared-memory budget: everything but the staging ring is fixed, the ring
 // gets as many stages as fit (at most 8).
 
-// SPARSE: the stage is filled by per-row bulk copies.  bf16 rows land in rows
-// padded by 16 bytes (eight consecutive rows then start on eight different
-// bank groups, so ldmatrix reads them without conflicts) and the consumers
-// use the stage directly; e4m3 rows land dense and are widened into the
-// swizzled operand tile as for the dense e4m3 path.
+// SPARSE: the stage is filled by four-row gathers (`tile::gather4` tensor
+// copies of whole rows seen as 8-byte elements), one per group of four
+// consecutive tile rows.  A group lands its rows back to back at a 128-byte
+// aligned place.  bf16 rows are padded to D * 2 + 32 bytes by the copy's own
+// out-of-range fill, the data at the start of the row in even groups and 16
+// bytes in (the box starts at element -2) in odd ones: the eight rows of two
+// groups then start on eight different 16-byte bank groups, so ldmatrix
+// reads them in place without conflicts.  e4m3 rows land dense and are
+// widened into the swizzled operand tile as for the dense e4m3 path.
 template <int D, int R, bool FP8, int TILE, bool SPARSE = false>
 struct MlaMmaCfg {
     static constexpr bool kStaged = FP8;                       // operand tile built from the stage
-    static constexpr bool kPadRows = SPARSE && !FP8;           // stage rows padded by 16 bytes
+    static constexpr bool kPadRows = SPARSE && !FP8;           // stage rows padded by 32 bytes
     static constexpr int kHeads = 16;
     static constexpr int kTile = TILE;                         // tokens per stage
     static constexpr int kHalf = kTile / 2;                    // tokens per QK warp
@@ -52,7 +70,8 @@ struct MlaMmaCfg {
     static constexpr int kThreads = kConsumers + 32;
     static constexpr int kPanels = D / 64;                     // 64-column bf16 panels
     static constexpr int kOpBytes = kPanels * kTile * 128;     // swizzled bf16 operand tile
-    static constexpr int kRowStride = kPadRows ? D * 2 + 16 : D * (FP8 ? 1 : 2);  // bytes per staged row
+    static constexpr int kRowStride = kPadRows ? D * 2 + 32 : D * (FP8 ? 1 : 2);  // bytes per staged row
+    static constexpr int kGroupBytes = 4 * kRowStride;         // one four-row gather (SPARSE)
     static constexpr int kStageBytes = kTile * kRowStride;     // whole cache rows
     static constexpr int kKSteps = D / 16;
     static constexpr int kKq = kKSteps / 4;                    // k-steps per head-dim quarter
@@ -72,11 +91,13 @@ struct MlaMmaCfg {
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
 
     // Byte offset of bf16 element (row, col) of the tile the consumers read:
-    // padded rows for the bf16 gather, else whole rows in the 128-byte
-    // swizzled layout of the tensor copies (or of the widened operand tile).
+    // padded rows of four-row groups for the bf16 gather, else whole rows in
+    // the 128-byte swizzled layout of the tensor copies (or of the widened
+    // operand tile).
     __device__ __forceinline__ static uint32_t op_addr(int row, int col) {
         if constexpr (kPadRows)
-            return static_cast<uint32_t>(row * kRowStride + col * 2);
+            return static_cast<uint32_t>((row >> 2) * kGroupBytes + (row & 3) * kRowStride + ((row >> 2) & 1) * 16 +
+                                         col * 2);
         else
             return swz_rows(row, col, kPanels);
     }
@@ -100,7 +121,9 @@ struct MlaMmaCfg {
     static_assert(kStages >= 2, "at least two pipeline stages");
     static_assert(D % 64 == 0 && kKSteps % 4 == 0, "head size must split into 4 quarters");
     static_assert(kColsPerWarp % 16 == 0, "P.V columns per warp must be a multiple of 16");
-    static_assert(kStageBytes % (kPadRows ? 16 : 1024) == 0, "stages stay aligned for their copies");
+    static_assert(kStageBytes % (SPARSE ? 128 : 1024) == 0, "stages stay aligned for their copies");
+    static_assert(!SPARSE || (kGroupBytes % 128 == 0 && kTile % 4 == 0), "gathered groups stay 128-byte aligned");
+    static_assert(!kPadRows || (kRowStride % 128 == 32), "padded rows: groups of four fill bank groups 0, 2, 4, 6");
     static_assert(kPanels % 2 == 1, "odd panel count keeps ldmatrix conflict free");
     static_assert(1024 + kOffCum + 4 * (2 * kMaxBatchSmem + 1) <= 227 * 1024, "shared memory budget");
 };
@@ -142,7 +165,7 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
         }
         *abort_s = 0;
         fence_mbar_init();
-        if constexpr (!SPARSE) prefetch_tmap(&a.tmap);
+        prefetch_tmap(&a.tmap);
     }
     // Zero the staging ring (and the widened operand tile) once so that rows
     // never written by a copy hold finite values.
@@ -161,18 +184,23 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
         const uint64_t pol = l2_policy_evict_first();
         if constexpr (SPARSE) {
             // Sparse decode: a tile is kTile entries of the request's index
-            // list; lane l gathers rows l, l + 32, each whole cache row by one
-            // bulk copy (rows are D * elt bytes: 16-byte aligned) into the
-            // stage (bf16: rows padded by 16 bytes, read in place; e4m3:
-            // dense rows, widened by the consumers).  The two dependent lookups of a row (its
+            // list; lane l looks up entries l, l + 32 and lane g < kTile / 4
+            // gathers rows 4g .. 4g + 3 by one four-row tensor copy into the
+            // stage (bf16: padded rows, read in place; e4m3: dense rows,
+            // widened by the consumers).  The two dependent lookups of a row (its
             // index entry, then its block id) are spread over the two tiles
             // before its own: in the turn of tile i the producer reads the
-            // entries of tile i + 2, the block ids of tile i + 1 and copies
-            // tile i, so no read waits on another within one turn.  Entries
-            // outside [0, seq_len) select nothing; bad block ids are reported.
+            // block ids of tile i + 1 and the entries of tile i + 2, then
+            // waits for the stage and copies tile i, so no read waits on
+            // another within one turn and both are in flight during the wait.
+            // Entries outside [0, seq_len) select nothing; bad block ids are
+            // reported.
             static_assert(C::kTile % 32 == 0, "whole warps of rows");
             constexpr int kPer = C::kTile / 32;
-            constexpr int kRowBytes = D * (FP8 ? 1 : 2);
+            constexpr int kGroups = C::kTile / 4;
+            // look-ahead in tiles of the index-entry and block-id reads
+            constexpr int kAheadE = 2, kAheadB = 1;
+            static_assert(kGroups <= 32, "one four-row group per lane");
             const long long cap = static_cast<long long>(a.bt_stride) * a.cache_page;
             struct Look {
                 int b, n;        // request and its length (seq_lens[b])
@@ -213,22 +241,29 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
             uint32_t phase = 0;
             int issued[C::kStages];
             for (int s = 0; s < C::kStages; ++s) issued[s] = -1;
-            Look L0, L1, L2;
-            bool h0 = unit != a.withhold && cur.next(a.plan, cum, lens, a.block_table);  // test hook
-            if (h0) read_entries(cur, L0);
-            bool h1 = h0 && cur.next(a.plan, cum, lens, a.block_table);
-            if (h1) read_entries(cur, L1);
-            if (h0) read_blocks(L0);
-            bool h2 = h1 && cur.next(a.plan, cum, lens, a.block_table);
-            if (h2) read_entries(cur, L2);
-            while (h0) {
-                if (h1) read_blocks(L1);
+            Look L[kAheadE + 1];
+            bool h[kAheadE + 1];
+            bool more = unit != a.withhold;  // test hook
+#pragma unroll
+            for (int j = 0; j < kAheadE; ++j) {
+                h[j] = more && cur.next(a.plan, cum, lens, a.block_table);
+                more = h[j];
+                if (h[j]) read_entries(cur, L[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < kAheadB; ++j)
+                if (h[j]) read_blocks(L[j]);
+            while (h[0]) {
+                if (h[kAheadB]) read_blocks(L[kAheadB]);
+                h[kAheadE] = h[kAheadE - 1] && cur.next(a.plan, cum, lens, a.block_table);
+                if (h[kAheadE]) read_entries(cur, L[kAheadE]);
+                Look& L0 = L[0];
                 if (!mbar_wait(&empty[stage], phase ^ 1)) {
                     report(a.status, MQA_ERR_DEVICE_TIMEOUT);
                     break;
                 }
                 uint8_t* dst = stages + stage * C::kStageBytes;
-                const uint8_t* src[kPer];
+                int row[kPer];  // the entry's row in the {D * elt / 8, num_blocks * page} view
 #pragma unroll
                 for (int k = 0; k < kPer; ++k) {
                     bool v = L0.val[k];
@@ -237,33 +272,54 @@ __global__ void __launch_bounds__(MlaMmaCfg<D, R, FP8, TILE, SPARSE>::kThreads, 
                         v = false;
                     }
                     L0.val[k] = v;
-                    src[k] = a.kv + (static_cast<long long>(v ? L0.blk[k] : 0) * a.cache_page +
-                                     (v ? L0.pos[k] % a.cache_page : 0)) * kRowBytes;
+                    row[k] = v ? L0.blk[k] * a.cache_page + L0.pos[k] % a.cache_page : 0;
                 }
                 uint64_t vmask = 0;
 #pragma unroll
                 for (int k = 0; k < kPer; ++k)
                     vmask |= static_cast<uint64_t>(__ballot_sync(0xffffffffu, L0.val[k])) << (32 * k);
+                // group `lane`: rows 4 lane .. 4 lane + 3, from the lanes
+                // holding those entries; an unselected row repeats a selected
+                // one of its group (masked by the consumers), and a group with
+                // none is not copied
+                int y[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int e = (4 * lane + i) & (C::kTile - 1);
+                    int r = 0;
+#pragma unroll
+                    for (int k = 0; k < kPer; ++k) {
+                        const int rk = __shfl_sync(0xffffffffu, row[k], e & 31);
+                        if ((e >> 5) == k) r = rk;
+                    }
+                    y[i] = r;
+                }
+                const uint32_t gbits = lane < kGroups ? static_cast<uint32_t>(vmask >> (4 * lane)) & 0xfu : 0u;
+                const int yf = (gbits & 1u) ? y[0] : (gbits & 2u) ? y[1] : (gbits & 4u) ? y[2] : y[3];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (!((gbits >> i) & 1u)) y[i] = yf;
+                const uint32_t gm = __ballot_sync(0xffffffffu, gbits != 0u);
                 if (lane == 0) {
                     mask_s[stage] = vmask;
-                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(__popcll(vmask)) * kRowBytes);
+                    mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(__popc(gm)) * C::kGroupBytes);
                 }
                 __syncwarp();
-#pragma unroll
-                for (int k = 0; k < kPer; ++k)
-                    if (L0.val[k])
-                        bulk_g2s(dst + (lane + 32 * k) * C::kRowStride, src[k], kRowBytes, &full[stage], pol);
+                // bf16: odd groups start their box at element -2, so their
+                // rows' data sits 16 bytes in (see MlaMmaCfg)
+                if (gbits)
+                    tma_gather4(dst + lane * C::kGroupBytes, &a.tmap, (C::kPadRows && (lane & 1)) ? -2 : 0, y[0], y[1],
+                                y[2], y[3], &full[stage], pol);
                 issued[stage] = static_cast<int>(phase);
                 if (++stage == C::kStages) {
                     stage = 0;
                     phase ^= 1;
                 }
-                L0 = L1;
-                L1 = L2;
-                h0 = h1;
-                h1 = h2;
-                h2 = h1 && cur.next(a.plan, cum, lens, a.block_table);
-                if (h2) read_entries(cur, L2);
+#pragma unroll
+                for (int j = 0; j < kAheadE; ++j) {
+                    L[j] = L[j + 1];
+                    h[j] = h[j + 1];
+                }
             }
             for (int s = 0; s < C::kStages; ++s)
                 if (issued[s] >= 0 && !mbar_wait(&full[s], static_cast<uint32_t>(issued[s])))
