@@ -125,15 +125,27 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
 }
 
 // The eight int4 codes of w (nibble i = element i, two's complement) -> four
-// f16 pairs, elements (0, 4), (1, 5), (2, 6), (3, 7), exact: one mask-and-xor
-// per pair (a single LOP3) puts x + 8 = nibble ^ 8 of elements i and i + 4
-// into the mantissas of two f16 1024s (0x6400), then 1032 is subtracted.
-// The callers absorb the element order (the K operand's reduction order, V's
-// tile columns).
-__device__ __forceinline__ uint4 int4x8_to_f16_pairs(uint32_t w) {
+// f16 pairs, elements (0, 4), (1, 5), (2, 6), (3, 7), exact.  One
+// mask-and-xor per pair (a single LOP3) puts x + 8 = nibble ^ 8 of elements
+// i and i + 4 into the mantissas of two f16 1024s (0x6400): a nibble in bits
+// 0..3 of a half gives 1024 + (x + 8), so 1032 is subtracted; a nibble in
+// bits 4..7 gives 1024 + 16 (x + 8), so the pair is scaled by 1/16 and 72
+// subtracted in one fused step (every value is an integer below 2048: no
+// rounding).  Elements 2, 3, 6 and 7 take the same two steps after one shift
+// by 8.  The callers absorb the element order (the K operand's reduction
+// order, V's tile columns).
+// Elements (0, 4) and (1, 5) of w.
+__device__ __forceinline__ uint2 int4_lo_pairs(uint32_t w) {
     const __half2 k = bits_h2(0x64086408u);
-    auto pair = [&](uint32_t x) { return h2_bits(__hsub2(bits_h2((x & 0x000f000fu) ^ 0x64086408u), k)); };
-    return make_uint4(pair(w), pair(w >> 4), pair(w >> 8), pair(w >> 12));
+    const __half2 s16 = __float2half2_rn(0.0625f), k72 = __float2half2_rn(-72.f);
+    return make_uint2(h2_bits(__hsub2(bits_h2((w & 0x000f000fu) ^ 0x64086408u), k)),
+                      h2_bits(__hfma2(bits_h2((w & 0x00f000f0u) ^ 0x64806480u), s16, k72)));
+}
+// Elements (2, 6) and (3, 7) of w.
+__device__ __forceinline__ uint2 int4_hi_pairs(uint32_t w) { return int4_lo_pairs(w >> 8); }
+__device__ __forceinline__ uint4 int4x8_to_f16_pairs(uint32_t w) {
+    const uint2 lo = int4_lo_pairs(w), hi = int4_hi_pairs(w);
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
 }
 
 // Tile column m (0..7) of an 8-column group of widened int4 V holds element
@@ -419,18 +431,17 @@ __global__ void __launch_bounds__(32 * (GqaQ8Cfg<D, KIND>::kMaxKvHeads + 1), q8_
             for (int hb = 0; hb < NHB; ++hb)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) st[hb][e][0] = st[hb][e][1] = st[hb][e][2] = st[hb][e][3] = 0.f;
-            uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;  // int4: one word of codes per two steps
+            uint32_t w0 = 0u, w1 = 0u;  // int4: one word of codes per two steps
 #pragma unroll
             for (int ks = 0; ks < C::kKSteps; ++ks) {
                 uint2 k0, k1;
                 if constexpr (KIND == kFmtInt4Pth) {  // 8 elements = 4 bytes per two steps
                     if ((ks & 1) == 0) {
-                        w0 = int4x8_to_f16_pairs(*reinterpret_cast<const uint32_t*>(kb + g * rstride + ks * 8 + 4 * c));
-                        w1 = int4x8_to_f16_pairs(
-                            *reinterpret_cast<const uint32_t*>(kb + (g + 8) * rstride + ks * 8 + 4 * c));
+                        w0 = *reinterpret_cast<const uint32_t*>(kb + g * rstride + ks * 8 + 4 * c);
+                        w1 = *reinterpret_cast<const uint32_t*>(kb + (g + 8) * rstride + ks * 8 + 4 * c);
                     }
-                    k0 = (ks & 1) ? make_uint2(w0.z, w0.w) : make_uint2(w0.x, w0.y);
-                    k1 = (ks & 1) ? make_uint2(w1.z, w1.w) : make_uint2(w1.x, w1.y);
+                    k0 = (ks & 1) ? int4_hi_pairs(w0) : int4_lo_pairs(w0);
+                    k1 = (ks & 1) ? int4_hi_pairs(w1) : int4_lo_pairs(w1);
                 } else {
                     k0 = widen4<KIND>(*reinterpret_cast<const uint32_t*>(kb + g * rstride + ks * 16 + 4 * c));
                     k1 = widen4<KIND>(*reinterpret_cast<const uint32_t*>(kb + (g + 8) * rstride + ks * 16 + 4 * c));
