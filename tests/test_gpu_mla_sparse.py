@@ -57,6 +57,18 @@ def test_sparse_parity(H, kv_dtype, page, splits, topk):
     check(case, idx, splits, f"sparse H={H} {kv_dtype} P={page} S={splits} topk={topk}")
 
 
+@pytest.mark.parametrize("H", [16, 128])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_sparse_parity_head_320(H, kv_dtype):
+    # head 320 (kv_lora_rank 256): a row is 640 (bf16) or 320 (e4m3) bytes,
+    # so the four-row gathers take boxes of 84 or 40 eight-byte elements
+    case = synth.poison(synth.make_mla_case(RAGGED, H=H, D=320, page=16, kv_dtype=kv_dtype, k_scale=0.05,
+                                            pool_factor=1.2, seed=63))
+    idx = synth.draw_topk_indices(np.random.default_rng(64), case.seq_lens, 300, pad=0.2)
+    for splits in (1, 3):
+        check(case, idx, splits, f"sparse D=320 H={H} {kv_dtype} S={splits}")
+
+
 def test_out_of_range_and_duplicate_entries():
     case = synth.poison(synth.make_mla_case([90, 200, 5], H=16, page=16, seed=63))
     idx = synth.draw_topk_indices(np.random.default_rng(64), case.seq_lens, 64)
