@@ -71,11 +71,11 @@ NCU_TRAFFIC = {
                 "kernel": "mla_decode_tc_kernel<576,512,0,1,2>"},
     "gqa": {"files": GQA_FILES, "src_sha": "5279abc033f1ca5a", "splits": 32, "bytes": 3241169152 + 4573696,
             "kernel": "gqa_decode_mma_kernel<128>"},
-    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "01e8905810e3ac99", "splits": 32, "bytes": 1535297280 + 5267712,
+    "gqa_fp8_pth": {"files": Q8_FILES, "src_sha": "dba3282edc657b61", "splits": 32, "bytes": 1535350272 + 5330944,
                     "kernel": "gqa_decode_q8_kernel<128,2,1>"},
-    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "01e8905810e3ac99", "splits": 32, "bytes": 1689841664 + 5692160,
+    "gqa_int8_pth": {"files": Q8_FILES, "src_sha": "dba3282edc657b61", "splits": 32, "bytes": 1689822464 + 5506560,
                      "kernel": "gqa_decode_q8_kernel<128,3,1>"},
-    "gqa_int4_pth": {"files": Q8_FILES, "src_sha": "01e8905810e3ac99", "splits": 32, "bytes": 843409152 + 4982528,
+    "gqa_int4_pth": {"files": Q8_FILES, "src_sha": "dba3282edc657b61", "splits": 32, "bytes": 843228416 + 4604160,
                      "kernel": "gqa_decode_q8_kernel<128,4,1>"},
     "dcp_merge_v3": {"files": MERGE_FILES, "src_sha": "8c157f962d4da4f4", "bytes": 126340608 + 7121920,
                      "kernel": "shard_merge_kernel"},

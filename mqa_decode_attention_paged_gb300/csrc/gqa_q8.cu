@@ -172,8 +172,10 @@ __device__ __forceinline__ uint2 widen4(uint32_t w) {
 
 // Widen one KV head's 16 rows of codes (src: the head's first code byte in
 // the plane tile, rows `rbytes` apart) into an f16 tile with row stride
-// kWStride.  Rows of tokens not in vmask become zeros without reading their
-// bytes.
+// kWStride.  e4m3: rows of tokens not in vmask become zeros without reading
+// their bytes (a stale or padding byte may be a NaN code).  int8 and int4:
+// every byte is a finite code, and a masked token's P and V scale are 0, so
+// its row is widened as it stands.
 template <int D, int KIND>
 __device__ __forceinline__ void widen_rows(const uint8_t* src, uint8_t* dst, uint64_t vmask, int rbytes,
                                            int lane) {
@@ -187,8 +189,7 @@ __device__ __forceinline__ void widen_rows(const uint8_t* src, uint8_t* dst, uin
 #pragma unroll
         for (int r0 = 0; r0 < C::kTile; r0 += kRowsPer) {
             const int r = r0 + sub;
-            const bool v = (vmask >> r) & 1ull;
-            const uint32_t w = v ? *reinterpret_cast<const uint32_t*>(src + r * rbytes + 4 * ch) : 0u;  // code 0
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(src + r * rbytes + 4 * ch);
             *reinterpret_cast<uint4*>(dst + r * C::kWStride + 16 * ch) = int4x8_to_f16_pairs(w);
         }
     } else {
@@ -198,7 +199,7 @@ __device__ __forceinline__ void widen_rows(const uint8_t* src, uint8_t* dst, uin
 #pragma unroll
         for (int r0 = 0; r0 < C::kTile; r0 += kRowsPer) {
             const int r = r0 + sub;
-            const bool v = (vmask >> r) & 1ull;
+            const bool v = KIND == kFmtInt8Pth || ((vmask >> r) & 1ull);
             const uint32_t w = v ? *reinterpret_cast<const uint32_t*>(src + r * rbytes + 4 * ch) : 0u;
             *reinterpret_cast<uint2*>(dst + r * C::kWStride + 8 * ch) = widen4<KIND>(w);
         }
